@@ -1,0 +1,354 @@
+/*
+ * csa_oracle.c -- plain, slow, fp64 CPU oracle for the CSA + HCA hybrid
+ * compressed attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or helper with the
+ * CUDA library; both sides only read the same seeded inputs.
+ *
+ * Sources (cited by page title and section):
+ *   [V4]   "DeepSeek-V4 core architecture" (gitcode.csdn.net article),
+ *          §2.2 "CSA: compressed sparse attention" -- step 1 token-level
+ *          compression, step 2 lightning indexer, step 3 shared-KV MQA;
+ *          §2.3 "HCA: heavily compressed attention".
+ *   [DEBT] "DeepSeek V4's architecture debt chain" (vendordeep.com),
+ *          "Constraint 1 -> Innovation 1: CSA+HCA hybrid attention"
+ *          (128x fusion of many tokens' KV into one compressed token).
+ *
+ * Readings where the pages leave a step open (all listed in the design
+ * notes):
+ *   R1  indexer score s(t,j) = sum over indexer heads h of q_{t,h} . k_j
+ *       (one key vector per compressed entry, shared by all heads); no
+ *       ReLU, weight or scale.
+ *   R2  a query also attends to the raw tokens of its own incomplete block.
+ *   R3  a block's entry is visible only once the block is complete:
+ *       entry j (tokens j*m .. j*m+m-1) is visible to position t iff
+ *       (j+1)*m <= t+1.
+ *   A1  blocks are non-overlapping and aligned at position 0.
+ *   A2  one scalar gate logit per token, shared across the d channels;
+ *       the block's weights are the softmax of its tokens' logits.
+ *   A7  top-k order: higher score first, ties to the lower entry index;
+ *       the selected indices are returned ascending, padded with -1.
+ *
+ * Everything is computed in double precision; bf16 and fp32 inputs
+ * convert to double exactly.  Plain loops, no blocking or reordering
+ * beyond the definitions.  OpenMP only splits independent queries/blocks.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 bit pattern -> double (exact: bf16 is the top half of an fp32). */
+static double bf16_to_double(uint16_t h)
+{
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------
+ * Token-level compression ([V4] §2.2 step 1: every m adjacent tokens' KV
+ * become one entry, with learnable softmax-normalised weights; [V4] §2.3 and
+ * [DEBT]: the same weighted fusion with m = 128 for HCA).
+ *
+ * Block j of one sequence holds tokens j*m .. j*m+m-1 (A1).  With the gate
+ * logits z of those tokens (A2):
+ *     w_t = exp(z_t) / sum_{s in block} exp(z_s)
+ *     e_j = sum_{t in block} w_t * c_t
+ * The largest logit is subtracted before exp (same value, no overflow).
+ * ---------------------------------------------------------------------- */
+static void compress_block(const uint16_t *c, const float *z, int d, int m,
+                           int64_t j, double *e)
+{
+    const int64_t t0 = j * (int64_t)m;
+    double zmax = -INFINITY;
+    for (int i = 0; i < m; i++)
+        if ((double)z[t0 + i] > zmax) zmax = (double)z[t0 + i];
+    double denom = 0.0;
+    for (int i = 0; i < m; i++) denom += exp((double)z[t0 + i] - zmax);
+    for (int x = 0; x < d; x++) e[x] = 0.0;
+    for (int i = 0; i < m; i++) {
+        const double w = exp((double)z[t0 + i] - zmax) / denom;
+        const uint16_t *row = c + (t0 + i) * (int64_t)d;
+        for (int x = 0; x < d; x++) e[x] += w * bf16_to_double(row[x]);
+    }
+}
+
+/* All complete blocks of one sequence of n_tok tokens: out[n_tok/m, d].
+ * A trailing partial block gets no entry (R3). */
+int orc_compress(const uint16_t *c, const float *z, int64_t n_tok, int d,
+                 int m, double *out)
+{
+    if (!c || !z || !out || d <= 0 || m <= 0 || n_tok < 0) return 1;
+    const int64_t n_blocks = n_tok / m;
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < n_blocks; j++)
+        compress_block(c, z, d, m, j, out + j * (int64_t)d);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Lightning indexer scores ([V4] §2.2 step 2: a light scorer rates each
+ * query against every compressed entry), in the form R1 fixes:
+ *     s_j = sum_{h < HI} sum_{i < dI} qI[h, i] * kI[j, i]
+ * qI: [HI, dI] one query's indexer heads; kI: [n, dI] one key per entry.
+ * ---------------------------------------------------------------------- */
+int orc_index_scores(const uint16_t *qI, const uint16_t *kI, int64_t n,
+                     int HI, int dI, double *s)
+{
+    if (!qI || (!kI && n > 0) || (!s && n > 0) || HI <= 0 || dI <= 0) return 1;
+    for (int64_t j = 0; j < n; j++) {
+        double acc = 0.0;
+        for (int h = 0; h < HI; h++)
+            for (int i = 0; i < dI; i++)
+                acc += bf16_to_double(qI[h * dI + i]) *
+                       bf16_to_double(kI[j * (int64_t)dI + i]);
+        s[j] = acc;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Top-k ([V4] §2.2 step 2: keep only the k most relevant entries).
+ * Order (A7): score descending, then index ascending.  The first min(k, n)
+ * are returned in ascending index order, the rest of idx[0..k) is -1.
+ * The library sort (qsort) is the selection step.
+ * ---------------------------------------------------------------------- */
+typedef struct { double s; int64_t j; } scored_t;
+
+static int cmp_scored(const void *a, const void *b)
+{
+    const scored_t *x = (const scored_t *)a, *y = (const scored_t *)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    return (x->j < y->j) ? -1 : (x->j > y->j);
+}
+
+static int cmp_i32(const void *a, const void *b)
+{
+    const int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+int orc_topk(const double *s, int64_t n, int k, int32_t *idx)
+{
+    if ((!s && n > 0) || !idx || k <= 0 || n < 0) return 1;
+    scored_t *all = (scored_t *)malloc(sizeof(scored_t) * (size_t)(n > 0 ? n : 1));
+    if (!all) return 2;
+    for (int64_t j = 0; j < n; j++) { all[j].s = s[j]; all[j].j = j; }
+    qsort(all, (size_t)n, sizeof(scored_t), cmp_scored);
+    const int64_t take = n < k ? n : k;
+    for (int64_t i = 0; i < take; i++) idx[i] = (int32_t)all[i].j;
+    qsort(idx, (size_t)take, sizeof(int32_t), cmp_i32);
+    for (int64_t i = take; i < k; i++) idx[i] = -1;
+    free(all);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Multi-query attention with shared KV ([V4] §2.2 step 3: every selected
+ * entry is both Key and Value, and all query heads share the same KV).
+ * q: [H, d] bf16; keys: [nk, d] fp64.  Per head h:
+ *     l_i = scale * q_h . x_i,  p = softmax(l),  o_h = sum_i p_i x_i,
+ *     lse_h = log sum_i exp(l_i)   (natural log)
+ * ---------------------------------------------------------------------- */
+int orc_attend(const uint16_t *q, int H, int d, const double *keys, int64_t nk,
+               double scale, double *o, double *lse)
+{
+    if (!q || !keys || !o || H <= 0 || d <= 0 || nk <= 0) return 1;
+    double *l = (double *)malloc(sizeof(double) * (size_t)nk);
+    if (!l) return 2;
+    for (int h = 0; h < H; h++) {
+        const uint16_t *qh = q + (int64_t)h * d;
+        double lmax = -INFINITY;
+        for (int64_t i = 0; i < nk; i++) {
+            double acc = 0.0;
+            for (int x = 0; x < d; x++)
+                acc += bf16_to_double(qh[x]) * keys[i * (int64_t)d + x];
+            l[i] = scale * acc;
+            if (l[i] > lmax) lmax = l[i];
+        }
+        double denom = 0.0;
+        for (int64_t i = 0; i < nk; i++) denom += exp(l[i] - lmax);
+        double *oh = o + (int64_t)h * d;
+        for (int x = 0; x < d; x++) oh[x] = 0.0;
+        for (int64_t i = 0; i < nk; i++) {
+            const double p = exp(l[i] - lmax) / denom;
+            for (int x = 0; x < d; x++) oh[x] += p * keys[i * (int64_t)d + x];
+        }
+        if (lse) lse[h] = lmax + log(denom);
+    }
+    free(l);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Whole queries of a packed batch.
+ *
+ * Sequence b owns tokens cu_kv[b] .. cu_kv[b+1]-1 (length L_b), CSA entries
+ * cu_csa[b] .. (floor(L_b/mC) of them) and queries cu_q[b] .. cu_q[b+1]-1;
+ * its queries are its last n_q = cu_q[b+1]-cu_q[b] positions.  For a query
+ * at position t (0-based within its sequence):
+ *     n_C = floor((t+1)/mC),  r_C = (t+1) mod mC     (R3, R2)
+ *     n_H = floor((t+1)/mH),  r_H = (t+1) mod mH
+ * CSA ([V4] §2.2): scores over entries j < n_C (R1), top-k (A7), attention
+ *   over the selected entries plus the r_C raw tokens t-r_C+1 .. t.
+ * HCA ([V4] §2.3): attention over all n_H entries plus the r_H raw tokens.
+ *
+ * The CSA entries a query needs are compressed on demand from the raw
+ * tokens; the HCA entries are taken from hca_entries (fp64, from
+ * orc_compress with m = mH, packed by cu_hca).  When given_idx is not NULL
+ * the CSA branch attends over those indices instead of its own top-k (to
+ * check attention on another selection).  Outputs (per evaluated query):
+ * idx[k] int32, oC[H,d], lseC[H], oH[H,d], lseH[H]; any output may be NULL
+ * to skip that branch's output (the CSA branch still needs idx storage
+ * internally).
+ * ---------------------------------------------------------------------- */
+static int64_t find_seq(int B, const int64_t *cu_q, int64_t qi)
+{
+    int64_t lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int64_t mid = (lo + hi + 1) / 2;
+        if (cu_q[mid] <= qi) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+int orc_hybrid_queries(int B, const int64_t *cu_kv, const int64_t *cu_q,
+                       const int64_t *cu_csa, const int64_t *cu_hca,
+                       const uint16_t *kv, const float *gate,
+                       const uint16_t *qI, const uint16_t *kI,
+                       const uint16_t *q, int d, int H, int HI, int dI,
+                       int mC, int mH, int top_k, double scale,
+                       const double *hca_entries, int64_t n_eval,
+                       const int64_t *eval_q, const int32_t *given_idx,
+                       int do_csa, int do_hca,
+                       int32_t *idx_out, double *oC, double *lseC,
+                       double *oH, double *lseH)
+{
+    if (B <= 0 || !cu_kv || !cu_q || !kv || !q || d <= 0 || H <= 0 ||
+        mC <= 0 || mH <= 0 || top_k <= 0 || n_eval < 0 || !eval_q)
+        return 1;
+    if (do_csa && (!cu_csa || !gate || !qI || !kI)) return 1;
+    if (do_hca && (!cu_hca || !hca_entries)) return 1;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t e = 0; e < n_eval; e++) {
+        const int64_t qi = eval_q[e];
+        const int64_t b = find_seq(B, cu_q, qi);
+        const int64_t L = cu_kv[b + 1] - cu_kv[b];
+        const int64_t nq = cu_q[b + 1] - cu_q[b];
+        const int64_t t = L - nq + (qi - cu_q[b]);
+        const uint16_t *c_seq = kv + cu_kv[b] * (int64_t)d;
+        const uint16_t *q_t = q + qi * (int64_t)H * d;
+        if (t < 0 || t >= L) { err |= 1; continue; }
+
+        if (do_csa) {
+            const int64_t nC = (t + 1) / mC, rC = (t + 1) % mC;
+            int32_t *sel = (int32_t *)malloc(sizeof(int32_t) * (size_t)top_k);
+            if (!sel) { err |= 2; continue; }
+            if (given_idx) {
+                memcpy(sel, given_idx + e * (int64_t)top_k, sizeof(int32_t) * (size_t)top_k);
+            } else {
+                double *s = (double *)malloc(sizeof(double) * (size_t)(nC > 0 ? nC : 1));
+                if (!s) { free(sel); err |= 2; continue; }
+                err |= orc_index_scores(qI + qi * (int64_t)HI * dI,
+                                        kI + cu_csa[b] * (int64_t)dI, nC, HI, dI, s);
+                err |= orc_topk(s, nC, top_k, sel);
+                free(s);
+            }
+            if (idx_out) memcpy(idx_out + e * (int64_t)top_k, sel, sizeof(int32_t) * (size_t)top_k);
+            int64_t nsel = 0;
+            for (int i = 0; i < top_k; i++) if (sel[i] >= 0) nsel++;
+            const int64_t nk = nsel + rC;
+            double *keys = (double *)malloc(sizeof(double) * (size_t)nk * d);
+            if (!keys) { free(sel); err |= 2; continue; }
+            int64_t w = 0;
+            for (int i = 0; i < top_k; i++) {
+                if (sel[i] < 0) continue;
+                if (sel[i] >= nC) err |= 4;   /* not visible: invalid selection */
+                else compress_block(c_seq, gate + cu_kv[b], d, mC, sel[i], keys + w * d);
+                w++;
+            }
+            for (int64_t r = 0; r < rC; r++, w++) {
+                const uint16_t *row = c_seq + (t - rC + 1 + r) * (int64_t)d;
+                for (int x = 0; x < d; x++) keys[w * d + x] = bf16_to_double(row[x]);
+            }
+            if (oC)
+                err |= orc_attend(q_t, H, d, keys, nk, scale,
+                                  oC + e * (int64_t)H * d, lseC ? lseC + e * (int64_t)H : NULL);
+            free(keys);
+            free(sel);
+        }
+        if (do_hca) {
+            const int64_t nH = (t + 1) / mH, rH = (t + 1) % mH;
+            const int64_t nk = nH + rH;
+            double *keys = (double *)malloc(sizeof(double) * (size_t)nk * d);
+            if (!keys) { err |= 2; continue; }
+            memcpy(keys, hca_entries + cu_hca[b] * (int64_t)d, sizeof(double) * (size_t)(nH * d));
+            for (int64_t r = 0; r < rH; r++) {
+                const uint16_t *row = c_seq + (t - rH + 1 + r) * (int64_t)d;
+                for (int x = 0; x < d; x++) keys[(nH + r) * d + x] = bf16_to_double(row[x]);
+            }
+            if (oH)
+                err |= orc_attend(q_t, H, d, keys, nk, scale,
+                                  oH + e * (int64_t)H * d, lseH ? lseH + e * (int64_t)H : NULL);
+            free(keys);
+        }
+    }
+    return err;
+}
+
+/* Compress the blocks of every sequence of a packed batch (entries packed
+ * by cu_out, floor(L_b/m) per sequence).  Used to build fp64 HCA entries. */
+int orc_compress_packed(int B, const int64_t *cu_kv, const int64_t *cu_out,
+                        const uint16_t *kv, const float *gate, int d, int m,
+                        double *out)
+{
+    if (B <= 0 || !cu_kv || !cu_out || !kv || !gate || !out) return 1;
+    int err = 0;
+    for (int b = 0; b < B; b++) {
+        const int64_t L = cu_kv[b + 1] - cu_kv[b];
+        if (cu_out[b + 1] - cu_out[b] != L / m) return 3;
+        err |= orc_compress(kv + cu_kv[b] * (int64_t)d, gate + cu_kv[b], L, d, m,
+                            out + cu_out[b] * (int64_t)d);
+    }
+    return err;
+}
+
+/* Compress only the listed blocks (global entry indices into the packed
+ * entry array), for sampled checks at full size. */
+int orc_compress_selected(int B, const int64_t *cu_kv, const int64_t *cu_out,
+                          const uint16_t *kv, const float *gate, int d, int m,
+                          int64_t n_sel, const int64_t *entry, double *out)
+{
+    if (B <= 0 || !cu_kv || !cu_out || !kv || !gate || !out || !entry) return 1;
+    int err = 0;
+#pragma omp parallel for schedule(static) reduction(| : err)
+    for (int64_t i = 0; i < n_sel; i++) {
+        const int64_t g = entry[i];
+        /* the last sequence whose first entry is <= g owns entry g */
+        const int64_t bb = find_seq(B, cu_out, g);
+        const int64_t j = g - cu_out[bb];
+        const int64_t L = cu_kv[bb + 1] - cu_kv[bb];
+        if (j < 0 || (j + 1) * m > L) { err |= 4; continue; }
+        compress_block(kv + cu_kv[bb] * (int64_t)d, gate + cu_kv[bb], d, m, j,
+                       out + i * (int64_t)d);
+    }
+    return err;
+}

@@ -1,0 +1,314 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Each test ties one oracle function to a closed form, a textbook/library
+routine, brute force on a tiny input, or an invariant that the definitions
+of the CSA/HCA path fix (DeepSeek-V4 core architecture, §2.2 CSA steps 1-3
+and §2.3 HCA), so that a dropped term, a wrong sign, an off-by-one in the
+block/visibility arithmetic or a transposed operand fails at least one.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from compressed_sparse_attention_21_b300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf(x):
+    """float array -> bf16 bit patterns (exact when x is bf16-representable)."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return wl.bits(t)
+
+
+def f(bits):
+    """bf16 bit patterns -> float64 values (exact)."""
+    b = np.ascontiguousarray(bits, np.uint16)
+    return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def tiny_problem(L, d=8, H=2, HI=2, dI=4, mC=4, mH=128, k=4, seed=0, n_q=None, gate_std=1.0):
+    w = wl.Workload("tiny", 1, [L], False, H=H, d=d, HI=HI, dI=dI, top_k=k, mC=mC, mH=mH,
+                    gate_std=gate_std, seed=seed)
+    return wl.to_numpy(wl.make_problem(w, n_q=n_q))
+
+
+def sdpa_causal(q_bits, kv_bits, scale):
+    """Dense causal MQA through torch's library routine, fp64 on the CPU.
+
+    q: [L, H, d]; kv: [L, d] shared by all heads (key = value)."""
+    q = torch.from_numpy(f(q_bits)).permute(1, 0, 2)[None]          # [1, H, L, d]
+    kv = torch.from_numpy(f(kv_bits))[None, None].expand(1, q.shape[1], -1, -1)
+    o = torch.nn.functional.scaled_dot_product_attention(q, kv, kv, is_causal=True, scale=scale)
+    return o[0].permute(1, 0, 2).numpy()                             # [L, H, d]
+
+
+# ----------------------------------------------------------------------------
+# compression (§2.2 step 1; §2.3)
+# ----------------------------------------------------------------------------
+
+def test_compress_closed_form_weights(orc):
+    # logits 0, ln2, ln3, ln4 -> weights 1/10, 2/10, 3/10, 4/10 exactly
+    z = np.log(np.array([1.0, 2.0, 3.0, 4.0])).astype(np.float32)
+    c = np.array([[1, -2], [0.5, 4], [-1, 8], [2, 0.25]], np.float32)
+    e = orc.compress(bf(c), z, 4)
+    zf = z.astype(np.float64)
+    w = np.exp(zf) / np.exp(zf).sum()          # the fp32-rounded logits, exactly
+    assert np.allclose(w, [0.1, 0.2, 0.3, 0.4], atol=1e-7)
+    expect = (w[:, None] * c.astype(np.float64)).sum(0)
+    assert np.allclose(e[0], expect, rtol=0, atol=1e-15)
+
+
+def test_compress_uniform_logits_is_mean_pooling(orc):
+    rng = np.random.default_rng(1)
+    L, d, m = 64, 16, 4
+    c = bf(rng.standard_normal((L, d)))
+    z = np.repeat(rng.standard_normal(L // m), m).astype(np.float32)   # constant per block
+    e = orc.compress(c, z, m)
+    mean = f(c).reshape(L // m, m, d).mean(1)
+    assert np.allclose(e, mean, rtol=0, atol=1e-14)
+
+
+def test_compress_block_alignment_and_trailing_block(orc):
+    # c_t = t in every channel, uniform logits: entry j = mean(4j .. 4j+3) = 4j + 1.5
+    L, d = 10, 3
+    c = bf(np.repeat(np.arange(L, dtype=np.float32)[:, None], d, 1))
+    e = orc.compress(c, np.zeros(L, np.float32), 4)
+    assert e.shape == (2, d)                         # tokens 8, 9 form no entry
+    assert np.array_equal(e[:, 0], [1.5, 5.5])
+
+
+def test_compress_invariances(orc):
+    rng = np.random.default_rng(2)
+    L, d, m = 32, 8, 4
+    c = bf(rng.standard_normal((L, d)))
+    z = rng.standard_normal(L).astype(np.float32)
+    e = orc.compress(c, z, m)
+    # shift all logits of a block by a constant (exactly representable shift)
+    e2 = orc.compress(c, (z + np.float32(3.0)).astype(np.float32), m)
+    assert np.allclose(e, e2, atol=1e-12)
+    # permute (c, z) pairs inside each block
+    perm = np.concatenate([j * m + rng.permutation(m) for j in range(L // m)])
+    e3 = orc.compress(c[perm], z[perm], m)
+    assert np.allclose(e, e3, atol=1e-14)
+
+
+def test_compress_dominant_logit_and_ratio_one(orc):
+    rng = np.random.default_rng(3)
+    L, d = 8, 5
+    c = bf(rng.standard_normal((L, d)))
+    z = np.zeros(L, np.float32)
+    z[2] = 50.0
+    z[5] = 50.0
+    e = orc.compress(c, z, 4)
+    # the other weights are exp(-50) ~ 2e-22
+    assert np.allclose(e[0], f(c)[2], rtol=0, atol=1e-19)
+    assert np.allclose(e[1], f(c)[5], rtol=0, atol=1e-19)
+    assert np.array_equal(orc.compress(c, rng.standard_normal(L).astype(np.float32), 1), f(c))
+
+
+def test_compress_hca_ratio(orc):
+    rng = np.random.default_rng(4)
+    L, d = 300, 4
+    c = bf(rng.standard_normal((L, d)))
+    z = rng.standard_normal(L).astype(np.float32)
+    e = orc.compress(c, z, 128)
+    assert e.shape == (2, d)
+    # brute force for block 1, straight from the definition in plain Python
+    zs = [float(v) for v in z[128:256]]
+    mx = max(zs)
+    ws = [math.exp(v - mx) for v in zs]
+    tot = sum(ws)
+    cf = f(c)
+    for x in range(d):
+        ref = sum(ws[i] / tot * cf[128 + i, x] for i in range(128))
+        assert abs(e[1, x] - ref) < 1e-13
+
+
+# ----------------------------------------------------------------------------
+# indexer and top-k (§2.2 step 2)
+# ----------------------------------------------------------------------------
+
+def test_index_scores_brute_force(orc):
+    rng = np.random.default_rng(5)
+    HI, dI, n = 3, 5, 7
+    qI = bf(rng.standard_normal((HI, dI)))
+    kI = bf(rng.standard_normal((n, dI)))
+    s = orc.index_scores(qI, kI)
+    qf, kf = f(qI), f(kI)
+    for j in range(n):
+        ref = 0.0
+        for h in range(HI):
+            for i in range(dI):
+                ref += qf[h, i] * kf[j, i]
+        assert abs(s[j] - ref) < 1e-12
+
+
+def test_index_scores_single_head_is_dot_and_head_sum(orc):
+    rng = np.random.default_rng(6)
+    dI, n = 64, 50
+    q1 = bf(rng.standard_normal((1, dI)))
+    kI = bf(rng.standard_normal((n, dI)))
+    assert np.allclose(orc.index_scores(q1, kI), f(kI) @ f(q1)[0], rtol=0, atol=1e-12)
+    q4 = bf(rng.standard_normal((4, dI)))
+    # the head sum can be taken first: sum_h q_h . k = (sum_h q_h) . k
+    assert np.allclose(orc.index_scores(q4, kI), f(kI) @ f(q4).sum(0), rtol=0, atol=1e-11)
+
+
+def test_topk_brute_force_with_ties(orc):
+    rng = np.random.default_rng(7)
+    for trial in range(50):
+        n = int(rng.integers(0, 40))
+        k = int(rng.integers(1, 20))
+        s = rng.integers(-3, 4, n).astype(np.float64)          # many ties
+        got = orc.topk(s, k)
+        order = sorted(range(n), key=lambda j: (-s[j], j))[:k]
+        want = sorted(order) + [-1] * (k - len(order))
+        assert list(got) == want, (trial, s, k)
+
+
+def test_topk_all_equal_takes_lowest_indices(orc):
+    got = orc.topk(np.zeros(100), 10)
+    assert list(got) == list(range(10))
+
+
+# ----------------------------------------------------------------------------
+# attention (§2.2 step 3; §2.3)
+# ----------------------------------------------------------------------------
+
+def test_attend_single_key(orc):
+    rng = np.random.default_rng(8)
+    H, d = 3, 6
+    q = bf(rng.standard_normal((H, d)))
+    key = rng.standard_normal((1, d))
+    o, lse = orc.attend(q, key, 0.5)
+    assert np.allclose(o, np.repeat(key, H, 0), atol=1e-15)
+    assert np.allclose(lse, 0.5 * f(q) @ key[0], atol=1e-14)
+
+
+def test_attend_matches_library_sdpa(orc):
+    rng = np.random.default_rng(9)
+    H, d, n = 4, 16, 37
+    q = bf(rng.standard_normal((H, d)))
+    keys = rng.standard_normal((n, d))
+    o, lse = orc.attend(q, keys, 1 / math.sqrt(d))
+    qt = torch.from_numpy(f(q))[None, :, None, :]            # [1, H, 1, d]
+    kt = torch.from_numpy(keys)[None, None].expand(1, H, n, d)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, kt, scale=1 / math.sqrt(d))
+    assert np.allclose(o, ref[0, :, 0].numpy(), atol=1e-13)
+    logits = (torch.from_numpy(f(q)) @ torch.from_numpy(keys).T) / math.sqrt(d)
+    assert np.allclose(lse, torch.logsumexp(logits, -1).numpy(), atol=1e-13)
+
+
+def test_csa_ratio_one_full_topk_is_dense_causal_mqa(orc):
+    # m_C = 1 and k >= n: every token is its own entry and all are selected
+    L = 40
+    p = tiny_problem(L, d=16, H=3, mC=1, k=64, seed=10)
+    out = orc.hybrid_queries(p, do_hca=False)
+    ref = sdpa_causal(p["q"], p["kv"], p["scale"])
+    assert np.allclose(out["oC"], ref, atol=1e-12)
+    assert (out["idx"][:, :L] >= -1).all()
+
+
+def test_hca_short_sequence_is_dense_causal_mqa(orc):
+    L = 100                                        # < 128: no HCA entry, only raw tail
+    p = tiny_problem(L, d=16, H=2, seed=11)
+    out = orc.hybrid_queries(p, do_csa=False)
+    assert np.allclose(out["oH"], sdpa_causal(p["q"], p["kv"], p["scale"]), atol=1e-12)
+
+
+def test_hca_ratio_one_is_dense_causal_mqa(orc):
+    L = 33
+    p = tiny_problem(L, d=8, H=2, mH=1, seed=12)
+    out = orc.hybrid_queries(p, do_csa=False)
+    assert np.allclose(out["oH"], sdpa_causal(p["q"], p["kv"], p["scale"]), atol=1e-12)
+
+
+def test_outputs_in_convex_hull_of_keys(orc):
+    L = 300
+    p = tiny_problem(L, d=8, H=4, k=8, seed=13)
+    out = orc.hybrid_queries(p)
+    kvf = f(p["kv"])
+    lo, hi = kvf.min(0) - 1e-12, kvf.max(0) + 1e-12   # entries are convex mixes of tokens
+    assert (out["oC"] >= lo).all() and (out["oC"] <= hi).all()
+    assert (out["oH"] >= lo).all() and (out["oH"] <= hi).all()
+
+
+def test_key_counts_via_lse(orc):
+    # q = 0 makes every logit 0, so lse = log(number of keys):
+    # CSA: min(k, n_C) + r_C, HCA: n_H + r_H  (visibility and own-block tail)
+    L, k = 300, 16
+    p = tiny_problem(L, d=4, H=1, k=k, seed=14)
+    p["q"] = np.zeros_like(p["q"])
+    out = orc.hybrid_queries(p)
+    for t in range(L):
+        nC, rC = (t + 1) // 4, (t + 1) % 4
+        nH, rH = (t + 1) // 128, (t + 1) % 128
+        assert abs(out["lseC"][t, 0] - math.log(min(k, nC) + rC)) < 1e-12, t
+        assert abs(out["lseH"][t, 0] - math.log(nH + rH)) < 1e-12, t
+        assert (out["idx"][t] >= 0).sum() == min(k, nC)
+
+
+def test_visibility_boundary(orc):
+    # entry j = 5 gets a huge indexer score; t = 4j+2 must not see it, t = 4j+3 must.
+    j = 5
+    p = tiny_problem(64, d=4, H=1, HI=1, dI=4, k=2, seed=15)
+    p["qI"] = bf(np.ones((64, 1, 4)))
+    kI = np.zeros((16, 4), np.float32)
+    kI[j] = 100.0
+    p["kI"] = bf(kI)
+    out = orc.hybrid_queries(p, eval_q=np.array([4 * j + 2, 4 * j + 3]), do_hca=False)
+    assert j not in out["idx"][0] and j in out["idx"][1]
+
+
+def test_causality_future_perturbation(orc):
+    L, t = 260, 150
+    p = tiny_problem(L, d=8, H=2, k=8, seed=16)
+    base = orc.hybrid_queries(p, eval_q=np.array([t]))
+    q2 = dict(p)
+    rng = np.random.default_rng(17)
+    kv = p["kv"].copy()
+    kv[t + 1:] = bf(rng.standard_normal((L - t - 1, 8)))
+    gate = p["gate"].copy()
+    gate[t + 1:] = 9.0
+    kI = p["kI"].copy()
+    kI[(t + 1) // 4:] = bf(100 * np.ones((kI.shape[0] - (t + 1) // 4, kI.shape[1])))
+    q = p["q"].copy()
+    q[t + 1:] = 0
+    q2.update(kv=kv, gate=gate, kI=kI, q=q)
+    pert = orc.hybrid_queries(q2, eval_q=np.array([t]))
+    for key in ("idx", "oC", "lseC", "oH", "lseH"):
+        assert np.array_equal(base[key], pert[key]), key
+
+
+def test_given_idx_reproduces_own_selection(orc):
+    p = tiny_problem(200, d=8, H=2, k=8, seed=18)
+    own = orc.hybrid_queries(p, do_hca=False)
+    again = orc.hybrid_queries(p, given_idx=own["idx"], do_hca=False)
+    assert np.array_equal(own["oC"], again["oC"])
+
+
+def test_structural_counts_golden(orc):
+    """Golden structural constants printed on the pages (see the fixture's citations)."""
+    rows = {}
+    with open(os.path.join(GOLDEN, "structural_counts.txt")) as fh:
+        for line in fh:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, val = line.split("=")
+                rows[key.strip()] = int(val)
+    L = rows["context_tokens"]
+    # one token dimension and one head keep this cheap; q = 0 -> lse = log(#keys)
+    inp = dict(cu_kv=np.array([0, L]), cu_q=np.array([0, 1]),
+               cu_csa=np.array([0, L // 4]), cu_hca=np.array([0, L // 128]),
+               kv=bf(np.ones((L, 1))), gate=np.zeros(L, np.float32),
+               qI=bf(np.ones((1, 1, 1))), kI=bf(np.ones((L // 4, 1))),
+               q=bf(np.zeros((1, 1, 1))), mC=4, mH=128, top_k=L, scale=1.0)
+    out = orc.hybrid_queries(inp)
+    n_csa = int((out["idx"][0] >= 0).sum())
+    assert n_csa == rows["csa_entries"]
+    assert abs(out["lseH"][0, 0] - math.log(rows["hca_entries"])) < 1e-9
+    assert rows["csa_entries"] * 4 == L and rows["hca_entries"] * 128 == L
