@@ -1,0 +1,542 @@
+// C-ABI entry points of the CSA + HCA library: host-side argument checks,
+// per-device state, workspace carving and the two-branch hybrid step.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "csa.h"
+#include "launch.h"
+
+namespace csa {
+
+// Device error word (one per device that loads the library).
+static __device__ int g_error_word;
+
+namespace {
+
+struct DeviceState {
+    bool ready = false;
+    int *err = nullptr;
+    cudaStream_t aux = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    int num_sms = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+csa_status_t device_state(DeviceState **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return CSA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return CSA_ERR_CUDA;
+        s.err = static_cast<int *>(p);
+        if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return CSA_ERR_CUDA;
+        if (cudaStreamCreateWithFlags(&s.aux, cudaStreamNonBlocking) != cudaSuccess) return CSA_ERR_CUDA;
+        if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
+        if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
+        s.ready = true;
+    }
+    *out = &s;
+    return CSA_OK;
+}
+
+// ---- timing registry ----
+std::atomic<bool> g_timing{false};
+std::mutex g_timing_mu;
+struct Pending {
+    std::string name;
+    cudaEvent_t a, b;
+};
+std::vector<Pending> g_pending;
+std::map<std::string, std::pair<int64_t, double>> g_timing_acc;
+
+// ---- dynamic shared memory grants ----
+std::mutex g_smem_mu;
+std::map<std::pair<int, const void *>, size_t> g_smem;
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+csa_status_t from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return CSA_OK;
+    if (e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration) return CSA_ERR_UNSUPPORTED;
+    return CSA_ERR_CUDA;
+}
+
+csa_status_t check_layout(const csa_layout *L, bool need_csa, bool need_hca)
+{
+    if (!L || L->reserved != 0 || L->batch <= 0) return CSA_ERR_INVALID_ARG;
+    if (!L->cu_kv || !L->cu_q) return CSA_ERR_INVALID_ARG;
+    if (need_csa && !L->cu_csa) return CSA_ERR_INVALID_ARG;
+    if (need_hca && !L->cu_hca) return CSA_ERR_INVALID_ARG;
+    if (L->max_kv_len <= 0 || L->max_q_len < 0 || L->max_q_len > L->max_kv_len) return CSA_ERR_INVALID_ARG;
+    if (L->total_kv < 0 || L->total_q < 0 || L->total_csa < 0 || L->total_hca < 0) return CSA_ERR_INVALID_ARG;
+    if (L->total_q > (int64_t)L->batch * L->max_q_len) return CSA_ERR_INVALID_ARG;
+    if (L->total_kv > (int64_t)L->batch * L->max_kv_len) return CSA_ERR_INVALID_ARG;
+    if (L->total_q > 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
+    return CSA_OK;
+}
+
+csa_status_t check_ptr(const void *p, bool needed)
+{
+    if (!needed) return CSA_OK;
+    if (!p) return CSA_ERR_INVALID_ARG;
+    return aligned16(p) ? CSA_OK : CSA_ERR_INVALID_ARG;
+}
+
+#define CSA_TRY(x)                                  \
+    do {                                            \
+        const csa_status_t s_ = (x);                \
+        if (s_ != CSA_OK) return s_;                \
+    } while (0)
+
+constexpr size_t kWsAlign = 256;
+inline size_t align_ws(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+IndexArgs index_args(const csa_layout *L, const csa_bf16 *q_idx, const csa_bf16 *k_idx, int hi, int di, int ratio,
+                     int top_k, int32_t *idx_out, float *score_out, void *ws, size_t ws_bytes, int *err)
+{
+    IndexArgs a;
+    a.batch = L->batch;
+    a.max_kv_len = L->max_kv_len;
+    a.max_q_len = L->max_q_len;
+    a.total_q = L->total_q;
+    a.cu_kv = L->cu_kv;
+    a.cu_q = L->cu_q;
+    a.cu_csa = L->cu_csa;
+    a.q_idx = q_idx;
+    a.k_idx = k_idx;
+    a.n_heads_idx = hi;
+    a.d_idx = di;
+    a.ratio = ratio;
+    a.top_k = top_k;
+    a.idx_out = idx_out;
+    a.score_out = score_out;
+    a.ws = ws;
+    a.ws_bytes = ws_bytes;
+    a.err = err;
+    return a;
+}
+
+AttendArgs attend_args(const csa_layout *L, const int64_t *cu_ent, const csa_bf16 *q, const csa_bf16 *entries,
+                       const csa_bf16 *kv, const int32_t *idx, int H, int d, int ratio, int top_k, float scale,
+                       csa_bf16 *out, float *lse, void *ws, size_t ws_bytes, int *err, int num_sms, int sm_share)
+{
+    AttendArgs a;
+    a.batch = L->batch;
+    a.max_kv_len = L->max_kv_len;
+    a.max_q_len = L->max_q_len;
+    a.total_q = L->total_q;
+    a.cu_kv = L->cu_kv;
+    a.cu_q = L->cu_q;
+    a.cu_ent = cu_ent;
+    a.q = q;
+    a.entries = entries;
+    a.kv = kv;
+    a.idx = idx;
+    a.n_heads = H;
+    a.d = d;
+    a.ratio = ratio;
+    a.top_k = top_k;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    a.ws = ws;
+    a.ws_bytes = ws_bytes;
+    a.err = err;
+    a.num_sms = num_sms;
+    a.sm_share = sm_share;
+    return a;
+}
+
+csa_status_t check_index(const csa_layout *L, const csa_bf16 *q_idx, const csa_bf16 *k_idx, int hi, int di,
+                         int ratio, int top_k, const int32_t *idx_out, const float *score_out)
+{
+    CSA_TRY(check_layout(L, true, false));
+    if (ratio <= 0 || ratio > 1024 || top_k <= 0) return CSA_ERR_INVALID_ARG;
+    if (!index_supported(hi, di, top_k)) return CSA_ERR_UNSUPPORTED;
+    CSA_TRY(check_ptr(q_idx, L->total_q > 0));
+    CSA_TRY(check_ptr(k_idx, L->total_csa > 0));
+    if (L->total_q > 0 && !idx_out) return CSA_ERR_INVALID_ARG;
+    if (score_out && (reinterpret_cast<uintptr_t>(score_out) & 3u)) return CSA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(idx_out) & 3u) return CSA_ERR_INVALID_ARG;
+    return CSA_OK;
+}
+
+csa_status_t check_attend(const csa_layout *L, bool sparse, const csa_bf16 *q, const csa_bf16 *entries,
+                          const csa_bf16 *kv, const int32_t *idx, int H, int d, int ratio, int top_k,
+                          const csa_bf16 *out, const float *lse)
+{
+    CSA_TRY(check_layout(L, sparse, !sparse));
+    if (ratio <= 0 || ratio > 1024) return CSA_ERR_INVALID_ARG;
+    if (sparse && top_k <= 0) return CSA_ERR_INVALID_ARG;
+    if (!attend_supported(H, d)) return CSA_ERR_UNSUPPORTED;
+    const bool any_q = L->total_q > 0;
+    CSA_TRY(check_ptr(q, any_q));
+    CSA_TRY(check_ptr(out, any_q));
+    CSA_TRY(check_ptr(kv, any_q));
+    CSA_TRY(check_ptr(entries, any_q && (sparse ? L->total_csa : L->total_hca) > 0));
+    if (sparse && any_q && (!idx || (reinterpret_cast<uintptr_t>(idx) & 3u))) return CSA_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return CSA_ERR_INVALID_ARG;
+    return CSA_OK;
+}
+
+csa_status_t compress_impl(const csa_layout *L, bool csa_side, const csa_bf16 *kv, const float *gate, int d,
+                           int ratio, csa_bf16 *out, cudaStream_t st)
+{
+    CSA_TRY(check_layout(L, csa_side, !csa_side));
+    if (!pow2(ratio) || ratio > 128) return CSA_ERR_UNSUPPORTED;
+    if (d != 128 && d != 512) return CSA_ERR_UNSUPPORTED;
+    CSA_TRY(check_ptr(kv, L->total_kv > 0));
+    if (L->total_kv > 0 && (!gate || (reinterpret_cast<uintptr_t>(gate) & 3u))) return CSA_ERR_INVALID_ARG;
+    CSA_TRY(check_ptr(out, (csa_side ? L->total_csa : L->total_hca) > 0));
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    CompressArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.batch = L->batch;
+    a.max_kv_len = L->max_kv_len;
+    a.max_q_len = L->max_q_len;
+    a.cu_kv = L->cu_kv;
+    a.cu_q = L->cu_q;
+    a.d = d;
+    a.kv = kv;
+    a.gate = gate;
+    a.err = ds->err;
+    const int64_t *cu = csa_side ? L->cu_csa : L->cu_hca;
+    if (ratio <= 32) {
+        a.ratio_small = ratio;
+        a.cu_small = cu;
+        a.out_small = out;
+    } else {
+        a.ratio_big = ratio;
+        a.cu_big = cu;
+        a.out_big = out;
+    }
+    if (!compress_supported(d, a.ratio_small, a.ratio_big)) return CSA_ERR_UNSUPPORTED;
+    if (L->total_q == 0) return CSA_OK;
+    return from_cuda(launch_compress(a, st));
+}
+
+size_t hybrid_ws_parts(const csa_hybrid_params *p, size_t *idx_ws, size_t *sp_ws, size_t *hc_ws, int num_sms)
+{
+    const csa_layout *L = &p->layout;
+    IndexArgs ia = index_args(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k, nullptr,
+                              nullptr, nullptr, 0, nullptr);
+    AttendArgs sa = attend_args(L, L->cu_csa, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d,
+                                p->ratio_csa, p->top_k, p->scale, nullptr, nullptr, nullptr, 0, nullptr, num_sms,
+                                num_sms);
+    sa.idx = reinterpret_cast<const int32_t *>(1);   // sparse plan
+    AttendArgs ha = attend_args(L, L->cu_hca, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca,
+                                0, p->scale, nullptr, nullptr, nullptr, 0, nullptr, num_sms, num_sms / 2);
+    *idx_ws = align_ws(index_workspace_bytes(ia));
+    *sp_ws = align_ws(attend_workspace_bytes(sa));
+    *hc_ws = align_ws(attend_workspace_bytes(ha));
+    return *idx_ws + *sp_ws + *hc_ws;
+}
+
+}  // namespace
+
+bool timing_enabled() { return g_timing.load(std::memory_order_relaxed); }
+
+void timing_record(const char *name, cudaEvent_t start, cudaEvent_t stop)
+{
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    g_pending.push_back(Pending{name, start, stop});
+}
+
+cudaError_t ensure_smem_fn(const void *kern, size_t smem)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    auto key = std::make_pair(dev, kern);
+    auto it = g_smem.find(key);
+    if (it != g_smem.end() && it->second >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) g_smem[key] = smem;
+    return e;
+}
+
+}  // namespace csa
+
+using namespace csa;
+
+extern "C" {
+
+csa_status_t csa_compress(const csa_layout *layout, const csa_bf16 *kv, const float *gate, int d, int ratio,
+                          csa_bf16 *out, csa_stream_t stream)
+{
+    return compress_impl(layout, true, kv, gate, d, ratio, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+csa_status_t hca_compress(const csa_layout *layout, const csa_bf16 *kv, const float *gate, int d, int ratio,
+                          csa_bf16 *out, csa_stream_t stream)
+{
+    return compress_impl(layout, false, kv, gate, d, ratio, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+csa_status_t csa_index_workspace_size(const csa_layout *layout, int n_heads_idx, int d_idx, int ratio, int top_k,
+                                      size_t *bytes)
+{
+    if (!bytes) return CSA_ERR_INVALID_ARG;
+    CSA_TRY(check_layout(layout, true, false));
+    if (ratio <= 0 || top_k <= 0) return CSA_ERR_INVALID_ARG;
+    if (!index_supported(n_heads_idx, d_idx, top_k)) return CSA_ERR_UNSUPPORTED;
+    IndexArgs a = index_args(layout, nullptr, nullptr, n_heads_idx, d_idx, ratio, top_k, nullptr, nullptr, nullptr,
+                             0, nullptr);
+    *bytes = align_ws(index_workspace_bytes(a));
+    return CSA_OK;
+}
+
+csa_status_t lightning_index_topk(const csa_layout *layout, const csa_bf16 *q_idx, const csa_bf16 *k_idx,
+                                  int n_heads_idx, int d_idx, int ratio, int top_k, int32_t *idx_out,
+                                  float *score_out, void *ws, size_t ws_bytes, csa_stream_t stream)
+{
+    CSA_TRY(check_index(layout, q_idx, k_idx, n_heads_idx, d_idx, ratio, top_k, idx_out, score_out));
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    IndexArgs a = index_args(layout, q_idx, k_idx, n_heads_idx, d_idx, ratio, top_k, idx_out, score_out, ws,
+                             ws_bytes, ds->err);
+    const size_t need = index_workspace_bytes(a);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return CSA_ERR_WORKSPACE;
+    return from_cuda(launch_index_topk(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status_t csa_attend_workspace_size(const csa_layout *layout, int n_heads, int d, int ratio, int top_k,
+                                       size_t *bytes)
+{
+    if (!bytes) return CSA_ERR_INVALID_ARG;
+    const bool sparse = top_k > 0;
+    CSA_TRY(check_layout(layout, sparse, !sparse));
+    if (ratio <= 0 || top_k < 0) return CSA_ERR_INVALID_ARG;
+    if (!attend_supported(n_heads, d)) return CSA_ERR_UNSUPPORTED;
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    AttendArgs a = attend_args(layout, sparse ? layout->cu_csa : layout->cu_hca, nullptr, nullptr, nullptr,
+                               sparse ? reinterpret_cast<const int32_t *>(1) : nullptr, n_heads, d, ratio, top_k,
+                               1.f, nullptr, nullptr, nullptr, 0, nullptr, ds->num_sms, ds->num_sms);
+    *bytes = align_ws(attend_workspace_bytes(a));
+    return CSA_OK;
+}
+
+csa_status_t sparse_mqa_attend(const csa_layout *layout, const csa_bf16 *q, const csa_bf16 *csa_entries,
+                               const csa_bf16 *kv, const int32_t *idx, int n_heads, int d, int ratio, int top_k,
+                               float scale, csa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                               csa_stream_t stream)
+{
+    CSA_TRY(check_attend(layout, true, q, csa_entries, kv, idx, n_heads, d, ratio, top_k, out, lse));
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    AttendArgs a = attend_args(layout, layout->cu_csa, q, csa_entries, kv, idx, n_heads, d, ratio, top_k, scale,
+                               out, lse, ws, ws_bytes, ds->err, ds->num_sms, ds->num_sms);
+    const size_t need = attend_workspace_bytes(a);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return CSA_ERR_WORKSPACE;
+    return from_cuda(launch_attend(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status_t hca_dense_attend(const csa_layout *layout, const csa_bf16 *q, const csa_bf16 *hca_entries,
+                              const csa_bf16 *kv, int n_heads, int d, int ratio, float scale, csa_bf16 *out,
+                              float *lse, void *ws, size_t ws_bytes, csa_stream_t stream)
+{
+    CSA_TRY(check_attend(layout, false, q, hca_entries, kv, nullptr, n_heads, d, ratio, 0, out, lse));
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    AttendArgs a = attend_args(layout, layout->cu_hca, q, hca_entries, kv, nullptr, n_heads, d, ratio, 0, scale,
+                               out, lse, ws, ws_bytes, ds->err, ds->num_sms, ds->num_sms);
+    const size_t need = attend_workspace_bytes(a);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return CSA_ERR_WORKSPACE;
+    return from_cuda(launch_attend(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status_t csa_workspace_size(const csa_hybrid_params *p, size_t *bytes)
+{
+    if (!p || !bytes) return CSA_ERR_INVALID_ARG;
+    CSA_TRY(check_layout(&p->layout, true, true));
+    if (p->ratio_csa <= 0 || p->ratio_hca <= 0 || p->top_k <= 0) return CSA_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    size_t a, b, c;
+    *bytes = hybrid_ws_parts(p, &a, &b, &c, ds->num_sms);
+    return CSA_OK;
+}
+
+csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
+{
+    if (!p || p->reserved != 0) return CSA_ERR_INVALID_ARG;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
+    const csa_layout *L = &p->layout;
+    CSA_TRY(check_index(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k, p->idx_out,
+                        p->score_out));
+    CSA_TRY(check_attend(L, true, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d, p->ratio_csa, p->top_k,
+                         p->o_csa, p->lse_csa));
+    CSA_TRY(check_attend(L, false, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca, 0, p->o_hca,
+                         p->lse_hca));
+    const bool compress = !(p->flags & CSA_SKIP_COMPRESS);
+    if (compress) {
+        if (!pow2(p->ratio_csa) || p->ratio_csa > 128 || !pow2(p->ratio_hca) || p->ratio_hca > 128)
+            return CSA_ERR_UNSUPPORTED;
+        CSA_TRY(check_ptr(p->kv, L->total_kv > 0));
+        if (L->total_kv > 0 && !p->gate) return CSA_ERR_INVALID_ARG;
+        CSA_TRY(check_ptr(p->csa_cache, L->total_csa > 0));
+        CSA_TRY(check_ptr(p->hca_cache, L->total_hca > 0));
+    }
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    size_t w_idx, w_sp, w_hc;
+    const size_t need = hybrid_ws_parts(p, &w_idx, &w_sp, &w_hc, ds->num_sms);
+    if (need > 0 && (!p->ws || p->ws_bytes < need || !aligned16(p->ws))) return CSA_ERR_WORKSPACE;
+    if (L->total_q == 0) return CSA_OK;
+    char *ws = static_cast<char *>(p->ws);
+
+    // a1: compression of the blocks closed by this call's query positions
+    if (compress) {
+        CompressArgs a;
+        std::memset(&a, 0, sizeof a);
+        a.batch = L->batch;
+        a.max_kv_len = L->max_kv_len;
+        a.max_q_len = L->max_q_len;
+        a.cu_kv = L->cu_kv;
+        a.cu_q = L->cu_q;
+        a.d = p->d;
+        a.kv = p->kv;
+        a.gate = p->gate;
+        a.err = ds->err;
+        if (compress_supported(p->d, p->ratio_csa, p->ratio_hca)) {
+            a.ratio_small = p->ratio_csa;
+            a.cu_small = L->cu_csa;
+            a.out_small = p->csa_cache;
+            a.ratio_big = p->ratio_hca;
+            a.cu_big = L->cu_hca;
+            a.out_big = p->hca_cache;
+            CSA_TRY(from_cuda(launch_compress(a, st)));
+        } else {
+            CSA_TRY(compress_impl(L, true, p->kv, p->gate, p->d, p->ratio_csa, p->csa_cache, st));
+            CSA_TRY(compress_impl(L, false, p->kv, p->gate, p->d, p->ratio_hca, p->hca_cache, st));
+        }
+    }
+
+    // fork: the HCA branch runs on the helper stream, concurrently with the CSA branch
+    if (cudaEventRecord(ds->fork, st) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaStreamWaitEvent(ds->aux, ds->fork, 0) != cudaSuccess) return CSA_ERR_CUDA;
+
+    AttendArgs ha = attend_args(L, L->cu_hca, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca, 0,
+                                p->scale, p->o_hca, p->lse_hca, w_hc ? ws + w_idx + w_sp : nullptr, w_hc, ds->err,
+                                ds->num_sms, ds->num_sms / 2);
+    csa_status_t s_h = from_cuda(launch_attend(ha, ds->aux));
+
+    IndexArgs ia = index_args(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k, p->idx_out,
+                              p->score_out, w_idx ? ws : nullptr, w_idx, ds->err);
+    csa_status_t s_c = from_cuda(launch_index_topk(ia, st));
+    if (s_c == CSA_OK) {
+        AttendArgs sa = attend_args(L, L->cu_csa, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d,
+                                    p->ratio_csa, p->top_k, p->scale, p->o_csa, p->lse_csa,
+                                    w_sp ? ws + w_idx : nullptr, w_sp, ds->err, ds->num_sms, ds->num_sms);
+        s_c = from_cuda(launch_attend(sa, st));
+    }
+    // join (always, so the helper stream never dangles inside a capture)
+    const bool j1 = cudaEventRecord(ds->join, ds->aux) == cudaSuccess;
+    const bool j2 = cudaStreamWaitEvent(st, ds->join, 0) == cudaSuccess;
+    if (s_c != CSA_OK) return s_c;
+    if (s_h != CSA_OK) return s_h;
+    return (j1 && j2) ? CSA_OK : CSA_ERR_CUDA;
+}
+
+csa_status_t csa_workspace_init(void *ws, size_t ws_bytes, csa_stream_t stream)
+{
+    if (ws_bytes == 0) return CSA_OK;
+    if (!ws) return CSA_ERR_INVALID_ARG;
+    return cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? CSA_OK
+                                                                                                  : CSA_ERR_CUDA;
+}
+
+const char *csa_status_string(csa_status_t s)
+{
+    switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "unsupported size";
+    case CSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case CSA_ERR_CUDA: return "CUDA error";
+    case CSA_ERR_TIMEOUT: return "device wait timed out";
+    case CSA_ERR_DEVICE: return "device-side layout or index error";
+    default: return "unknown status";
+    }
+}
+
+csa_status_t csa_check_device_error(csa_stream_t stream, csa_status_t *device_status)
+{
+    if (!device_status) return CSA_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, ds->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(ds->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return CSA_ERR_CUDA;
+    *device_status = static_cast<csa_status_t>(v);
+    return CSA_OK;
+}
+
+int csa_version(void) { return 100; }
+
+csa_status_t csa_timing_enable(int enable)
+{
+    g_timing.store(enable != 0);
+    return CSA_OK;
+}
+
+int csa_timing_read(int cap, const char **names, int64_t *launches, double *total_ms)
+{
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    for (auto &pd : g_pending) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(pd.b) == cudaSuccess && cudaEventElapsedTime(&ms, pd.a, pd.b) == cudaSuccess) {
+            auto &acc = g_timing_acc[pd.name];
+            acc.first += 1;
+            acc.second += ms;
+        }
+        cudaEventDestroy(pd.a);
+        cudaEventDestroy(pd.b);
+    }
+    g_pending.clear();
+    int i = 0;
+    for (auto &kv : g_timing_acc) {
+        if (i < cap) {
+            if (names) names[i] = kv.first.c_str();
+            if (launches) launches[i] = kv.second.first;
+            if (total_ms) total_ms[i] = kv.second.second;
+        }
+        i++;
+    }
+    return i;
+}
+
+void csa_timing_reset(void)
+{
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    for (auto &pd : g_pending) {
+        cudaEventDestroy(pd.a);
+        cudaEventDestroy(pd.b);
+    }
+    g_pending.clear();
+    g_timing_acc.clear();
+}
+
+}  // extern "C"

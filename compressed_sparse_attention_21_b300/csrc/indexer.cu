@@ -1,0 +1,633 @@
+// Lightning indexer + top-k ("DeepSeek-V4 core architecture", §2.2 CSA step 2:
+// a light scorer rates each query against every compressed entry and only the
+// top-k entries take part in attention).
+//
+// Score of visible entry j (j < n(t) = floor((t+1)/m)) for the query at t:
+//     s = fp32 sum over indexer heads h of q_{t,h} . k_j
+// computed as (sum_h q_{t,h}) . k_j: the head sum is formed once per query in
+// fp32 and the dot product runs in fp32 FMAs.  Ties go to the lower index and
+// the kept indices are written in ascending order, padded with -1.
+//
+// Scores are mapped onto order-preserving 32-bit keys.  Two paths:
+//  * per-query CTA (prefill-sized batches, n(t) <= kCtaMaxN): the query's
+//    whole key row lives in shared memory; an 8-bit radix select finds the
+//    k-th key exactly and one ordered pass emits the selection in index
+//    order (ties resolved by rank among equal keys);
+//  * multi-CTA (decode-sized batches or long rows): many CTAs per query scan
+//    the indexer keys (the HBM-bound part), write the key row to the
+//    workspace and build a 4096-bin histogram of the keys' top 12 bits; the
+//    last CTA of a query (atomic ticket, no waiting) locates the bin that
+//    holds the k-th key.  A second kernel keeps everything above that bin,
+//    collects the bin's members as candidates, and its last CTA per query
+//    resolves them with a radix select on (key, index), then sorts the k
+//    winners by index.
+// The full score matrix is never stored; only one key row per query in the
+// multi-CTA path.
+#include "common.cuh"
+#include "launch.h"
+
+namespace csa {
+
+namespace {
+
+constexpr int kCtaThreads = 512;
+constexpr int kCtaMaxN = 40960;       // key row in shared memory: 160 KiB
+constexpr int kMaxTopK = 2048;
+constexpr int kScanThreads = 256;
+constexpr int kScanChunk = 1024;      // entries per scan/filter CTA
+constexpr int kHistBits = 12;
+constexpr int kHistBins = 1 << kHistBits;
+constexpr int kMetaWords = 8;         // per-query: ticket1, ticket2, n_sel, n_cand, bin, above
+constexpr int64_t kGroupBudget = int64_t(1) << 30;   // max workspace of the multi-CTA path
+
+__host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Workspace carving of the multi-CTA path for `gq` queries.
+struct WsD {
+    uint32_t *keys;   // [gq][key_stride]
+    uint32_t *hist;   // [gq][kHistBins]          zero between calls
+    uint32_t *meta;   // [gq][kMetaWords]         words 0..3 zero between calls
+    uint64_t *sel;    // [gq][top_k]
+    uint64_t *cand;   // [gq][cand_stride]
+    int64_t key_stride, cand_stride;
+};
+
+__host__ __device__ inline int64_t wsd_bytes_per_query(int64_t max_n, int top_k)
+{
+    return align_up(max_n, 64) * 4 + kHistBins * 4 + kMetaWords * 4 + align_up(top_k, 32) * 8 +
+           align_up(max_n, 32) * 8;
+}
+
+inline WsD carve_wsd(void *ws, int64_t gq, int64_t max_n, int top_k)
+{
+    WsD w;
+    char *p = static_cast<char *>(ws);
+    w.key_stride = align_up(max_n, 64);
+    w.cand_stride = align_up(max_n, 32);
+    w.hist = reinterpret_cast<uint32_t *>(p);
+    p += align_up(gq * kHistBins * 4, 256);
+    w.meta = reinterpret_cast<uint32_t *>(p);
+    p += align_up(gq * kMetaWords * 4, 256);
+    w.keys = reinterpret_cast<uint32_t *>(p);
+    p += align_up(gq * w.key_stride * 4, 256);
+    w.sel = reinterpret_cast<uint64_t *>(p);
+    p += align_up(gq * align_up(top_k, 32) * 8, 256);
+    w.cand = reinterpret_cast<uint64_t *>(p);
+    return w;
+}
+
+inline int64_t wsd_total_bytes(int64_t gq, int64_t max_n, int top_k)
+{
+    return align_up(gq * kHistBins * 4, 256) + align_up(gq * kMetaWords * 4, 256) +
+           align_up(gq * align_up(max_n, 64) * 4, 256) + align_up(gq * align_up(top_k, 32) * 8, 256) +
+           align_up(gq * align_up(max_n, 32) * 8, 256);
+}
+
+// ---------------------------------------------------------------------------
+// shared pieces
+// ---------------------------------------------------------------------------
+template <int DI>
+__device__ __forceinline__ void load_qsum(const uint16_t *__restrict__ qI, int64_t qi, int HI, float *s_q)
+{
+    for (int i = threadIdx.x; i < DI; i += blockDim.x) {
+        float s = 0.f;
+        for (int h = 0; h < HI; h++) {
+            const uint32_t bits = __ldg(qI + (qi * HI + h) * DI + i);
+            s += __uint_as_float(bits << 16);
+        }
+        s_q[i] = s;
+    }
+}
+
+template <int DI>
+__device__ __forceinline__ float score_row(const uint16_t *__restrict__ krow, const float *s_q)
+{
+    const uint4 *p = reinterpret_cast<const uint4 *>(krow);
+    uint4 v[DI / 8];
+#pragma unroll
+    for (int c = 0; c < DI / 8; c++) v[c] = __ldg(p + c);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < DI / 8; c++) {
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            acc = fmaf(s_q[8 * c + 2 * k], bf16_lo(w[k]), acc);
+            acc = fmaf(s_q[8 * c + 2 * k + 1], bf16_hi(w[k]), acc);
+        }
+    }
+    return acc;
+}
+
+// Warp-aggregated shared-memory histogram increment; all 32 lanes must call.
+__device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t bin, bool valid)
+{
+    const unsigned act = __ballot_sync(0xffffffffu, valid);
+    if (!valid) return;
+    const unsigned peers = __match_any_sync(act, bin);
+    if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(hist + bin, (uint32_t)__popc(peers));
+}
+
+// Warp 0: in a 256-bin histogram walked from the top bin down, find the bin
+// that holds the `remaining`-th largest element; report it and the count of
+// elements in higher bins.
+__device__ __forceinline__ void find_digit_256(const uint32_t *hist, uint32_t remaining, uint32_t *out_digit,
+                                               uint32_t *out_above)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t c[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        c[i] = hist[255 - 8 * lane - i];
+        sum += c[i];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const uint32_t excl = incl - sum;
+    if (excl < remaining && remaining <= incl) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            if (acc + c[i] >= remaining) {
+                *out_digit = 255 - 8 * lane - i;
+                *out_above = acc;
+                break;
+            }
+            acc += c[i];
+        }
+    }
+}
+
+// CTA-wide exclusive scan of one value per thread; returns the prefix and
+// the total.  s_w holds 2 * NT/32 + 1 words.
+template <int NT>
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *s_w, uint32_t &total)
+{
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) s_w[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t t = lane < NW ? s_w[lane] : 0u;
+        uint32_t ti = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o) ti += u;
+        }
+        if (lane < NW) s_w[NW + lane] = ti - t;
+        if (lane == 31) s_w[2 * NW] = ti;
+    }
+    __syncthreads();
+    total = s_w[2 * NW];
+    const uint32_t r = s_w[NW + warp] + incl - v;
+    __syncthreads();   // s_w may be reused right away
+    return r;
+}
+
+__device__ __forceinline__ void write_row_padding(int32_t *idx_row, float *score_row_out, int from, int top_k)
+{
+    for (int i = from + threadIdx.x; i < top_k; i += blockDim.x) {
+        idx_row[i] = -1;
+        if (score_row_out) score_row_out[i] = -INFINITY;
+    }
+}
+
+__device__ __forceinline__ bool entry_count_ok(const int64_t *cu_csa, const QueryPos &p, int ratio)
+{
+    return __ldg(cu_csa + p.b + 1) - __ldg(cu_csa + p.b) == p.L / ratio && p.t >= 0 && p.t < p.L;
+}
+
+// ---------------------------------------------------------------------------
+// path 1: one CTA per query, key row in shared memory
+// ---------------------------------------------------------------------------
+template <int DI>
+__global__ void __launch_bounds__(kCtaThreads)
+index_topk_cta_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                      const int64_t *__restrict__ cu_csa, int64_t q_begin, const uint16_t *__restrict__ qI,
+                      const uint16_t *__restrict__ kI, int HI, int ratio, int top_k, int n_cap,
+                      int32_t *__restrict__ idx_out, float *__restrict__ score_out, int *err)
+{
+    extern __shared__ uint32_t s_keys[];
+    __shared__ float s_q[DI];
+    __shared__ uint32_t s_hist[256];
+    __shared__ uint32_t s_w[2 * (kCtaThreads / 32) + 1];
+    __shared__ uint32_t s_digit, s_above;
+
+    const int tid = threadIdx.x;
+    const int64_t qi = q_begin + blockIdx.x;
+    const QueryPos p = query_pos(cu_kv, cu_q, batch, qi);
+    int32_t *idx_row = idx_out + qi * top_k;
+    float *sc_row = score_out ? score_out + qi * top_k : nullptr;
+    const int64_t n64 = (p.t + 1) / ratio;
+    if (!entry_count_ok(cu_csa, p, ratio) || n64 > n_cap) {
+        if (tid == 0) set_error(err, CSA_ERR_DEVICE);
+        write_row_padding(idx_row, sc_row, 0, top_k);
+        return;
+    }
+    const int n = (int)n64;
+    const uint16_t *kbase = kI + __ldg(cu_csa + p.b) * DI;
+
+    load_qsum<DI>(qI, qi, HI, s_q);
+    __syncthreads();
+    for (int j = tid; j < n; j += kCtaThreads) s_keys[j] = score_key(score_row<DI>(kbase + (int64_t)j * DI, s_q));
+    __syncthreads();
+
+    if (n <= top_k) {
+        for (int i = tid; i < n; i += kCtaThreads) {
+            idx_row[i] = i;
+            if (sc_row) sc_row[i] = key_score(s_keys[i]);
+        }
+        write_row_padding(idx_row, sc_row, n, top_k);
+        return;
+    }
+
+    // exact k-th largest key: four 8-bit radix passes
+    uint32_t prefix = 0, pmask = 0, remaining = (uint32_t)top_k;
+    for (int sh = 24; sh >= 0; sh -= 8) {
+        for (int i = tid; i < 256; i += kCtaThreads) s_hist[i] = 0;
+        __syncthreads();
+        for (int base = 0; base < n; base += kCtaThreads) {
+            const int j = base + tid;
+            const uint32_t key = j < n ? s_keys[j] : 0u;
+            hist_add(s_hist, (key >> sh) & 255u, j < n && (key & pmask) == prefix);
+        }
+        __syncthreads();
+        if (tid < 32) find_digit_256(s_hist, remaining, &s_digit, &s_above);
+        __syncthreads();
+        remaining -= s_above;
+        prefix |= s_digit << sh;
+        pmask |= 255u << sh;
+        __syncthreads();
+    }
+    const uint32_t kstar = prefix;
+    const uint32_t need_eq = remaining;   // members equal to kstar still to take, lowest index first
+
+    // one ordered pass: emit the selection in ascending index order
+    uint32_t sel_base = 0, eq_base = 0;
+    for (int base = 0; base < n; base += kCtaThreads) {
+        const int j = base + tid;
+        const uint32_t key = j < n ? s_keys[j] : 0u;
+        const bool gt = j < n && key > kstar;
+        const bool eq = j < n && key == kstar;
+        uint32_t eq_tot, sel_tot;
+        const uint32_t eq_rank = eq_base + block_scan<kCtaThreads>(eq ? 1u : 0u, s_w, eq_tot);
+        const bool sel = gt || (eq && eq_rank < need_eq);
+        const uint32_t pos = sel_base + block_scan<kCtaThreads>(sel ? 1u : 0u, s_w, sel_tot);
+        if (sel && pos < (uint32_t)top_k) {
+            idx_row[pos] = j;
+            if (sc_row) sc_row[pos] = key_score(key);
+        }
+        eq_base += eq_tot;
+        sel_base += sel_tot;
+    }
+    if (tid == 0 && sel_base != (uint32_t)top_k) set_error(err, CSA_ERR_DEVICE);
+}
+
+// ---------------------------------------------------------------------------
+// path 2: many CTAs per query
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int64_t chunks_of(int64_t n) { return n <= 0 ? 1 : (n + kScanChunk - 1) / kScanChunk; }
+
+template <int DI>
+__global__ void __launch_bounds__(kScanThreads)
+index_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                  const int64_t *__restrict__ cu_csa, int64_t q_begin, const uint16_t *__restrict__ qI,
+                  const uint16_t *__restrict__ kI, int HI, int ratio, int top_k, WsD w, int32_t *__restrict__ idx_out,
+                  float *__restrict__ score_out, int *err)
+{
+    __shared__ float s_q[DI];
+    __shared__ uint32_t s_hist[kHistBins];
+    __shared__ uint32_t s_sum[2 * (kScanThreads / 32) + 1];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x;
+    const int64_t qg = blockIdx.y;
+    const int64_t qi = q_begin + qg;
+    const QueryPos p = query_pos(cu_kv, cu_q, batch, qi);
+    const int64_t n = (p.t + 1) / ratio;
+    const int64_t nchunks = chunks_of(n);
+    if ((int64_t)blockIdx.x >= nchunks) return;
+    if (!entry_count_ok(cu_csa, p, ratio) || n > w.key_stride) {
+        if (blockIdx.x == 0) {
+            if (tid == 0) set_error(err, CSA_ERR_DEVICE);
+            write_row_padding(idx_out + qi * top_k, score_out ? score_out + qi * top_k : nullptr, 0, top_k);
+        }
+        return;
+    }
+    for (int i = tid; i < kHistBins; i += kScanThreads) s_hist[i] = 0;
+    load_qsum<DI>(qI, qi, HI, s_q);
+    __syncthreads();
+
+    const uint16_t *kbase = kI + __ldg(cu_csa + p.b) * DI;
+    uint32_t *keys = w.keys + qg * w.key_stride;
+    const int64_t c0 = (int64_t)blockIdx.x * kScanChunk;
+    float sc[kScanChunk / kScanThreads];
+#pragma unroll
+    for (int i = 0; i < kScanChunk / kScanThreads; i++) {
+        const int64_t j = c0 + i * kScanThreads + tid;
+        sc[i] = j < n ? score_row<DI>(kbase + j * DI, s_q) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kScanChunk / kScanThreads; i++) {
+        const int64_t j = c0 + i * kScanThreads + tid;
+        const uint32_t key = score_key(sc[i]);
+        if (j < n) keys[j] = key;
+        hist_add(s_hist, key >> (32 - kHistBits), j < n);
+    }
+    __syncthreads();
+    uint32_t *ghist = w.hist + qg * kHistBins;
+    for (int i = tid; i < kHistBins; i += kScanThreads) {
+        const uint32_t c = s_hist[i];
+        if (c) atomicAdd(ghist + i, c);
+    }
+    __threadfence();
+    __syncthreads();
+    uint32_t *meta = w.meta + qg * kMetaWords;
+    if (tid == 0) s_last = atomicAdd(meta + 0, 1u) == (uint32_t)(nchunks - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // last CTA of this query: locate the bin of the k-th largest key
+    const int64_t k_eff = n < top_k ? n : top_k;
+    if (n <= top_k) {
+        if (tid == 0) {
+            meta[4] = 0xffffffffu;        // every bin is above: take all
+            meta[5] = (uint32_t)n;
+        }
+    } else {
+        // thread t owns bins [4095-16t-15, 4095-16t], walked from the top
+        uint32_t c[16], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            c[i] = __ldcg(ghist + (kHistBins - 1 - 16 * tid - i));
+            sum += c[i];
+        }
+        uint32_t tot;
+        const uint32_t excl = block_scan<kScanThreads>(sum, s_sum, tot);
+        if (excl < (uint32_t)k_eff && (uint32_t)k_eff <= excl + sum) {
+            uint32_t acc = excl;
+            for (int i = 0; i < 16; i++) {
+                if (acc + c[i] >= (uint32_t)k_eff) {
+                    meta[4] = (uint32_t)(kHistBins - 1 - 16 * tid - i);
+                    meta[5] = acc;
+                    break;
+                }
+                acc += c[i];
+            }
+        }
+    }
+    // leave the histogram and the ticket zeroed for the next call
+    for (int i = tid; i < kHistBins; i += kScanThreads) ghist[i] = 0;
+    if (tid == 0) meta[0] = 0;
+}
+
+template <int NT>
+__device__ __forceinline__ void warp_append(bool flag, uint64_t value, uint32_t *counter, uint64_t *list)
+{
+    const unsigned m = __ballot_sync(0xffffffffu, flag);
+    if (!m) return;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(m) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(counter, (uint32_t)__popc(m));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (flag) list[base + __popc(m & ((1u << lane) - 1u))] = value;
+}
+
+__device__ __forceinline__ uint64_t composite(uint32_t key, int64_t j)
+{
+    return ((uint64_t)key << 32) | (uint64_t)(0xffffffffu - (uint32_t)j);
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+index_filter_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                    const int64_t *__restrict__ cu_csa, int64_t q_begin, int ratio, int top_k, WsD w,
+                    int32_t *__restrict__ idx_out, float *__restrict__ score_out, int *err)
+{
+    __shared__ uint32_t s_hist[256];
+    __shared__ uint32_t s_digit, s_above, s_cnt;
+    __shared__ int s_last;
+    __shared__ int32_t s_idx[kMaxTopK];
+    __shared__ uint32_t s_key[kMaxTopK];
+
+    const int tid = threadIdx.x;
+    const int64_t qg = blockIdx.y;
+    const int64_t qi = q_begin + qg;
+    const QueryPos p = query_pos(cu_kv, cu_q, batch, qi);
+    const int64_t n = (p.t + 1) / ratio;
+    const int64_t nchunks = chunks_of(n);
+    if ((int64_t)blockIdx.x >= nchunks) return;
+    if (!entry_count_ok(cu_csa, p, ratio) || n > w.key_stride) return;   // reported by the scan
+
+    uint32_t *meta = w.meta + qg * kMetaWords;
+    const uint32_t bstar = meta[4];
+    const uint32_t *keys = w.keys + qg * w.key_stride;
+    uint64_t *sel = w.sel + qg * align_up(top_k, 32);
+    uint64_t *cand = w.cand + qg * w.cand_stride;
+    const int64_t c0 = (int64_t)blockIdx.x * kScanChunk;
+#pragma unroll
+    for (int i = 0; i < kScanChunk / kScanThreads; i++) {
+        const int64_t j = c0 + i * kScanThreads + tid;
+        const uint32_t key = j < n ? __ldcg(keys + j) : 0u;
+        const uint32_t bin = key >> (32 - kHistBits);
+        const bool above = j < n && (bstar == 0xffffffffu || bin > bstar);
+        const bool at = j < n && bstar != 0xffffffffu && bin == bstar;
+        warp_append<kScanThreads>(above, composite(key, j), meta + 2, sel);
+        warp_append<kScanThreads>(at, composite(key, j), meta + 3, cand);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(meta + 1, 1u) == (uint32_t)(nchunks - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // last CTA of this query: resolve the boundary bin exactly
+    const uint32_t n_sel = __ldcg(meta + 2);
+    const uint32_t n_cand = __ldcg(meta + 3);
+    const int64_t k_eff = n < top_k ? n : top_k;
+    const uint32_t need = (uint32_t)k_eff - __ldcg(meta + 5);   // from the candidates
+    // composite keys of candidates share their top 12 bits; select on bits 51..0
+    uint64_t prefix = 0, hmask = 0;
+    bool take_none = need == 0;
+    if (need > 0 && need < n_cand) {
+        uint32_t remaining = need;
+        for (int sh = 44; sh >= -4; sh -= 8) {
+            const int s = sh < 0 ? 0 : sh;
+            const uint64_t dmask = sh < 0 ? 0xfull : 0xffull;
+            for (int i = tid; i < 256; i += kScanThreads) s_hist[i] = 0;
+            __syncthreads();
+            for (uint32_t base = 0; base < n_cand; base += kScanThreads) {
+                const uint32_t c = base + tid;
+                const uint64_t ck = c < n_cand ? __ldcg(cand + c) : 0ull;
+                hist_add(s_hist, (uint32_t)((ck >> s) & dmask), c < n_cand && (ck & hmask) == prefix);
+            }
+            __syncthreads();
+            if (tid < 32) find_digit_256(s_hist, remaining, &s_digit, &s_above);
+            __syncthreads();
+            const uint32_t dgt = s_digit;
+            remaining -= s_above;
+            prefix |= (uint64_t)dgt << s;
+            hmask |= dmask << s;
+            const bool done = s_hist[dgt] == remaining;
+            __syncthreads();
+            if (done) break;
+        }
+    }
+    // gather the winners
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
+    for (uint32_t c = tid; c < n_sel; c += kScanThreads) {
+        const uint64_t ck = __ldcg(sel + c);
+        const uint32_t pos = atomicAdd(&s_cnt, 1u);
+        if (pos < kMaxTopK) {
+            s_idx[pos] = (int32_t)(0xffffffffu - (uint32_t)ck);
+            s_key[pos] = (uint32_t)(ck >> 32);
+        }
+    }
+    if (!take_none) {
+        for (uint32_t c = tid; c < n_cand; c += kScanThreads) {
+            const uint64_t ck = __ldcg(cand + c);
+            if ((ck & hmask) >= prefix) {
+                const uint32_t pos = atomicAdd(&s_cnt, 1u);
+                if (pos < kMaxTopK) {
+                    s_idx[pos] = (int32_t)(0xffffffffu - (uint32_t)ck);
+                    s_key[pos] = (uint32_t)(ck >> 32);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const uint32_t got = s_cnt;
+    if (tid == 0 && got != (uint32_t)k_eff) set_error(err, CSA_ERR_DEVICE);
+    int npow = 1;
+    while (npow < (int)k_eff) npow <<= 1;
+    for (int i = (int)(got < (uint32_t)kMaxTopK ? got : (uint32_t)kMaxTopK) + tid; i < npow; i += kScanThreads) {
+        s_idx[i] = 0x7fffffff;
+        s_key[i] = 0;
+    }
+    __syncthreads();
+    // bitonic sort by index, ascending
+    for (int size = 2; size <= npow; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < npow; i += kScanThreads) {
+                const int jj = i ^ stride;
+                if (jj > i) {
+                    const bool up = (i & size) == 0;
+                    const int32_t a = s_idx[i], bb = s_idx[jj];
+                    if ((a > bb) == up) {
+                        s_idx[i] = bb;
+                        s_idx[jj] = a;
+                        const uint32_t t = s_key[i];
+                        s_key[i] = s_key[jj];
+                        s_key[jj] = t;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    int32_t *idx_row = idx_out + qi * top_k;
+    float *sc_row = score_out ? score_out + qi * top_k : nullptr;
+    for (int i = tid; i < top_k; i += kScanThreads) {
+        const bool v = i < k_eff && s_idx[i] != 0x7fffffff;
+        idx_row[i] = v ? s_idx[i] : -1;
+        if (sc_row) sc_row[i] = v ? key_score(s_key[i]) : -INFINITY;
+    }
+    // leave the counters zeroed for the next call
+    if (tid == 0) {
+        meta[1] = 0;
+        meta[2] = 0;
+        meta[3] = 0;
+    }
+}
+
+bool use_cta_path(const IndexArgs &a)
+{
+    const int64_t max_n = a.max_kv_len / a.ratio;
+    return max_n <= kCtaMaxN && a.total_q >= 1024;
+}
+
+int64_t group_size(const IndexArgs &a)
+{
+    const int64_t max_n = a.max_kv_len / a.ratio;
+    const int64_t per_q = wsd_bytes_per_query(max_n, a.top_k);
+    int64_t g = kGroupBudget / per_q;
+    if (g < 1) g = 1;
+    if (g > 65535) g = 65535;   // queries ride on grid.y
+    return g < a.total_q ? g : a.total_q;
+}
+
+template <int DI>
+cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
+{
+    if (a.total_q <= 0) return cudaSuccess;
+    const int64_t max_n = a.max_kv_len / a.ratio;
+    if (use_cta_path(a)) {
+        const int64_t nsm = max_n < 1 ? 1 : max_n;
+        const size_t smem = (size_t)nsm * 4;
+        for (int64_t q0 = 0; q0 < a.total_q; q0 += 1 << 30) {
+            const int64_t nq = a.total_q - q0 < (1 << 30) ? a.total_q - q0 : (1 << 30);
+            cudaError_t e = launch_kernel("index_topk_cta", index_topk_cta_kernel<DI>, dim3((unsigned)nq),
+                                          dim3(kCtaThreads), smem, st, a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0,
+                                          a.q_idx, a.k_idx, a.n_heads_idx, a.ratio, a.top_k, (int)nsm,
+                                          a.idx_out, a.score_out, a.err);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    const int64_t gq = group_size(a);
+    const int64_t nchunks = (max_n <= 0 ? 1 : (max_n + kScanChunk - 1) / kScanChunk);
+    WsD w = carve_wsd(a.ws, gq, max_n < 1 ? 1 : max_n, a.top_k);
+    for (int64_t q0 = 0; q0 < a.total_q; q0 += gq) {
+        const int64_t nq = a.total_q - q0 < gq ? a.total_q - q0 : gq;
+        dim3 grid((unsigned)nchunks, (unsigned)nq);
+        cudaError_t e = launch_kernel("index_scan", index_scan_kernel<DI>, grid, dim3(kScanThreads), 0, st,
+                                      a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0, a.q_idx, a.k_idx, a.n_heads_idx,
+                                      a.ratio, a.top_k, w, a.idx_out, a.score_out, a.err);
+        if (e != cudaSuccess) return e;
+        e = launch_kernel("index_filter", index_filter_kernel, grid, dim3(kScanThreads), 0, st, a.batch, a.cu_kv,
+                          a.cu_q, a.cu_csa, q0, a.ratio, a.top_k, w, a.idx_out, a.score_out, a.err);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+bool index_supported(int n_heads_idx, int d_idx, int top_k)
+{
+    return n_heads_idx >= 1 && n_heads_idx <= 16 && (d_idx == 32 || d_idx == 64 || d_idx == 128) && top_k >= 1 &&
+           top_k <= kMaxTopK;
+}
+
+size_t index_workspace_bytes(const IndexArgs &a)
+{
+    if (a.total_q <= 0 || use_cta_path(a)) return 0;
+    const int64_t max_n = a.max_kv_len / a.ratio;
+    return (size_t)wsd_total_bytes(group_size(a), max_n < 1 ? 1 : max_n, a.top_k);
+}
+
+cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t st)
+{
+    switch (a.d_idx) {
+    case 32: return launch_index_t<32>(a, st);
+    case 64: return launch_index_t<64>(a, st);
+    case 128: return launch_index_t<128>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace csa

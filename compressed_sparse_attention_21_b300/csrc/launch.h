@@ -1,0 +1,100 @@
+// Internal launch interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+namespace csa {
+
+// ---- per-kernel timing (diagnostics; off unless csa_timing_enable(1)) ----
+bool timing_enabled();
+void timing_record(const char *name, cudaEvent_t start, cudaEvent_t stop);
+
+// Raise a kernel's dynamic shared memory limit (remembered per kernel and device).
+cudaError_t ensure_smem_fn(const void *kern, size_t smem);
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(const char *name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, Args &&...args)
+{
+    cudaError_t e = cudaSuccess;
+    if (smem > 48 * 1024) {
+        e = ensure_smem_fn(reinterpret_cast<const void *>(kern), smem);
+        if (e != cudaSuccess) return e;
+    }
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    const bool timed = timing_enabled();
+    if (timed) {
+        cudaEventCreate(&e0);
+        cudaEventCreate(&e1);
+        cudaEventRecord(e0, st);
+    }
+    kern<<<grid, block, smem, st>>>(std::forward<Args>(args)...);
+    e = cudaGetLastError();
+    if (timed) {
+        cudaEventRecord(e1, st);
+        timing_record(name, e0, e1);
+    }
+    return e;
+}
+
+// ---- compression ----
+struct CompressArgs {
+    int batch;
+    int max_kv_len, max_q_len;
+    const int64_t *cu_kv, *cu_q;
+    const int64_t *cu_small, *cu_big;   // entry prefix arrays for the two ratios
+    int d;
+    int ratio_small;                    // 0 = none, else power of two <= 32
+    int ratio_big;                      // 0 = none, else 64 or 128
+    const uint16_t *kv;
+    const float *gate;
+    uint16_t *out_small, *out_big;
+    int *err;
+};
+bool compress_supported(int d, int ratio_small, int ratio_big);
+cudaError_t launch_compress(const CompressArgs &a, cudaStream_t st);
+
+// ---- indexer + top-k ----
+struct IndexArgs {
+    int batch;
+    int max_kv_len, max_q_len;
+    int64_t total_q;
+    const int64_t *cu_kv, *cu_q, *cu_csa;
+    const uint16_t *q_idx, *k_idx;
+    int n_heads_idx, d_idx, ratio, top_k;
+    int32_t *idx_out;
+    float *score_out;
+    void *ws;
+    size_t ws_bytes;
+    int *err;
+};
+bool index_supported(int n_heads_idx, int d_idx, int top_k);
+size_t index_workspace_bytes(const IndexArgs &a);
+cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t st);
+
+// ---- attention ----
+struct AttendArgs {
+    int batch;
+    int max_kv_len, max_q_len;
+    int64_t total_q;
+    const int64_t *cu_kv, *cu_q, *cu_ent;
+    const uint16_t *q, *entries, *kv;
+    const int32_t *idx;   // sparse: [total_q, top_k]; dense: nullptr
+    int n_heads, d, ratio, top_k;
+    float scale;
+    uint16_t *out;
+    float *lse;
+    void *ws;
+    size_t ws_bytes;
+    int *err;
+    int num_sms;          // SMs of the current device (sizes the split-KV grid)
+    int sm_share;         // SMs this launch may count on (concurrent branches)
+};
+bool attend_supported(int n_heads, int d);
+size_t attend_workspace_bytes(const AttendArgs &a);
+cudaError_t launch_attend(const AttendArgs &a, cudaStream_t st);
+
+}  // namespace csa

@@ -1,0 +1,248 @@
+/*
+ * csa.h -- C ABI of the B300 (sm_103a) CSA + HCA hybrid compressed attention.
+ *
+ * The operations follow the DeepSeek-V4 hybrid attention as described in
+ * "DeepSeek-V4 core architecture" (gitcode.csdn.net article):
+ *   §2.2 "CSA: compressed sparse attention"
+ *        step 1  token-level compression: every m adjacent tokens' KV become
+ *                one entry, weighted by learnable softmax-normalised weights;
+ *        step 2  lightning indexer: a light scorer rates each query against
+ *                every compressed entry and only the top-k entries are kept;
+ *        step 3  multi-query attention with shared KV: each selected entry is
+ *                both key and value, and all query heads share it;
+ *   §2.3 "HCA: heavily compressed attention": 128 tokens per entry, dense
+ *        attention over all entries, no selection; CSA and HCA alternate
+ *        across layers.
+ * and "DeepSeek V4's architecture debt chain" (vendordeep.com),
+ * "Constraint 1 -> Innovation 1" (many tokens' KV weighted into one
+ * compressed token at up to 128x).
+ *
+ * Where the pages leave a step open this library takes these readings:
+ *   - one scalar gate logit per token; the weights of a block are the
+ *     softmax of its tokens' logits; blocks are non-overlapping and aligned
+ *     at position 0; a trailing partial block has no entry;
+ *   - the indexer score of entry j for the query at t is the fp32 sum over
+ *     indexer heads h of q_{t,h} . k_j, with one indexer key per entry;
+ *   - an entry becomes visible only once its block is complete: entry j of
+ *     ratio m is visible to position t iff (j+1)*m <= t+1;
+ *   - each query also attends to the raw tokens of its own incomplete
+ *     block: r(t) = (t+1) mod m tokens, positions t-r(t)+1 .. t;
+ *   - top-k keeps the min(k, n(t)) highest scores, ties to the lower entry
+ *     index, and returns them in ascending index order padded with -1.
+ *
+ * Conventions shared by every call:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, row-major,
+ *     contiguous and 16-byte aligned.  bf16 tensors are passed as their raw
+ *     16-bit patterns (csa_bf16).  Rows of all sequences are packed.
+ *   - The library allocates no device memory.  Scratch space is the caller's
+ *     workspace (ws, ws_bytes), sized by the *_workspace_size calls.  It must
+ *     be zero-filled once before its first use (csa_workspace_init does
+ *     that); every call that returns CSA_OK leaves it zero-filled again.
+ *     After a call that failed, zero it again before reuse.
+ *   - Every call is asynchronous on the given stream and does not
+ *     synchronise.  Calls that share one workspace must not overlap in time.
+ *   - Every call returns a csa_status_t.  Argument errors are detected on the
+ *     host before anything is launched.  Layout inconsistencies that can only
+ *     be seen on the device (for example an entry count that does not equal
+ *     floor(L/m), or an index that is not visible) set the device error word,
+ *     which csa_check_device_error reads; the offending rows are skipped.
+ *   - The first call on a device creates one helper stream and two events
+ *     for that device (hybrid_attend runs its two branches concurrently on
+ *     them).  Make that first call outside any CUDA graph capture.
+ */
+#ifndef CSA_H
+#define CSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *csa_stream_t;
+
+/* Raw bf16 bit pattern. */
+typedef uint16_t csa_bf16;
+
+typedef enum csa_status {
+    CSA_OK = 0,
+    CSA_ERR_INVALID_ARG = 1,   /* bad pointer, size or layout value (host check) */
+    CSA_ERR_UNSUPPORTED = 2,   /* a size this build has no kernel for */
+    CSA_ERR_WORKSPACE = 3,     /* ws missing or smaller than required */
+    CSA_ERR_CUDA = 4,          /* a CUDA runtime call or a launch failed */
+    CSA_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out */
+    CSA_ERR_DEVICE = 6         /* device: layout inconsistency / invalid index */
+} csa_status_t;
+
+/*
+ * Packed variable-length batch.  Sequence b (0 <= b < batch) has
+ * L_b = cu_kv[b+1] - cu_kv[b] tokens at rows cu_kv[b] .. of the token
+ * tensors, n_q,b = cu_q[b+1] - cu_q[b] queries at rows cu_q[b] .. of the
+ * query tensors, and its compressed entries at rows cu_csa[b] .. and
+ * cu_hca[b] .. of the entry tensors.  The queries of a sequence are its
+ * LAST n_q,b positions: L_b - n_q,b .. L_b - 1 (n_q,b = L_b for a prefill,
+ * 1 for a decode step).  cu_csa[b+1] - cu_csa[b] must equal floor(L_b /
+ * ratio_csa) and likewise for cu_hca with ratio_hca.  The cu_* arrays are
+ * int64 device arrays of batch+1 elements starting at 0; the totals and
+ * maxima are host copies of what they imply (used to size grids without a
+ * device read).  A call that does not use a given array may pass NULL.
+ */
+typedef struct csa_layout {
+    int32_t batch;
+    int32_t max_kv_len;        /* max over b of L_b */
+    int32_t max_q_len;         /* max over b of n_q,b */
+    int32_t reserved;          /* must be 0 */
+    const int64_t *cu_kv;
+    const int64_t *cu_q;
+    const int64_t *cu_csa;
+    const int64_t *cu_hca;
+    int64_t total_kv;          /* cu_kv[batch] */
+    int64_t total_q;           /* cu_q[batch] */
+    int64_t total_csa;         /* cu_csa[batch] */
+    int64_t total_hca;         /* cu_hca[batch] */
+} csa_layout;
+
+/* ---------------------------------------------------------------------------
+ * Token-level compression (§2.2 step 1 with ratio m = 4; §2.3 with m = 128).
+ *
+ * For every block j whose last token is a query position of its sequence
+ * (position >= L_b - n_q,b), writes
+ *     out[cu_*[b] + j] = sum_{t in block j} softmax_block(gate)_t * kv[t]
+ * computed in fp32 and rounded to bf16 once.  With n_q = L (prefill) that is
+ * every complete block; with n_q = 1 (decode) it is the block completed by
+ * the newest token, if any.  Rows of `out` for other blocks are not touched.
+ *   kv    [total_kv, d] bf16     per-token KV vectors
+ *   gate  [total_kv]    fp32     per-token gate logits
+ *   out   [total_csa, d] bf16 (csa_compress, packed by cu_csa)
+ *         [total_hca, d] bf16 (hca_compress, packed by cu_hca)
+ *   d     128 or 512;  ratio a power of two in 1 .. 128.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_compress(const csa_layout *layout, const csa_bf16 *kv, const float *gate,
+                          int d, int ratio, csa_bf16 *out, csa_stream_t stream);
+csa_status_t hca_compress(const csa_layout *layout, const csa_bf16 *kv, const float *gate,
+                          int d, int ratio, csa_bf16 *out, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Lightning indexer + top-k (§2.2 step 2).
+ *
+ * For each query row i (position t of sequence b) over the visible entries
+ * j < n(t) = floor((t+1)/ratio):
+ *     s(i, j) = fp32 sum_{h < n_heads_idx} q_idx[i, h, :] . k_idx[cu_csa[b] + j, :]
+ * and writes the top min(top_k, n(t)) entries by (score desc, index asc) to
+ * idx_out[i, 0 .. top_k) as sequence-local entry indices in ascending
+ * order, padded with -1.  score_out (nullable) receives the fp32 score of
+ * each returned index (padding slots: -inf).
+ *   q_idx  [total_q, n_heads_idx, d_idx] bf16
+ *   k_idx  [total_csa, d_idx]            bf16   one key per CSA entry
+ *   (n_heads_idx, d_idx) in {(2,32), (4,64)} or any n_heads_idx <= 16 with
+ *   d_idx in {32, 64, 128};  1 <= top_k <= 2048.
+ * The full score matrix is never written out: decode-sized batches keep one
+ * score row per query in the workspace; prefill-sized batches keep it in
+ * shared memory.
+ * ------------------------------------------------------------------------- */
+csa_status_t lightning_index_topk(const csa_layout *layout, const csa_bf16 *q_idx,
+                                  const csa_bf16 *k_idx, int n_heads_idx, int d_idx,
+                                  int ratio, int top_k, int32_t *idx_out, float *score_out,
+                                  void *ws, size_t ws_bytes, csa_stream_t stream);
+csa_status_t csa_index_workspace_size(const csa_layout *layout, int n_heads_idx, int d_idx,
+                                      int ratio, int top_k, size_t *bytes);
+
+/* ---------------------------------------------------------------------------
+ * Sparse shared-KV multi-query attention (§2.2 step 3).
+ *
+ * Query row i at position t of sequence b attends, with every one of its
+ * n_heads heads, over the key set
+ *     { csa_entries[cu_csa[b] + idx[i, s]] : idx[i, s] >= 0 }
+ *   U { kv[cu_kv[b] + u] : t - r(t) < u <= t },  r(t) = (t+1) mod ratio,
+ * each key serving as its own value:
+ *     out[i, h] = sum_x softmax_x(scale * q[i, h] . x) x,
+ *     lse[i, h] = ln sum_x exp(scale * q[i, h] . x)
+ * idx rows are laid out as lightning_index_topk writes them: at most
+ * min(top_k, n(t)) valid entries first, then -1.  An index >= n(t) is not
+ * visible: it sets CSA_ERR_DEVICE and is skipped.
+ *   q      [total_q, n_heads, d] bf16
+ *   out    [total_q, n_heads, d] bf16;  lse [total_q, n_heads] fp32 (nullable)
+ *   d in {128, 512};  n_heads in {1 .. 16} or a multiple of 64 up to 256.
+ * ------------------------------------------------------------------------- */
+csa_status_t sparse_mqa_attend(const csa_layout *layout, const csa_bf16 *q,
+                               const csa_bf16 *csa_entries, const csa_bf16 *kv,
+                               const int32_t *idx, int n_heads, int d, int ratio, int top_k,
+                               float scale, csa_bf16 *out, float *lse,
+                               void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * HCA dense shared-KV multi-query attention (§2.3).
+ *
+ * Like sparse_mqa_attend with the key set
+ *     { hca_entries[cu_hca[b] + j] : j < floor((t+1)/ratio) }
+ *   U { kv[cu_kv[b] + u] : t - r(t) < u <= t },  r(t) = (t+1) mod ratio.
+ * ------------------------------------------------------------------------- */
+csa_status_t hca_dense_attend(const csa_layout *layout, const csa_bf16 *q,
+                              const csa_bf16 *hca_entries, const csa_bf16 *kv, int n_heads,
+                              int d, int ratio, float scale, csa_bf16 *out, float *lse,
+                              void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/* Workspace for one attention call (sparse: top_k > 0; dense: top_k = 0). */
+csa_status_t csa_attend_workspace_size(const csa_layout *layout, int n_heads, int d, int ratio,
+                                       int top_k, size_t *bytes);
+
+/* ---------------------------------------------------------------------------
+ * Hybrid step (§2.3: CSA and HCA layers alternate): runs, on the same
+ * inputs, compression into both caches (unless CSA_SKIP_COMPRESS), then the
+ * CSA branch (indexer, top-k, sparse attention) and the HCA branch (dense
+ * attention) concurrently, and returns both branches' outputs.
+ * ------------------------------------------------------------------------- */
+#define CSA_SKIP_COMPRESS 0x1   /* caches already hold every needed entry */
+
+typedef struct csa_hybrid_params {
+    csa_layout layout;
+    int32_t d, n_heads, n_heads_idx, d_idx;
+    int32_t ratio_csa, ratio_hca, top_k, flags;
+    float scale;
+    int32_t reserved;          /* must be 0 */
+    const csa_bf16 *kv;        /* [total_kv, d] */
+    const float *gate;         /* [total_kv] */
+    const csa_bf16 *q_idx;     /* [total_q, n_heads_idx, d_idx] */
+    const csa_bf16 *k_idx;     /* [total_csa, d_idx] */
+    const csa_bf16 *q;         /* [total_q, n_heads, d] */
+    csa_bf16 *csa_cache;       /* [total_csa, d]  written by compression */
+    csa_bf16 *hca_cache;       /* [total_hca, d]  written by compression */
+    int32_t *idx_out;          /* [total_q, top_k] */
+    float *score_out;          /* [total_q, top_k] or NULL */
+    csa_bf16 *o_csa;           /* [total_q, n_heads, d] */
+    float *lse_csa;            /* [total_q, n_heads] or NULL */
+    csa_bf16 *o_hca;           /* [total_q, n_heads, d] */
+    float *lse_hca;            /* [total_q, n_heads] or NULL */
+    void *ws;
+    size_t ws_bytes;
+} csa_hybrid_params;
+
+csa_status_t hybrid_attend(const csa_hybrid_params *params, csa_stream_t stream);
+csa_status_t csa_workspace_size(const csa_hybrid_params *params, size_t *bytes);
+
+/* Zero-fill a workspace (cudaMemsetAsync on `stream`). */
+csa_status_t csa_workspace_init(void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics.
+ * csa_check_device_error synchronises `stream`, then reads and clears the
+ * current device's error word (CSA_OK if no kernel reported anything).
+ * csa_timing_* time each kernel launch with CUDA events on the stream it
+ * runs on (disabled by default; only for eager, non-captured calls).
+ * ------------------------------------------------------------------------- */
+const char *csa_status_string(csa_status_t status);
+csa_status_t csa_check_device_error(csa_stream_t stream, csa_status_t *device_status);
+int csa_version(void);
+
+csa_status_t csa_timing_enable(int enable);
+/* Per kernel name: launches and total milliseconds since the last reset.
+ * Returns the number of distinct kernels; fills at most `cap` entries. */
+int csa_timing_read(int cap, const char **names, int64_t *launches, double *total_ms);
+void csa_timing_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_H */

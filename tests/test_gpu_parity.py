@@ -1,0 +1,280 @@
+"""GPU parity: every step of the CUDA path against the fp64 oracle, through the C ABI.
+
+Small ragged cases cover tiles, ragged tails, lengths below one block, exact
+block boundaries and n(t) <= k; the five workloads run at full size (the
+128K prefill on a sampled query set, every other workload on every query).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from compressed_sparse_attention_21_b300 import _lib as csa
+from compressed_sparse_attention_21_b300 import build as csa_build
+from compressed_sparse_attention_21_b300 import workloads as wl
+
+from . import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    csa_build.build()
+    csa.load()
+    oracle.build()
+    yield
+    assert csa.check_device_error() == 0
+
+
+def problem(lengths, n_q, H=8, d=128, HI=2, dI=32, k=16, mC=4, mH=128, seed=0, gate_std=1.0):
+    w = wl.Workload("case", len(lengths), list(lengths), False, H=H, d=d, HI=HI, dI=dI, top_k=k, mC=mC,
+                    mH=mH, gate_std=gate_std, seed=seed)
+    return wl.make_problem(w, n_q=n_q)
+
+
+RAGGED = [1, 3, 4, 5, 127, 128, 129, 300, 1000]
+
+
+# ---------------------------------------------------------------------------
+# a1: compression
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("d", [128, 512])
+@pytest.mark.parametrize("ratio,side", [(1, "csa"), (2, "csa"), (4, "csa"), (8, "csa"), (32, "csa"),
+                                        (64, "hca"), (128, "hca"), (4, "hca")])
+def test_compress_prefill(d, ratio, side):
+    p = problem(RAGGED, RAGGED, d=d, mC=ratio if side == "csa" else 4, mH=ratio if side == "hca" else 128,
+                seed=ratio)
+    g = P.GpuProblem(p)
+    inp = wl.to_numpy(p)
+    cu = inp["cu_csa"] if side == "csa" else inp["cu_hca"]
+    out = torch.full((int(cu[-1]), d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    (csa.csa_compress if side == "csa" else csa.hca_compress)(g.full, g.kv, g.gate, out, ratio=ratio)
+    torch.cuda.synchronize()
+    ref = oracle.compress_packed(inp["cu_kv"], cu, inp["kv"], inp["gate"], ratio)
+    err = np.abs(P.bf16_to_f64(out) - ref).max()
+    assert err <= P.ENTRY_TOL
+    # tighter: fp32 accumulation + one bf16 rounding stays within one bf16 ulp of the exact value
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+    assert (np.abs(P.bf16_to_f64(out) - ref) <= ulp + 1e-6).all()
+
+
+def test_compress_fused_and_decode_append():
+    lengths = [4, 127, 128, 260, 512, 777]
+    p = problem(lengths, [1] * len(lengths), d=512, seed=3)
+    g = P.GpuProblem(p)
+    inp = wl.to_numpy(p)
+    ref_c = oracle.compress_packed(inp["cu_kv"], inp["cu_csa"], inp["kv"], inp["gate"], 4)
+    ref_h = oracle.compress_packed(inp["cu_kv"], inp["cu_hca"], inp["kv"], inp["gate"], 128)
+    # decode layout: only the block closed by the newest token may be written
+    h = csa.Hybrid(g.layout, g.kv, g.gate, g.qI, g.kI, g.q, p["top_k"], p["scale"],
+                   csa_cache=torch.full((g.layout.total_csa, 512), 7.0, dtype=torch.bfloat16, device="cuda"),
+                   hca_cache=torch.full((g.layout.total_hca, 512), 7.0, dtype=torch.bfloat16, device="cuda"))
+    h()
+    torch.cuda.synchronize()
+    got_c, got_h = P.bf16_to_f64(h.csa_cache), P.bf16_to_f64(h.hca_cache)
+    for b, L in enumerate(lengths):
+        for j in range(L // 4):
+            row = inp["cu_csa"][b] + j
+            if (j + 1) * 4 == L:
+                assert np.abs(got_c[row] - ref_c[row]).max() <= P.ENTRY_TOL
+            else:
+                assert (got_c[row] == 7.0).all(), (b, j)
+        for j in range(L // 128):
+            row = inp["cu_hca"][b] + j
+            if (j + 1) * 128 == L:
+                assert np.abs(got_h[row] - ref_h[row]).max() <= P.ENTRY_TOL
+            else:
+                assert (got_h[row] == 7.0).all(), (b, j)
+
+
+# ---------------------------------------------------------------------------
+# a2/a3: indexer + top-k, both paths
+# ---------------------------------------------------------------------------
+def _check_index(p, idx, score):
+    inp = wl.to_numpy(p)
+    idx = idx.cpu().numpy()
+    score = score.cpu().numpy()
+    total_q = int(inp["cu_q"][-1])
+    orc = oracle.hybrid_queries(inp, do_hca=False)
+    kinds = {"equal": 0, "tie": 0, "fp32tie": 0}
+    for qi in range(total_q):
+        b = int(np.searchsorted(inp["cu_q"], qi, side="right") - 1)
+        L = inp["cu_kv"][b + 1] - inp["cu_kv"][b]
+        t = L - (inp["cu_q"][b + 1] - inp["cu_q"][b]) + (qi - inp["cu_q"][b])
+        n = int((t + 1) // p["mC"])
+        kseq = inp["kI"][inp["cu_csa"][b]:inp["cu_csa"][b] + n]
+        s = oracle.index_scores(inp["qI"][qi], kseq) if n else np.zeros(0)
+        kind, _ = P.check_topk_row(idx[qi], orc["idx"][qi], s, n, p["top_k"], inp["qI"][qi], kseq)
+        kinds[kind] += 1
+        v = idx[qi] >= 0
+        # returned scores are the fp32 scores of the returned indices
+        assert np.allclose(score[qi][v], s[idx[qi][v]], rtol=1e-5, atol=1e-3)
+        assert np.isneginf(score[qi][~v]).all()
+    return kinds
+
+
+@pytest.mark.parametrize("HI,dI,k", [(2, 32, 64), (4, 64, 512), (4, 64, 1024), (1, 128, 7)])
+def test_index_topk_multi_cta_path(HI, dI, k):
+    lengths = [1, 5, 100, 4096, 5001, 20000, 70001]
+    p = problem(lengths, [1] * len(lengths), HI=HI, dI=dI, k=k, seed=11)
+    g = P.GpuProblem(p)
+    idx, score = csa.lightning_index_topk(g.layout, g.qI, g.kI, k)
+    torch.cuda.synchronize()
+    kinds = _check_index(p, idx, score)
+    assert kinds["equal"] >= len(lengths) - 1
+
+
+@pytest.mark.parametrize("HI,dI,k", [(2, 32, 64), (4, 64, 512)])
+def test_index_topk_cta_path(HI, dI, k):
+    lengths = [1500, 700]                  # 2200 queries: the per-query CTA path
+    p = problem(lengths, lengths, HI=HI, dI=dI, k=k, seed=12)
+    g = P.GpuProblem(p)
+    idx, score = csa.lightning_index_topk(g.layout, g.qI, g.kI, k)
+    torch.cuda.synchronize()
+    _check_index(p, idx, score)
+
+
+@pytest.mark.parametrize("queries", ["decode", "prefill"])
+def test_index_topk_all_ties_lowest_index_wins(queries):
+    lengths = [3000, 4100] if queries == "prefill" else [3000, 4100, 9000]
+    p = problem(lengths, lengths if queries == "prefill" else [1] * len(lengths), HI=2, dI=32, k=64, seed=13)
+    p["kI"] = torch.ones_like(p["kI"])      # every entry scores the same
+    g = P.GpuProblem(p)
+    idx, _ = csa.lightning_index_topk(g.layout, g.qI, g.kI, 64)
+    idx = idx.cpu().numpy()
+    for qi in range(idx.shape[0]):
+        b = int(np.searchsorted(g.layout.host["cu_q"], qi, side="right") - 1)
+        L = lengths[b]
+        t = L - g.layout.n_q[b] + (qi - g.layout.host["cu_q"][b])
+        n = (t + 1) // 4
+        want = list(range(min(64, n))) + [-1] * (64 - min(64, n))
+        assert list(idx[qi]) == want
+
+
+# ---------------------------------------------------------------------------
+# a4/a5: attention, on the oracle's own selection
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("H,d", [(8, 128), (8, 512), (64, 512), (128, 512), (64, 128)])
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_attend_parity(H, d, mode):
+    lengths = [1, 3, 4, 129, 1000, 5003] if mode == "decode" else [1, 130, 257]
+    n_q = [1] * len(lengths) if mode == "decode" else lengths
+    k = 64 if mode == "prefill" else 128
+    p = problem(lengths, n_q, H=H, d=d, k=k, seed=H + d)
+    g = P.GpuProblem(p)
+    inp = wl.to_numpy(p)
+    csa_cache, hca_cache = g.build_caches()
+    orc_hca = oracle.compress_packed(inp["cu_kv"], inp["cu_hca"], inp["kv"], inp["gate"], 128)
+    orc = oracle.hybrid_queries(inp, hca_entries=orc_hca)
+    idx = torch.from_numpy(orc["idx"]).cuda()
+    oC, lC = csa.sparse_mqa_attend(g.layout, g.q, csa_cache, g.kv, idx, k, p["scale"])
+    oH, lH = csa.hca_dense_attend(g.layout, g.q, hca_cache, g.kv, p["scale"])
+    torch.cuda.synchronize()
+    P.assert_att(P.bf16_to_f64(oC), orc["oC"], "sparse")
+    P.assert_att(P.bf16_to_f64(oH), orc["oH"], "dense")
+    assert np.abs(lC.cpu().numpy() - orc["lseC"]).max() <= 1e-2
+    assert np.abs(lH.cpu().numpy() - orc["lseH"]).max() <= 1e-2
+
+
+def test_attend_invisible_index_is_reported_and_skipped():
+    p = problem([64, 64], [1, 1], k=8, seed=21)
+    g = P.GpuProblem(p)
+    csa_cache, _ = g.build_caches()
+    idx = torch.full((2, 8), -1, dtype=torch.int32, device="cuda")
+    idx[:, 0] = 3
+    idx[1, 1] = 16                           # n(63) = 16: index 16 is not visible
+    csa.sparse_mqa_attend(g.layout, g.q, csa_cache, g.kv, idx, 8, p["scale"])
+    assert csa.check_device_error() == 6
+    assert csa.check_device_error() == 0    # reading clears it
+
+
+# ---------------------------------------------------------------------------
+# a6: the hybrid step
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", ["prefill_small", "decode_small", "chunked"])
+def test_hybrid_small(case):
+    if case == "prefill_small":
+        p = problem([1, 200, 513], [1, 200, 513], H=64, d=512, HI=4, dI=64, k=32, seed=31)
+    elif case == "decode_small":
+        p = problem([4, 4097, 8191, 30001], [1] * 4, H=128, d=512, HI=4, dI=64, k=256, seed=32)
+    else:
+        p = problem([1000, 2000], [37, 300], H=64, d=512, HI=4, dI=64, k=64, seed=33)
+    g = P.GpuProblem(p)
+    h = g.hybrid(prebuilt=case != "prefill_small")
+    rep = P.check_hybrid(p, h)
+    assert rep["topk"]["equal"] >= rep["queries"] - 2
+    # a second call on the same workspace gives the same answer (counters were left clean)
+    o1 = h.o_csa.clone()
+    h()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, h.o_csa)
+
+
+def test_hybrid_ratio_one_is_dense_causal():
+    # m_C = 1, k >= L: the CSA branch is dense causal MQA (and so is HCA with m_H = 1)
+    L = 300
+    p = problem([L], [L], H=8, d=128, k=512, mC=1, mH=1, seed=34)
+    g = P.GpuProblem(p)
+    h = g.hybrid(prebuilt=False)
+    q = P.bf16_to_f64(g.q).transpose(1, 0, 2)[None]
+    kvf = P.bf16_to_f64(g.kv)[None, None].repeat(8, 1)
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q), torch.from_numpy(kvf),
+                                                           torch.from_numpy(kvf), is_causal=True,
+                                                           scale=p["scale"])[0].permute(1, 0, 2).numpy()
+    P.assert_att(P.bf16_to_f64(h.o_csa), ref, "CSA m=1")
+    P.assert_att(P.bf16_to_f64(h.o_hca), ref, "HCA m=1")
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size
+# ---------------------------------------------------------------------------
+def sample_queries(L, n, seed):
+    """Boundary-heavy query sample for a long prefill (positions t of one sequence)."""
+    fixed = set(range(16)) | set(range(L - 16, L))
+    fixed |= {t for t in range(512) if t % 4 in (2, 3) or t % 128 in (126, 127)}
+    fixed |= set(range(4090, 4111)) | set(range(8180, 8201))
+    fixed = sorted(t for t in fixed if t < L)
+    rng = np.random.default_rng(seed + 100)
+    rest = np.setdiff1d(np.arange(L), fixed)
+    extra = rng.choice(rest, size=max(0, n - len(fixed)), replace=False)
+    return np.sort(np.concatenate([fixed, extra]).astype(np.int64))[:max(n, len(fixed))]
+
+
+def _workload_check(name, eval_q=None, entries="all"):
+    w = wl.WORKLOADS[name]
+    p = wl.make_problem(w)
+    g = P.GpuProblem(p)
+    h = g.hybrid(prebuilt=w.decode)
+    rep = P.check_hybrid(p, h, eval_q=eval_q, check_entries=entries)
+    assert csa.check_device_error() == 0
+    print(name, rep)
+    return rep
+
+
+def test_workload_prefill_4k_every_query():
+    rep = _workload_check("prefill_4k")
+    assert rep["queries"] == 4096
+
+
+def test_workload_decode_64k_every_query():
+    _workload_check("decode_64k", entries="sampled")
+
+
+@pytest.mark.slow
+def test_workload_ragged_decode_every_query():
+    _workload_check("ragged_decode", entries="sampled")
+
+
+@pytest.mark.slow
+def test_workload_decode_1m_every_query():
+    _workload_check("decode_1m", entries="sampled")
+
+
+@pytest.mark.slow
+def test_workload_prefill_128k_sampled_queries():
+    eval_q = sample_queries(131072, 1024, wl.WORKLOADS["prefill_128k"].seed)
+    rep = _workload_check("prefill_128k", eval_q=eval_q, entries="sampled")
+    assert rep["queries"] >= 1024
