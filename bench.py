@@ -1,0 +1,505 @@
+#!/usr/bin/env python3
+"""Benchmark of the CSA + HCA hybrid attention step on B300.
+
+One step = one ``hybrid_attend`` over one batch: compression of the blocks the
+step's tokens close, the lightning indexer and top-k, sparse shared-KV MQA
+and HCA dense MQA.  Default workload: 64K-context decode, batch 16 (H=64,
+d=512, indexer 4x64, top-k 512), caches built before the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own batch
+(independent sequences: weak scaling, no collective on the data path); the
+reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA+HCA attention tokens/s at 64K–1M ctx; % of HBM / tensor-core roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM traffic per launch of the dominant kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel name, with
+# the sha256 of the kernel's source file at capture time; a changed source
+# makes the figure stale and it is reported as null.
+NCU_TRAFFIC = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="decode_64k")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--copies", type=int, default=8, help="rotating state copies (decode)")
+    ap.add_argument("--min-seconds", type=float, default=2.0, help="repeat the K-step region this long")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (bytes and flops) of one step, per kernel
+# ---------------------------------------------------------------------------
+def step_work(p):
+    """Algorithmic bytes/flops of one hybrid step on problem p (dict from workloads)."""
+    H, d, HI, dI, k, mC, mH = p["H"], p["d"], p["HI"], p["dI"], p["top_k"], p["mC"], p["mH"]
+    w = {"compress": 0, "index_scan": 0, "sparse_attend": 0, "dense_attend": 0}
+    flops = {"index": 0, "sparse": 0, "dense": 0}
+    for L, nq in zip(p["lengths"], p["n_q"]):
+        lo = L - nq
+        # compression: tokens of blocks closed by query positions are read once, entries written once
+        n_blk_c = L // mC - lo // mC if nq else 0
+        n_blk_h = L // mH - lo // mH if nq else 0
+        tok = max(n_blk_c * mC, n_blk_h * mH)
+        w["compress"] += 2 * d * tok + 4 * tok + 2 * d * (n_blk_c + n_blk_h)
+        for t in range(lo, L):
+            nC, rC = (t + 1) // mC, (t + 1) % mC
+            nH, rH = (t + 1) // mH, (t + 1) % mH
+            sel = min(k, nC)
+            w["index_scan"] += 2 * (HI * dI + nC * dI) + 4 * k
+            w["sparse_attend"] += 2 * ((sel + rC) * d + 2 * H * d) + 4 * k + 4 * H
+            w["dense_attend"] += 2 * ((nH + rH) * d + 2 * H * d) + 4 * H
+            flops["index"] += 2 * dI * nC
+            flops["sparse"] += 4 * H * d * (sel + rC)
+            flops["dense"] += 4 * H * d * (nH + rH)
+    return w, flops
+
+
+def step_work_fast(p):
+    """Closed-form version of step_work for prefill-sized problems (same counts)."""
+    if sum(p["n_q"]) <= 4096:
+        return step_work(p)
+    H, d, HI, dI, k, mC, mH = p["H"], p["d"], p["HI"], p["dI"], p["top_k"], p["mC"], p["mH"]
+    import numpy as np
+    w = {"compress": 0, "index_scan": 0, "sparse_attend": 0, "dense_attend": 0}
+    flops = {"index": 0, "sparse": 0, "dense": 0}
+    for L, nq in zip(p["lengths"], p["n_q"]):
+        lo = L - nq
+        t = np.arange(lo, L, dtype=np.int64)
+        nC, rC = (t + 1) // mC, (t + 1) % mC
+        nH, rH = (t + 1) // mH, (t + 1) % mH
+        sel = np.minimum(k, nC)
+        n_blk_c, n_blk_h = L // mC - lo // mC, L // mH - lo // mH
+        tok = max(n_blk_c * mC, n_blk_h * mH)
+        w["compress"] += 2 * d * tok + 4 * tok + 2 * d * (n_blk_c + n_blk_h)
+        w["index_scan"] += int((2 * (HI * dI + nC * dI) + 4 * k).sum())
+        w["sparse_attend"] += int((2 * ((sel + rC) * d + 2 * H * d) + 4 * k + 4 * H).sum())
+        w["dense_attend"] += int((2 * ((nH + rH) * d + 2 * H * d) + 4 * H).sum())
+        flops["index"] += int((2 * dI * nC).sum())
+        flops["sparse"] += int((4 * H * d * (sel + rC)).sum())
+        flops["dense"] += int((4 * H * d * (nH + rH)).sum())
+    return w, flops
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# oracle on the host cores
+# ---------------------------------------------------------------------------
+def oracle_sample(p, n_queries):
+    """Inputs restricted to the first n_queries decode sequences (a bounded sample)."""
+    from compressed_sparse_attention_21_b300 import workloads as wl
+    import numpy as np
+    inp = wl.to_numpy(p)
+    if n_queries >= int(inp["cu_q"][-1]):
+        return inp, np.arange(int(inp["cu_q"][-1]))
+    # keep the sequences that own the first n_queries queries
+    b_last = int(np.searchsorted(inp["cu_q"], n_queries - 1, side="right") - 1)
+    B = b_last + 1
+    sub = dict(inp)
+    for key in ("cu_kv", "cu_q", "cu_csa", "cu_hca"):
+        sub[key] = inp[key][:B + 1]
+    sub["kv"] = inp["kv"][:inp["cu_kv"][B]]
+    sub["gate"] = inp["gate"][:inp["cu_kv"][B]]
+    sub["qI"] = inp["qI"][:inp["cu_q"][B]]
+    sub["q"] = inp["q"][:inp["cu_q"][B]]
+    sub["kI"] = inp["kI"][:inp["cu_csa"][B]]
+    return sub, np.arange(n_queries)
+
+
+def time_oracle(p, target_s=10.0, max_reps=50, n_queries=None):
+    import oracle
+    oracle.build()
+    total_q = sum(p["n_q"])
+    nq = total_q if n_queries is None else min(n_queries, total_q)
+    inp, eval_q = oracle_sample(p, nq)
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle.hybrid_queries(inp, eval_q=eval_q)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all >= target_s or len(times) >= max_reps:
+            break
+    per = statistics.mean(times)
+    return {"value": nq / per, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{nq} of {total_q} queries of {p['workload']}, whole step from raw inputs "
+                      f"(compression of every block the queries need, indexer, top-k, both attentions), "
+                      f"{len(times)} repetitions, {sum(times):.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    from compressed_sparse_attention_21_b300 import workloads as wl
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = wl.WORKLOADS[args.workload]
+    p = wl.make_problem(w)
+    inp, eval_q = oracle_sample(p, 1)
+    for _ in range(max(args.warmup, 0)):
+        oracle.hybrid_queries(inp, eval_q=eval_q)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.hybrid_queries(inp, eval_q=eval_q)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, p),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"one decode query of {w.name} per step (whole step from raw inputs)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, p):
+    return {"workload": w.name, "batch": w.batch, "ctx": (max(p["lengths"]) if w.lengths is None else w.lengths[0]),
+            "lengths": "uniform [32768,131072], not multiples of 128" if w.lengths is None else "fixed",
+            "queries_per_seq": "1 (decode)" if w.decode else "all positions (prefill)", "H": w.H, "d": w.d,
+            "indexer": f"{w.HI}x{w.dI}", "top_k": w.top_k, "ratio_csa": w.mC, "ratio_hca": w.mH,
+            "gate_std": w.gate_std, "seed": w.seed}
+
+
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    from compressed_sparse_attention_21_b300 import _lib as csa
+    from compressed_sparse_attention_21_b300 import build as csa_build
+    from compressed_sparse_attention_21_b300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        csa_build.build()
+    if world > 1:
+        dist.barrier()
+    csa.load()
+
+    w = wl.WORKLOADS[args.workload]
+    p = wl.make_problem(w)                 # each rank serves its own batch of the same shape
+    peaks, peak_src = load_peaks()
+
+    # CPU baseline first (oracle threads run before heavy GPU work; rank 0 only, N=1 only)
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = time_oracle(p, target_s=10.0, n_queries=None if w.decode else 64)
+
+    layout = csa.Layout(p["lengths"], p["n_q"], w.mC, w.mH, device=dev)
+    full = csa.Layout(p["lengths"], p["lengths"], w.mC, w.mH, device=dev)
+    base = {k: p[k].to(dev) for k in ("kv", "gate", "qI", "kI", "q")}
+    ncopies = max(1, args.copies if w.decode else 1)
+    copies = []
+    for c in range(ncopies):
+        t = {k: (v if c == 0 else v.clone()) for k, v in base.items()}
+        csa_cache = torch.empty((full.total_csa, w.d), dtype=torch.bfloat16, device=dev)
+        hca_cache = torch.empty((full.total_hca, w.d), dtype=torch.bfloat16, device=dev)
+        if w.decode:   # caches hold every entry before the step (built by a prefill-shaped call)
+            csa.csa_compress(full, t["kv"], t["gate"], csa_cache)
+            csa.hca_compress(full, t["kv"], t["gate"], hca_cache)
+        h = csa.Hybrid(layout, t["kv"], t["gate"], t["qI"], t["kI"], t["q"], w.top_k, w.scale,
+                       csa_cache=csa_cache, hca_cache=hca_cache)
+        copies.append(h)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    # cache build time (prefill-shaped compression of the whole context), reported apart
+    cache_build_ms = None
+    if w.decode:
+        h0 = copies[0]
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            csa.csa_compress(full, h0.kv, h0.gate, h0.csa_cache)
+            csa.hca_compress(full, h0.kv, h0.gate, h0.hca_cache)
+        ev0.record()
+        for _ in range(10):
+            csa.csa_compress(full, h0.kv, h0.gate, h0.csa_cache)
+            csa.hca_compress(full, h0.kv, h0.gate, h0.hca_cache)
+        ev1.record()
+        torch.cuda.synchronize()
+        cache_build_ms = ev0.elapsed_time(ev1) / 10
+
+    # warm-up (eager; also creates the library's per-device stream/events)
+    for i in range(max(args.warmup, 3)):
+        copies[i % ncopies]()
+    torch.cuda.synchronize()
+
+    # one CUDA graph replays one step on each copy in turn
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for h in copies:
+            h()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    def timed_region(K):
+        """Exactly K steps (graph replays of ncopies steps plus eager remainder)."""
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        full_reps, rem = divmod(K, ncopies)
+        for _ in range(full_reps):
+            graph.replay()
+        for i in range(rem):
+            copies[i]()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms = float(tt.item())
+        return ms
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    reps = []
+    t_start = time.perf_counter()
+    while True:
+        reps.append(timed_region(args.steps))
+        if time.perf_counter() - t_start >= args.min_seconds and len(reps) >= 3:
+            break
+    clocks = sampler.stop()
+    ms_region = statistics.median(reps)
+    ms_step = ms_region / args.steps
+    tokens_per_step = sum(p["n_q"])
+    value = tokens_per_step * world / (ms_step * 1e-3)
+
+    # per-kernel durations: an instrumented eager pass (events on each launch's stream)
+    csa.timing_reset()
+    csa.timing_enable(True)
+    for i in range(args.steps):
+        copies[i % ncopies]()
+    torch.cuda.synchronize()
+    kt = csa.timing_read()
+    csa.timing_enable(False)
+    csa.timing_reset()
+    launches_per_step = sum(n for n, _ in kt.values()) / args.steps
+
+    work, flops = step_work_fast(p)
+    kernel_bytes = {"compress": work["compress"], "index_scan": work["index_scan"],
+                    "sparse_attend": work["sparse_attend"], "dense_attend": work["dense_attend"]}
+    kernels = {}
+    for name, (n, ms) in kt.items():
+        per_launch = ms / n
+        per_step_launches = n / args.steps
+        entry = {"launches_per_step": per_step_launches, "avg_us": per_launch * 1e3}
+        if name in kernel_bytes and per_step_launches > 0:
+            b = kernel_bytes[name] / per_step_launches
+            entry["alg_bytes_per_launch"] = b
+            entry["alg_GBps"] = b / (per_launch * 1e-3) / 1e9
+        kernels[name] = entry
+    step_bytes = sum(work.values())
+    step_flops = sum(flops.values())
+
+    # dominant kernel and its roofline
+    dom = max(kt.items(), key=lambda kv: kv[1][1])[0]
+    n_dom, ms_dom = kt[dom]
+    avg_dom_s = ms_dom / n_dom * 1e-3
+    if w.decode or dom not in ("sparse_attend", "dense_attend"):
+        if dom in kernel_bytes:
+            alg = kernel_bytes[dom] / (n_dom / args.steps)
+        else:
+            alg = 0.0
+        achieved = alg / avg_dom_s / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"hbm_gbs ({peak_src})",
+                "alg_bytes_per_launch": alg}
+    else:
+        fl = flops["sparse" if dom == "sparse_attend" else "dense"] / (n_dom / args.steps)
+        achieved = fl / avg_dom_s / 1e12
+        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"bf16_tflops_sustained ({peak_src})",
+                "alg_flops_per_launch": fl}
+    traffic = None
+    t_rec = NCU_TRAFFIC.get(dom)
+    if t_rec:
+        src = os.path.join(ROOT, "compressed_sparse_attention_21_b300", "csrc", t_rec["source"])
+        if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest() == t_rec["sha256"]:
+            traffic = t_rec["bytes_per_launch"] * t_rec.get("scale", 1.0)
+    roof["traffic"] = traffic
+
+    # whole-step roofline (context)
+    step_roof = {"alg_bytes": step_bytes, "alg_flops": step_flops,
+                 "GBps": step_bytes / (ms_step * 1e-3) / 1e9,
+                 "frac_hbm_measured": step_bytes / (ms_step * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+                 "frac_hbm_8TBps": step_bytes / (ms_step * 1e-3) / 8e12,
+                 "TFLOPs": step_flops / (ms_step * 1e-3) / 1e12}
+
+    # end to end through the public API with host buffers (pinned), eager calls
+    e2e = None
+    if not args.no_e2e:
+        h = copies[0]
+        q_host = p["q"].pin_memory()
+        qI_host = p["qI"].pin_memory()
+        oC_host = torch.empty(h.o_csa.shape, dtype=h.o_csa.dtype).pin_memory()
+        oH_host = torch.empty(h.o_hca.shape, dtype=h.o_hca.dtype).pin_memory()
+        lC_host = torch.empty(h.lse_csa.shape, dtype=torch.float32).pin_memory()
+        lH_host = torch.empty(h.lse_hca.shape, dtype=torch.float32).pin_memory()
+        bi = q_host.numel() * 2 + qI_host.numel() * 2
+        bo = (oC_host.numel() + oH_host.numel()) * 2 + (lC_host.numel() + lH_host.numel()) * 4
+
+        def e2e_step(hh):
+            hh.q.copy_(q_host, non_blocking=True)
+            hh.q_idx.copy_(qI_host, non_blocking=True)
+            hh()
+            oC_host.copy_(hh.o_csa, non_blocking=True)
+            oH_host.copy_(hh.o_hca, non_blocking=True)
+            lC_host.copy_(hh.lse_csa, non_blocking=True)
+            lH_host.copy_(hh.lse_hca, non_blocking=True)
+
+        for i in range(3):
+            e2e_step(copies[i % ncopies])
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(args.steps):
+            e2e_step(copies[i % ncopies])
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms = float(tt.item())
+        e2e = {"value": tokens_per_step * world / (ms / args.steps * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": ms / args.steps,
+               "path": "eager hybrid_attend calls through the C ABI, pinned host q/q_idx in, "
+                       "both outputs and LSEs out, one stream"}
+
+    touched = step_bytes
+    cfg = workload_config(w, p)
+    cfg["l2"] = (f"{ncopies} rotating copies of the step state; {touched / 2**20:.1f} MiB algorithmic per step, "
+                 f"{ncopies * touched / 2**20:.0f} MiB per rotation vs 126 MB L2") if ncopies > 1 else \
+        "inputs larger than L2"
+    cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg, "roofline": roof,
+            "step_roofline": step_roof, "cpu_baseline": cpu_base, "e2e": e2e,
+            "gpu_launches": int(round(launches_per_step * args.steps)), "launches_per_step": launches_per_step,
+            "kernels": kernels, "clocks": clocks, "cache_build_ms": cache_build_ms,
+            "timed_region_reps": len(reps), "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
+                                                      "bf16_tflops": peaks["bf16_tflops"]}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

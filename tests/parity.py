@@ -2,7 +2,9 @@
 fp64 oracle on the same seeded inputs.
 
 Acceptance (per query or entry):
-  * compressed entries: max abs error <= 1e-2;
+  * compressed entries: max abs error <= 1e-2, or half a bf16 ulp of the
+    value (+1e-5) where that is larger (|e| >= 4: the bf16 cache format
+    cannot hold such values to 1e-2);
   * top-k: the index sets are equal, except swaps whose oracle scores lie
     within 1e-4 relative of the oracle's k-th score; every index is visible,
     none repeats, and there are exactly min(k, n(t)) of them.  Swaps outside
@@ -31,6 +33,26 @@ U32 = 2.0 ** -24
 
 def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().double().numpy()
+
+
+def half_ulp_bf16(x):
+    """Half the bf16 spacing at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(ax)) - 8)
+
+
+def entry_err(gpu, ref):
+    """Max abs error of stored bf16 entries, and the worst ratio to the allowed bound.
+
+    The bound is 1e-2, widened to half a bf16 ulp of the value (plus 1e-5 for
+    the fp32 accumulation) where the storage format alone cannot meet 1e-2:
+    for |e| >= 4 one bf16 rounding can move a value by up to 2^-6.
+    """
+    err = np.abs(gpu - ref)
+    if err.size == 0:
+        return 0.0, 0.0
+    bound = np.maximum(ENTRY_TOL, half_ulp_bf16(np.maximum(np.abs(gpu), np.abs(ref))) + 1e-5)
+    return float(err.max()), float((err / bound).max())
 
 
 class GpuProblem:
@@ -141,18 +163,18 @@ def check_hybrid(p, h: "csa.Hybrid", eval_q=None, check_entries="all", entry_sam
     if check_entries == "all":
         gpu_csa = h.csa_cache.cpu()
         orc_csa = oracle.compress_packed(inp["cu_kv"], inp["cu_csa"], inp["kv"], inp["gate"], p["mC"])
-        e_csa = float(np.abs(bf16_to_f64(gpu_csa) - orc_csa).max()) if orc_csa.size else 0.0
+        e_csa, r_csa = entry_err(bf16_to_f64(gpu_csa), orc_csa)
     else:
         rng = np.random.default_rng(seed)
         n_csa = h.csa_cache.shape[0]
         ent = np.unique(np.concatenate([rng.integers(0, n_csa, entry_sample or 4096), [0, n_csa - 1]]))
         orc = oracle.compress_selected(inp["cu_kv"], inp["cu_csa"], inp["kv"], inp["gate"], p["mC"], ent)
         sel = h.csa_cache[torch.from_numpy(ent).to(h.csa_cache.device)].cpu()
-        e_csa = float(np.abs(bf16_to_f64(sel) - orc).max())
+        e_csa, r_csa = entry_err(bf16_to_f64(sel), orc)
     orc_hca = oracle.compress_packed(inp["cu_kv"], inp["cu_hca"], inp["kv"], inp["gate"], p["mH"])
-    e_hca = float(np.abs(bf16_to_f64(gpu_hca) - orc_hca).max()) if orc_hca.size else 0.0
-    assert e_csa <= ENTRY_TOL, f"CSA entries max abs {e_csa}"
-    assert e_hca <= ENTRY_TOL, f"HCA entries max abs {e_hca}"
+    e_hca, r_hca = entry_err(bf16_to_f64(gpu_hca), orc_hca)
+    assert r_csa <= 1.0, f"CSA entries max abs {e_csa}"
+    assert r_hca <= 1.0, f"HCA entries max abs {e_hca}"
     rep["entry_err_csa"], rep["entry_err_hca"] = e_csa, e_hca
 
     # --- oracle on its own selection ---
