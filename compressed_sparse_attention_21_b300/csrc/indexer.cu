@@ -46,7 +46,7 @@ __host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + 
 struct WsD {
     uint32_t *keys;   // [gq][key_stride]
     uint32_t *hist;   // [gq][kHistBins]          zero between calls
-    uint32_t *meta;   // [gq][kMetaWords]         words 0..3 zero between calls
+    uint32_t *meta;   // [gq][kMetaWords]         zero between calls
     uint64_t *sel;    // [gq][top_k]
     uint64_t *cand;   // [gq][cand_stride]
     int64_t key_stride, cand_stride;
@@ -546,11 +546,14 @@ index_filter_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
         idx_row[i] = v ? s_idx[i] : -1;
         if (sc_row) sc_row[i] = v ? key_score(s_key[i]) : -INFINITY;
     }
-    // leave the counters zeroed for the next call
+    // leave the counters and the boundary record zeroed for the next call (every
+    // other CTA of this query read meta[4] before taking its ticket)
     if (tid == 0) {
         meta[1] = 0;
         meta[2] = 0;
         meta[3] = 0;
+        meta[4] = 0;
+        meta[5] = 0;
     }
 }
 
