@@ -48,6 +48,7 @@ class csa_hybrid_params(ctypes.Structure):
 
 # Every symbol include/csa.h declares (checked by the CPU test suite).
 EXPORTS = ("csa_compress", "hca_compress", "lightning_index_topk", "csa_index_workspace_size",
+           "lightning_index_topk_static",
            "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size", "hybrid_attend",
            "csa_workspace_size", "csa_workspace_init", "csa_status_string", "csa_check_device_error",
            "csa_version", "csa_timing_enable", "csa_timing_read", "csa_timing_reset")
@@ -68,6 +69,7 @@ def load():
     lib.hca_compress.argtypes = [LP, P, P, I, I, P, P]
     lib.lightning_index_topk.argtypes = [LP, P, P, I, I, I, I, P, P, P, Z, P]
     lib.csa_index_workspace_size.argtypes = [LP, I, I, I, I, ctypes.POINTER(Z)]
+    lib.lightning_index_topk_static.argtypes = [LP, P, P, I, I, I, I, P, P, P]
     lib.sparse_mqa_attend.argtypes = [LP, P, P, P, P, I, I, I, I, F, P, P, P, Z, P]
     lib.hca_dense_attend.argtypes = [LP, P, P, P, I, I, I, F, P, P, P, Z, P]
     lib.csa_attend_workspace_size.argtypes = [LP, I, I, I, I, ctypes.POINTER(Z)]
@@ -84,7 +86,8 @@ def load():
     lib.csa_timing_read.restype = I
     lib.csa_timing_reset.restype = None
     for f in ("csa_compress", "hca_compress", "lightning_index_topk", "csa_index_workspace_size",
-              "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size", "hybrid_attend",
+              "lightning_index_topk_static", "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size",
+              "hybrid_attend",
               "csa_workspace_size", "csa_workspace_init", "csa_check_device_error", "csa_timing_enable"):
         getattr(lib, f).restype = I
     _lib = lib
@@ -202,6 +205,30 @@ def lightning_index_topk(layout, q_idx, k_idx, top_k, idx_out=None, score_out=No
     _check(load().lightning_index_topk(ctypes.byref(layout.c), _ptr(q_idx), _ptr(k_idx), HI, dI, ratio, top_k,
                                        _ptr(idx_out), _ptr(score_out), _ptr(ws), nb, _stream(stream)),
            "lightning_index_topk")
+    return idx_out, score_out
+
+
+STATIC_SCRATCH_BYTES = 32 << 20   # CSA_INDEX_STATIC_SCRATCH_BYTES
+
+
+def lightning_index_topk_static(layout, q_idx, k_idx, top_k, idx_out=None, score_out=None, ratio=None, stream=None,
+                                with_scores=True):
+    """lightning_index_topk for callers that cannot allocate device memory.
+
+    The library takes the scratch from its own fixed device array, so no
+    workspace is passed or allocated for the call itself; only the outputs
+    are created here when the caller does not pass them.
+    """
+    ratio = layout.ratio_csa if ratio is None else ratio
+    dev = q_idx.device
+    if idx_out is None:
+        idx_out = torch.empty((layout.total_q, top_k), dtype=torch.int32, device=dev)
+    if score_out is None and with_scores:
+        score_out = torch.empty((layout.total_q, top_k), dtype=torch.float32, device=dev)
+    HI, dI = q_idx.shape[-2], q_idx.shape[-1]
+    _check(load().lightning_index_topk_static(ctypes.byref(layout.c), _ptr(q_idx), _ptr(k_idx), HI, dI, ratio,
+                                              top_k, _ptr(idx_out), _ptr(score_out), _stream(stream)),
+           "lightning_index_topk_static")
     return idx_out, score_out
 
 

@@ -54,6 +54,26 @@ csa_status_t device_state(DeviceState **out)
     return CSA_OK;
 }
 
+// Address of the device error word on the current device, without creating
+// the helper stream and events of device_state (for the scratch-free entry).
+std::mutex g_err_mu;
+int *g_err_ptr[kMaxDevices];
+
+csa_status_t error_word(int **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return CSA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_err_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return CSA_ERR_CUDA;
+        g_err_ptr[dev] = static_cast<int *>(p);
+    }
+    *out = g_err_ptr[dev];
+    return CSA_OK;
+}
+
 // ---- timing registry ----
 std::atomic<bool> g_timing{false};
 std::mutex g_timing_mu;
@@ -317,6 +337,29 @@ csa_status_t lightning_index_topk(const csa_layout *layout, const csa_bf16 *q_id
     const size_t need = index_workspace_bytes(a);
     if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return CSA_ERR_WORKSPACE;
     return from_cuda(launch_index_topk(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status_t lightning_index_topk_static(const csa_layout *layout, const csa_bf16 *q_idx, const csa_bf16 *k_idx,
+                                         int n_heads_idx, int d_idx, int ratio, int top_k, int32_t *idx_out,
+                                         float *score_out, csa_stream_t stream)
+{
+    CSA_TRY(check_index(layout, q_idx, k_idx, n_heads_idx, d_idx, ratio, top_k, idx_out, score_out));
+    IndexArgs a = index_args(layout, q_idx, k_idx, n_heads_idx, d_idx, ratio, top_k, idx_out, score_out, nullptr, 0,
+                             nullptr);
+    // the whole problem must fit the library-owned scratch (checked before any CUDA call)
+    if (index_workspace_bytes(a) > kIndexStaticScratchBytes) return CSA_ERR_WORKSPACE;
+    int *err = nullptr;
+    CSA_TRY(error_word(&err));
+    void *scratch = nullptr;
+    if (index_static_scratch(&scratch) != cudaSuccess) return CSA_ERR_CUDA;
+    a.ws = scratch;
+    a.ws_bytes = kIndexStaticScratchBytes;
+    a.err = err;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // histograms and counters start at zero whatever an earlier (possibly failed) call left there
+    const size_t zero = index_static_zero_bytes(a);
+    if (zero > 0 && cudaMemsetAsync(scratch, 0, zero, st) != cudaSuccess) return CSA_ERR_CUDA;
+    return from_cuda(launch_index_topk(a, st));
 }
 
 csa_status_t csa_attend_workspace_size(const csa_layout *layout, int n_heads, int d, int ratio, int top_k,

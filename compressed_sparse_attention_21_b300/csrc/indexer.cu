@@ -23,6 +23,8 @@
 //    winners by index.
 // The full score matrix is never stored; only one key row per query in the
 // multi-CTA path.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -631,6 +633,49 @@ cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t st)
     case 128: return launch_index_t<128>(a, st);
     default: return cudaErrorInvalidValue;
     }
+}
+
+// ---------------------------------------------------------------------------
+// Library-owned scratch for callers that cannot allocate device memory.
+//
+// The multi-CTA path needs a workspace (key rows, histograms, counters and
+// candidate lists).  For callers that cannot hand one over, this file-scope
+// device array stands in for it.  Every device that loads this code holds
+// the array until the process exits, and every call shares it: calls that
+// overlap on the GPU race on it.  Its address is looked up once per device,
+// with that device current (host code cannot use the symbol itself: on the
+// host it names a stand-in, not device memory).
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_index_static_scratch[kIndexStaticScratchBytes];
+
+namespace {
+constexpr int kMaxStaticDevices = 64;
+void *g_static_ptr[kMaxStaticDevices];
+std::mutex g_static_mu;
+}  // namespace
+
+cudaError_t index_static_scratch(void **ptr)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxStaticDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_index_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_static_ptr[dev] = p;
+    }
+    *ptr = g_static_ptr[dev];
+    return cudaSuccess;
+}
+
+size_t index_static_zero_bytes(const IndexArgs &a)
+{
+    if (a.total_q <= 0 || use_cta_path(a)) return 0;
+    const int64_t gq = group_size(a);
+    return (size_t)(align_up(gq * kHistBins * 4, 256) + align_up(gq * kMetaWords * 4, 256));
 }
 
 }  // namespace csa

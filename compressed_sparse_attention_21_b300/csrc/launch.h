@@ -6,6 +6,8 @@
 
 #include <utility>
 
+#include "csa.h"
+
 namespace csa {
 
 // ---- per-kernel timing (diagnostics; off unless csa_timing_enable(1)) ----
@@ -74,6 +76,12 @@ struct IndexArgs {
 bool index_supported(int n_heads_idx, int d_idx, int top_k);
 size_t index_workspace_bytes(const IndexArgs &a);
 cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t st);
+// Library-owned scratch of lightning_index_topk_static (see indexer.cu):
+// its device address on the current device (looked up on first use), and the
+// leading bytes of a workspace that must be zero before a call.
+constexpr size_t kIndexStaticScratchBytes = CSA_INDEX_STATIC_SCRATCH_BYTES;
+cudaError_t index_static_scratch(void **ptr);
+size_t index_static_zero_bytes(const IndexArgs &a);
 
 // ---- attention ----
 struct AttendArgs {

@@ -150,6 +150,40 @@ csa_status_t csa_index_workspace_size(const csa_layout *layout, int n_heads_idx,
                                       int ratio, int top_k, size_t *bytes);
 
 /* ---------------------------------------------------------------------------
+ * lightning_index_topk without a caller workspace.  The paper has no
+ * counterpart: this is a library convenience, not a step of the method.
+ *
+ * Some callers cannot allocate device memory.  Examples are a plug-in host
+ * that hands a custom operation only its input and output buffers (no
+ * allocator, no workspace), and a latency-critical loop that may not call
+ * cudaMalloc, which can synchronise the whole device.  For them this entry
+ * point computes exactly what lightning_index_topk computes (same kernels,
+ * same results) and takes its scratch from a library-owned device array of
+ * CSA_INDEX_STATIC_SCRATCH_BYTES (32 MiB).  That array lives in every GPU
+ * that loads the library until the process exits.  This call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ *   - Arguments, layout and outputs are those of lightning_index_topk; the
+ *     caller still provides q_idx, k_idx, idx_out and score_out.
+ *   - A problem whose workspace (csa_index_workspace_size) exceeds
+ *     CSA_INDEX_STATIC_SCRATCH_BYTES is rejected with CSA_ERR_WORKSPACE
+ *     before anything is launched.  Prefill-sized batches (total_q >= 1024
+ *     and at most 40960 entries per sequence) need no scratch at all.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current).  Make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents;
+ *     each call clears the histograms and counters it needs on `stream`
+ *     first.  Calls that overlap on the GPU (on different streams or host
+ *     threads) race on the array and must not be issued.
+ * ------------------------------------------------------------------------- */
+#define CSA_INDEX_STATIC_SCRATCH_BYTES (32u << 20)
+csa_status_t lightning_index_topk_static(const csa_layout *layout, const csa_bf16 *q_idx,
+                                         const csa_bf16 *k_idx, int n_heads_idx, int d_idx,
+                                         int ratio, int top_k, int32_t *idx_out, float *score_out,
+                                         csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Sparse shared-KV multi-query attention (§2.2 step 3).
  *
  * Query row i at position t of sequence b attends, with every one of its
