@@ -24,7 +24,7 @@ struct DeviceState {
     bool ready = false;
     int *err = nullptr;
     cudaStream_t aux = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, cdone = nullptr;
     int num_sms = 0;
 };
 
@@ -48,6 +48,7 @@ csa_status_t device_state(DeviceState **out)
         if (cudaStreamCreateWithFlags(&s.aux, cudaStreamNonBlocking) != cudaSuccess) return CSA_ERR_CUDA;
         if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
         if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
+        if (cudaEventCreateWithFlags(&s.cdone, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
         s.ready = true;
     }
     *out = &s;
@@ -136,6 +137,7 @@ IndexArgs index_args(const csa_layout *L, const csa_bf16 *q_idx, const csa_bf16 
     a.max_kv_len = L->max_kv_len;
     a.max_q_len = L->max_q_len;
     a.total_q = L->total_q;
+    a.pdl = false;
     a.cu_kv = L->cu_kv;
     a.cu_q = L->cu_q;
     a.cu_csa = L->cu_csa;
@@ -179,6 +181,7 @@ AttendArgs attend_args(const csa_layout *L, const int64_t *cu_ent, const csa_bf1
     a.ws = ws;
     a.ws_bytes = ws_bytes;
     a.err = err;
+    a.pdl = false;
     a.num_sms = num_sms;
     a.sm_share = sm_share;
     return a;
@@ -263,7 +266,7 @@ size_t hybrid_ws_parts(const csa_hybrid_params *p, size_t *idx_ws, size_t *sp_ws
                                 num_sms);
     sa.idx = reinterpret_cast<const int32_t *>(1);   // sparse plan
     AttendArgs ha = attend_args(L, L->cu_hca, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca,
-                                0, p->scale, nullptr, nullptr, nullptr, 0, nullptr, num_sms, num_sms / 2);
+                                0, p->scale, nullptr, nullptr, nullptr, 0, nullptr, num_sms, num_sms);
     *idx_ws = align_ws(index_workspace_bytes(ia));
     *sp_ws = align_ws(attend_workspace_bytes(sa));
     *hc_ws = align_ws(attend_workspace_bytes(ha));
@@ -448,7 +451,15 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
     if (L->total_q == 0) return CSA_OK;
     char *ws = static_cast<char *>(p->ws);
 
-    // a1: compression of the blocks closed by this call's query positions
+    // Streams.  The caller's stream `st` runs the CSA branch (indexer, top-k,
+    // sparse attention); the helper stream runs the compression and then the
+    // HCA branch.  The indexer reads no compressed entry, so it overlaps the
+    // compression; the sparse attention waits for both.
+    if (cudaEventRecord(ds->fork, st) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaStreamWaitEvent(ds->aux, ds->fork, 0) != cudaSuccess) return CSA_ERR_CUDA;
+
+    // a1 on the helper stream: compression of the blocks closed by this call's query positions
+    csa_status_t s_h = CSA_OK;
     if (compress) {
         CompressArgs a;
         std::memset(&a, 0, sizeof a);
@@ -468,29 +479,34 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
             a.ratio_big = p->ratio_hca;
             a.cu_big = L->cu_hca;
             a.out_big = p->hca_cache;
-            CSA_TRY(from_cuda(launch_compress(a, st)));
+            s_h = from_cuda(launch_compress(a, ds->aux));
         } else {
-            CSA_TRY(compress_impl(L, true, p->kv, p->gate, p->d, p->ratio_csa, p->csa_cache, st));
-            CSA_TRY(compress_impl(L, false, p->kv, p->gate, p->d, p->ratio_hca, p->hca_cache, st));
+            s_h = compress_impl(L, true, p->kv, p->gate, p->d, p->ratio_csa, p->csa_cache, ds->aux);
+            if (s_h == CSA_OK)
+                s_h = compress_impl(L, false, p->kv, p->gate, p->d, p->ratio_hca, p->hca_cache, ds->aux);
         }
     }
+    const bool c1 = cudaEventRecord(ds->cdone, ds->aux) == cudaSuccess;
 
-    // fork: the HCA branch runs on the helper stream, concurrently with the CSA branch
-    if (cudaEventRecord(ds->fork, st) != cudaSuccess) return CSA_ERR_CUDA;
-    if (cudaStreamWaitEvent(ds->aux, ds->fork, 0) != cudaSuccess) return CSA_ERR_CUDA;
+    // a5 on the helper stream (may overlap the compression's tail; waits for it on the device)
+    if (s_h == CSA_OK) {
+        AttendArgs ha = attend_args(L, L->cu_hca, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d,
+                                    p->ratio_hca, 0, p->scale, p->o_hca, p->lse_hca,
+                                    w_hc ? ws + w_idx + w_sp : nullptr, w_hc, ds->err, ds->num_sms, ds->num_sms);
+        ha.pdl = compress;
+        s_h = from_cuda(launch_attend(ha, ds->aux));
+    }
 
-    AttendArgs ha = attend_args(L, L->cu_hca, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca, 0,
-                                p->scale, p->o_hca, p->lse_hca, w_hc ? ws + w_idx + w_sp : nullptr, w_hc, ds->err,
-                                ds->num_sms, ds->num_sms / 2);
-    csa_status_t s_h = from_cuda(launch_attend(ha, ds->aux));
-
+    // a2 + a3 on the caller's stream, then a4 once the compression is done
     IndexArgs ia = index_args(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k, p->idx_out,
                               p->score_out, w_idx ? ws : nullptr, w_idx, ds->err);
     csa_status_t s_c = from_cuda(launch_index_topk(ia, st));
+    const bool c2 = cudaStreamWaitEvent(st, ds->cdone, 0) == cudaSuccess;
     if (s_c == CSA_OK) {
         AttendArgs sa = attend_args(L, L->cu_csa, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d,
                                     p->ratio_csa, p->top_k, p->scale, p->o_csa, p->lse_csa,
                                     w_sp ? ws + w_idx : nullptr, w_sp, ds->err, ds->num_sms, ds->num_sms);
+        sa.pdl = true;
         s_c = from_cuda(launch_attend(sa, st));
     }
     // join (always, so the helper stream never dangles inside a capture)
@@ -498,7 +514,7 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
     const bool j2 = cudaStreamWaitEvent(st, ds->join, 0) == cudaSuccess;
     if (s_c != CSA_OK) return s_c;
     if (s_h != CSA_OK) return s_h;
-    return (j1 && j2) ? CSA_OK : CSA_ERR_CUDA;
+    return (c1 && c2 && j1 && j2) ? CSA_OK : CSA_ERR_CUDA;
 }
 
 csa_status_t csa_workspace_init(void *ws, size_t ws_bytes, csa_stream_t stream)

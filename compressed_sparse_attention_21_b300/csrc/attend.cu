@@ -30,6 +30,7 @@ constexpr int kSStride = 72;            // fp32 row stride of the score tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxSplits = 64;
+constexpr int kIdxCap = 1792;           // selected indices of one split held in shared memory
 
 __host__ __device__ constexpr int64_t align_up64(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
@@ -48,14 +49,16 @@ struct Cfg {
     static constexpr size_t k_bytes = size_t(kTile) * RB;
     static constexpr size_t s_bytes = size_t(HT) * kSStride * 4;
     static constexpr size_t p_bytes = size_t(HT) * kTile * 2;
+    static constexpr int NST = (HT == 16 && D == 512) ? 3 : 2;   // key tiles in the ring
     static constexpr size_t off_q = 0;
     static constexpr size_t off_k0 = off_q + q_bytes;
-    static constexpr size_t off_k1 = off_k0 + k_bytes;
-    static constexpr size_t off_s = off_k1 + k_bytes;
+    static constexpr size_t off_s = off_k0 + NST * k_bytes;
     static constexpr size_t off_p = off_s + s_bytes;
     static constexpr size_t off_stats = off_p + p_bytes;             // m, l, alpha: 3*HT floats
-    static constexpr size_t off_valid = off_stats + 3 * HT * 4;      // 2 x 64 flags
-    static constexpr size_t smem = off_valid + 2 * kTile * 4 + 16;
+    static constexpr size_t off_valid = off_stats + 3 * HT * 4;      // NST x 64 flags
+    static constexpr size_t off_idx = off_valid + NST * kTile * 4;   // this split's selection
+    static constexpr size_t smem = off_idx + kIdxCap * 4 + 16;
+    static_assert(smem <= 232448, "shared memory per CTA");
     static_assert(HT == 16 || HT == 64, "head tile");
     static_assert(NT8 % 2 == 0, "PV n-tiles come in pairs");
     static_assert(CPR >= 8, "swizzle needs 8 chunks per row");
@@ -77,7 +80,7 @@ struct KeySet {
     const uint16_t *safe;      // any valid global address (source of zero-size copies)
     const uint16_t *entries;   // sequence's first entry row
     const uint16_t *tail;      // first raw tail token row
-    const int32_t *idx;        // sparse: this query's idx row; dense: nullptr
+    const int32_t *idx;        // sparse: this query's idx row (indexed by slot); dense: nullptr
     int64_t n_vis;             // visible entries
     int n_main;                // main key slots (entries)
     int n_keys;                // main + tail
@@ -88,7 +91,7 @@ __device__ __forceinline__ const uint16_t *key_row(const KeySet &ks, int slot, i
 {
     if (slot < ks.n_main) {
         if (GATHER) {
-            const int e = __ldg(ks.idx + slot);
+            const int e = ks.idx[slot];   // shared memory (prefetched) or global
             if (e < 0) return nullptr;
             if ((int64_t)e >= ks.n_vis) {
                 set_error(err, CSA_ERR_DEVICE);
@@ -137,19 +140,19 @@ attend_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__res
     const int split = blockIdx.y / HG;
     const int64_t qi = blockIdx.x;
 
-    const QueryPos p = query_pos(cu_kv, cu_q, batch, qi);
+    const QueryPos p = query_pos(cu_kv, cu_q, cu_ent, batch, qi);
     const int64_t n_vis = (p.t + 1) / ratio;
     const int r_tail = (int)((p.t + 1) % ratio);
     const bool bad = p.t < 0 || p.t >= p.L || p.L > max_kv_len ||
-                     __ldg(cu_ent + p.b + 1) - __ldg(cu_ent + p.b) != p.L / ratio;
+                     p.ne != p.L / ratio;
     if (bad) {
         if (tid == 0) set_error(err, CSA_ERR_DEVICE);
         return;
     }
     KeySet ks;
     ks.safe = kv;
-    ks.entries = entries + __ldg(cu_ent + p.b) * D;
-    ks.tail = kv + (__ldg(cu_kv + p.b) + p.t - r_tail + 1) * D;
+    ks.entries = entries + p.e0 * D;
+    ks.tail = kv + (p.kv0 + p.t - r_tail + 1) * D;
     ks.idx = GATHER ? idx + qi * top_k : nullptr;
     ks.n_vis = n_vis;
     ks.n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
@@ -178,8 +181,28 @@ attend_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__res
             cp_async_16(sQ + swz<C::RB>(row, chunk), src, h < H ? 16 : 0);
         }
     }
-    load_tile<D, HT, GATHER>(smem, sb + C::off_k0, s_valid, ks, key0, err);
-    cp_async_commit();
+    // everything below reads what earlier kernels produced (selection, entries)
+    // or writes what they may still read: wait for them
+    griddep_wait();
+    if (GATHER) {
+        // this split's selected indices, read once: the gathers then need no
+        // global round trip of their own
+        const int i1 = min(key1, ks.n_main);
+        if (i1 - key0 <= kIdxCap) {
+            int32_t *s_idx = reinterpret_cast<int32_t *>(smem + C::off_idx);
+            for (int i = key0 + tid; i < i1; i += kThreads) s_idx[i - key0] = __ldg(ks.idx + i);
+            __syncthreads();
+            ks.idx = s_idx - key0;
+        }
+    }
+    // the first NST-1 key tiles (the Q tile travels with the first group)
+#pragma unroll
+    for (int st = 0; st < C::NST - 1; st++) {
+        if (st < ntiles)
+            load_tile<D, HT, GATHER>(smem, sb + C::off_k0 + st * C::k_bytes, s_valid + st * kTile, ks,
+                                     key0 + st * kTile, err);
+        cp_async_commit();
+    }
     for (int i = tid; i < HT; i += kThreads) {
         s_m[i] = -INFINITY;
         s_l[i] = 0.f;
@@ -194,13 +217,14 @@ attend_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__res
     for (int i = 0; i < C::NT8; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
     for (int it = 0; it < ntiles; it++) {
-        const int buf = it & 1;
-        const uint32_t sK = sb + (buf ? C::off_k1 : C::off_k0);
-        if (it + 1 < ntiles)
-            load_tile<D, HT, GATHER>(smem, sb + (buf ? C::off_k0 : C::off_k1), s_valid + (buf ^ 1) * kTile, ks,
-                                     key0 + (it + 1) * kTile, err);
+        const int buf = it % C::NST;
+        const uint32_t sK = sb + C::off_k0 + buf * C::k_bytes;
+        const int nxt = it + C::NST - 1;   // refills the stage computed in the previous iteration
+        if (nxt < ntiles)
+            load_tile<D, HT, GATHER>(smem, sb + C::off_k0 + (nxt % C::NST) * C::k_bytes,
+                                     s_valid + (nxt % C::NST) * kTile, ks, key0 + nxt * kTile, err);
         cp_async_commit();
-        cp_async_wait<1>();
+        cp_async_wait<C::NST - 1>();
         __syncthreads();
 
         // ---- S = Q K^T for rows of tile mt, keys [ds*QKN*8, +QKN*8) ----
@@ -402,25 +426,48 @@ attend_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__res
         s_lse[row] = (M + log2f(Lsum)) * kLn2;
     }
     __syncthreads();
+    // weighted sum of the partial outputs: U float4 columns per thread at a
+    // time, so that U loads per split are in flight instead of one
     const float *pbase = part_o + unit * nsplit_max * (int64_t)HT * D;
-    for (int e = tid; e < HT * D / 4; e += kThreads) {
-        const int row = e / (D / 4), col = (e % (D / 4)) * 4;
-        const int h = hg * HT + row;
-        if (h >= H) continue;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < nsplit; s++) {
-            const float w = s_wt[row * kMaxSplits + s];
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(pbase + ((int64_t)s * HT + row) * D + col));
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+    constexpr int NE = HT * D / 4;
+    constexpr int EPT = NE / kThreads;
+    constexpr int U = EPT < 4 ? EPT : 4;
+    static_assert(NE % kThreads == 0 && EPT % U == 0, "merge tiling");
+    for (int e0 = 0; e0 < EPT; e0 += U) {
+        int rows[U], cols[U];
+        float4 acc[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int e = tid + (e0 + u) * kThreads;
+            rows[u] = e / (D / 4);
+            cols[u] = (e % (D / 4)) * 4;
+            acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const float inv = s_inv[row];
-        uint2 pk;
-        pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2 *>(out + (qi * H + h) * (int64_t)D + col) = pk;
+#pragma unroll 2
+        for (int s = 0; s < nsplit; s++) {
+            float4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; u++)
+                v[u] = __ldcg(reinterpret_cast<const float4 *>(pbase + ((int64_t)s * HT + rows[u]) * D + cols[u]));
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const float w = s_wt[rows[u] * kMaxSplits + s];
+                acc[u].x = fmaf(w, v[u].x, acc[u].x);
+                acc[u].y = fmaf(w, v[u].y, acc[u].y);
+                acc[u].z = fmaf(w, v[u].z, acc[u].z);
+                acc[u].w = fmaf(w, v[u].w, acc[u].w);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int h = hg * HT + rows[u];
+            if (h >= H) continue;
+            const float inv = s_inv[rows[u]];
+            uint2 pk;
+            pk.x = pack_bf16x2(acc[u].x * inv, acc[u].y * inv);
+            pk.y = pack_bf16x2(acc[u].z * inv, acc[u].w * inv);
+            *reinterpret_cast<uint2 *>(out + (qi * H + h) * (int64_t)D + cols[u]) = pk;
+        }
     }
     if (lse)
         for (int row = tid; row < HT; row += kThreads)
@@ -438,20 +485,33 @@ struct Plan {
     int nsplit_max;
 };
 
+constexpr int kMinSplitKeys = 128;   // fewest keys worth a split of their own
+
 Plan make_plan(const AttendArgs &a)
 {
     Plan pl;
-    pl.HT = a.n_heads <= 16 ? 16 : 64;
+    const int share = a.sm_share > 0 ? a.sm_share : (a.num_sms > 0 ? a.num_sms : 148);
+    // Head tile.  When there are at least as many 64-head units as SMs (prefill),
+    // 64 heads of a query share every key tile a CTA loads.  Otherwise (decode)
+    // 16-head tiles spread a query over more SMs without splitting its keys:
+    // every key split costs an fp32 partial output of HT x d, which at d = 512
+    // and 64 heads is as many bytes as 128 keys.
+    const int64_t units64 = a.total_q * ((a.n_heads + 63) / 64);
+    pl.HT = (a.n_heads <= 16 || units64 < share) ? 16 : 64;
     pl.HG = (a.n_heads + pl.HT - 1) / pl.HT;
     const int64_t max_vis = a.max_kv_len / a.ratio;
     int64_t mk = (a.idx ? (max_vis < a.top_k ? max_vis : a.top_k) : max_vis) + (a.ratio - 1);
     if (mk > a.max_kv_len) mk = a.max_kv_len;   // tail never exceeds the sequence
     if (mk < 1) mk = 1;
     pl.max_keys = (int)mk;
+    // Key splits: as many as keep every unit's CTAs within one wave of `share`
+    // CTAs, and no fewer than kMinSplitKeys keys per split.
     const int64_t units = a.total_q * pl.HG;
-    const int share = a.sm_share > 0 ? a.sm_share : (a.num_sms > 0 ? a.num_sms : 148);
-    int64_t want = units >= share ? 1 : (share + units - 1) / units;
+    int64_t want = units >= share ? 1 : share / units;
+    const int64_t by_keys = (mk + kMinSplitKeys - 1) / kMinSplitKeys;
+    if (want > by_keys) want = by_keys;
     if (want > kMaxSplits) want = kMaxSplits;
+    if (want < 1) want = 1;
     int64_t kps = align_up64((mk + want - 1) / want, kTile);
     if (kps < kTile) kps = kTile;
     int64_t ns = (mk + kps - 1) / kps;
@@ -497,7 +557,7 @@ cudaError_t launch_t(const AttendArgs &a, const Plan &pl, const WsA &w, cudaStre
     dim3 grid((unsigned)a.total_q, (unsigned)(pl.HG * pl.nsplit_max));
     const float scale_log2 = a.scale * kLog2e;
     return launch_kernel(GATHER ? "sparse_attend" : "dense_attend", attend_kernel<D, HT, GATHER>, grid,
-                         dim3(kThreads), C::smem, st, a.batch, a.cu_kv, a.cu_q, a.cu_ent, a.q, a.entries, a.kv,
+                         dim3(kThreads), C::smem, st, a.pdl, a.batch, a.cu_kv, a.cu_q, a.cu_ent, a.q, a.entries, a.kv,
                          a.idx, a.n_heads, a.ratio, a.top_k, scale_log2, pl.kps, pl.nsplit_max, a.max_kv_len,
                          a.out, a.lse, w.part_o, w.part_ml, w.tickets, a.err);
 }
@@ -519,13 +579,14 @@ bool attend_supported(int n_heads, int d)
 
 size_t attend_workspace_bytes(const AttendArgs &a)
 {
-    if (a.total_q <= 0) return 0;
+    if (a.total_q <= 0 || attend_tc_applicable(a)) return 0;
     return ws_bytes_for(a, make_plan(a), nullptr);
 }
 
 cudaError_t launch_attend(const AttendArgs &a, cudaStream_t st)
 {
     if (a.total_q <= 0) return cudaSuccess;
+    if (attend_tc_applicable(a)) return launch_attend_tc(a, st);
     const Plan pl = make_plan(a);
     WsA w;
     ws_bytes_for(a, pl, &w);

@@ -20,32 +20,51 @@ __device__ __forceinline__ void set_error(int *err, int code)
 // --------------------------------------------------------------------------
 // Packed layout lookups.
 // --------------------------------------------------------------------------
-// Sequence that owns packed row `i` of a cu array (the last b with cu[b] <= i).
-__device__ __forceinline__ int find_seq(const int64_t *cu, int batch, int64_t i)
-{
-    int lo = 0, hi = batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(cu + mid) <= i) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
-
 struct QueryPos {
     int b;          // sequence
     int64_t t;      // 0-based position of the query within its sequence
     int64_t L;      // sequence length
+    int64_t kv0;    // first token row of the sequence
+    int64_t e0;     // first entry row of the sequence (entry array passed in)
+    int64_t ne;     // entries of the sequence
 };
 
-// Queries of sequence b are its last n_q positions.
-__device__ __forceinline__ QueryPos query_pos(const int64_t *cu_kv, const int64_t *cu_q,
+// Queries of sequence b are its last n_q positions.  Warp-cooperative: every
+// lane of the calling warp must call it with the same arguments.  The 32
+// lanes probe cu_q together (one round trip to memory per factor of 32 in
+// the batch), then the sequence's offsets arrive in one more round trip;
+// cu_e (an entry prefix array) may be null.
+__device__ __forceinline__ QueryPos query_pos(const int64_t *cu_kv, const int64_t *cu_q, const int64_t *cu_e,
                                               int batch, int64_t qi)
 {
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = batch - 1;          // invariant: cu_q[lo] <= qi
+    while (hi > lo) {
+        const int stride = (hi - lo + 32) / 32;
+        const int at = min(lo + lane * stride, hi);
+        const unsigned m = __ballot_sync(0xffffffffu, __ldg(cu_q + at) <= qi);
+        const int L = m ? 31 - __clz(m) : 0;   // last probe at or below qi (lane 0, unless cu_q is malformed)
+        const int nlo = min(lo + L * stride, hi);
+        const int nhi = (L < 31 && lo + (L + 1) * stride <= hi) ? lo + (L + 1) * stride - 1 : hi;
+        lo = nlo;
+        hi = nhi;
+    }
+    const int b = lo;
+    int64_t v = 0;
+    if (lane < 6) {
+        const int64_t *arr = lane < 2 ? cu_kv : (lane < 4 ? cu_q : cu_e);
+        if (arr) v = __ldg(arr + b + (lane & 1));
+    }
+    const int64_t kv0 = __shfl_sync(0xffffffffu, v, 0), kv1 = __shfl_sync(0xffffffffu, v, 1);
+    const int64_t q0 = __shfl_sync(0xffffffffu, v, 2), q1 = __shfl_sync(0xffffffffu, v, 3);
+    const int64_t e0 = __shfl_sync(0xffffffffu, v, 4), e1 = __shfl_sync(0xffffffffu, v, 5);
     QueryPos p;
-    p.b = find_seq(cu_q, batch, qi);
-    p.L = __ldg(cu_kv + p.b + 1) - __ldg(cu_kv + p.b);
-    const int64_t nq = __ldg(cu_q + p.b + 1) - __ldg(cu_q + p.b);
-    p.t = p.L - nq + (qi - __ldg(cu_q + p.b));
+    p.b = b;
+    p.L = kv1 - kv0;
+    p.t = p.L - (q1 - q0) + (qi - q0);
+    p.kv0 = kv0;
+    p.e0 = e0;
+    p.ne = e1 - e0;
     return p;
 }
 
@@ -126,6 +145,71 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+
+// --------------------------------------------------------------------------
+// mbarrier + bulk (TMA) copies.  Waits are bounded: a wait that runs out
+// returns false and the caller reports CSA_ERR_TIMEOUT instead of hanging.
+// --------------------------------------------------------------------------
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;   // 0.2 s of wall time
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+// Wait for the phase with `parity` to complete; gives up (returns false)
+// after kWaitLimitNs of wall time.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+// Contiguous global -> shared copy by the bulk-copy (TMA) engine; completes
+// `bytes` of transaction count on `bar`.  Both addresses 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Programmatic dependent launch.  griddep_wait() blocks until every grid this
+// one depends on has completed and its memory is visible (a no-op for a
+// launch without a programmatic dependency); griddep_launch() lets the grids
+// that depend on this one begin launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
 __device__ __forceinline__ float warp_max(float v)
 {

@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kCompressThreads = 256;
 constexpr int kSpan = 128;
+constexpr int kSliceCols = 128;   // columns per CTA (a d = 512 row is split over 4 CTAs)
 
 template <int D, int MS, int MB>
 __global__ void __launch_bounds__(kCompressThreads)
@@ -29,19 +30,23 @@ compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ c
                 const uint16_t *__restrict__ kv, const float *__restrict__ gate,
                 uint16_t *__restrict__ out_s, uint16_t *__restrict__ out_b, int *err)
 {
-    constexpr int G = D / 8;                       // 16-byte column groups per row
+    constexpr int CS = D < kSliceCols ? D : kSliceCols;   // columns of this CTA's slice
+    constexpr int G = CS / 8;                      // 16-byte column groups per slice row
     constexpr int R = kCompressThreads / G;        // row lanes
     constexpr int U = MS > 0 ? MS : 4;             // tokens per unit
     constexpr int NU = kSpan / U;                  // units per span
+    constexpr int UPT = (NU + R - 1) / R;          // units per thread
     constexpr int NB = MB > 0 ? kSpan / MB : 0;    // large blocks per span
-    static_assert(kCompressThreads % G == 0, "D/8 must divide the CTA");
+    static_assert(kCompressThreads % G == 0, "slice groups must divide the CTA");
     static_assert(MS == 0 || (kSpan % MS == 0 && MS <= 32), "small ratio");
     static_assert(MB == 0 || MB == 64 || MB == 128, "large ratio");
+    static_assert(UPT * U <= 32, "row registers per thread");
 
     __shared__ float s_wred[kCompressThreads / 32];
     __shared__ float s_zmax[2], s_zsum[2];
-    __shared__ float s_red[NB > 0 ? R * NB * D : 1];
+    __shared__ float s_red[NB > 0 ? R * NB * CS : 1];
 
+    griddep_launch();
     const int b = blockIdx.x;
     const int64_t kv0 = cu_kv[b];
     const int64_t L = cu_kv[b + 1] - kv0;
@@ -49,7 +54,7 @@ compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ c
     const bool bad = nq < 0 || nq > L || (MS > 0 && cu_s[b + 1] - cu_s[b] != L / MS) ||
                      (MB > 0 && cu_b[b + 1] - cu_b[b] != L / MB);
     if (bad) {
-        if (threadIdx.x == 0 && blockIdx.y == 0) set_error(err, CSA_ERR_DEVICE);
+        if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_error(err, CSA_ERR_DEVICE);
         return;
     }
     if (nq == 0) return;
@@ -59,6 +64,7 @@ compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ c
 
     const int tid = threadIdx.x;
     const int g = tid % G, r = tid / G;
+    const int col0 = blockIdx.z * CS;               // first column of the slice
 
     // Which large blocks of this span are complete and end at a query position.
     bool do_big[NB > 0 ? NB : 1];
@@ -70,13 +76,36 @@ compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ c
         any_big |= do_big[bb];
     }
 
+    // This thread's units: u = r + i*R.  Load every row it needs first (one
+    // round trip to memory), then reduce.
+    uint4 row[UPT][U];
+    float z[UPT][U];
+    bool small_needed[UPT], big_read[UPT];
+#pragma unroll
+    for (int i = 0; i < UPT; i++) {
+        const int u = r + i * R;
+        const int64_t tu = t0 + (int64_t)u * U;     // first token of the unit
+        const bool in_span = u < NU;
+        const bool complete = in_span && tu + U <= L;
+        small_needed[i] = MS > 0 && complete && (tu + U - 1 >= lo);
+        big_read[i] = false;
+        if constexpr (MB > 0) big_read[i] = in_span && do_big[(u * U) / MB];
+        const bool need = small_needed[i] || big_read[i];
+#pragma unroll
+        for (int k = 0; k < U; k++) {
+            row[i][k] = need ? __ldg(reinterpret_cast<const uint4 *>(kv + (kv0 + tu + k) * D + col0) + g)
+                             : make_uint4(0, 0, 0, 0);
+            z[i][k] = need ? __ldg(gate + kv0 + tu + k) : 0.f;
+        }
+    }
+
     if constexpr (NB > 0) {
         // softmax statistics of the large blocks: warp w < 4 holds tokens 32w..32w+31
         const int w = tid / 32, lane = tid % 32;
         const int bb_w = (w * 32) / MB;
-        float z = -INFINITY;
-        if (any_big && w < 4 && do_big[bb_w]) z = gate[kv0 + t0 + w * 32 + lane];
-        float m = warp_max(z);
+        float zz = -INFINITY;
+        if (any_big && w < 4 && do_big[bb_w]) zz = gate[kv0 + t0 + w * 32 + lane];
+        float m = warp_max(zz);
         if (lane == 0) s_wred[w] = m;
         __syncthreads();
         if (tid < NB) {
@@ -86,7 +115,7 @@ compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ c
         }
         __syncthreads();
         float e = 0.f;
-        if (any_big && w < 4 && do_big[bb_w]) e = expf(z - s_zmax[bb_w]);
+        if (any_big && w < 4 && do_big[bb_w]) e = expf(zz - s_zmax[bb_w]);
         e = warp_sum(e);
         if (lane == 0) s_wred[w] = e;
         __syncthreads();
@@ -104,36 +133,25 @@ compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ c
 #pragma unroll
         for (int x = 0; x < 8; x++) acc_b[bb][x] = 0.f;
 
-    for (int u = r; u < NU; u += R) {
-        const int64_t tu = t0 + (int64_t)u * U;     // first token of the unit
-        const bool complete = tu + U <= L;
-        const bool small_needed = MS > 0 && complete && (tu + U - 1 >= lo);
-        const int bb = MB > 0 ? (u * U) / MB : 0;
-        const bool big_read = MB > 0 && do_big[bb];
-        if (!small_needed && !big_read) continue;
-
-        uint4 row[U];
-        float z[U];
 #pragma unroll
-        for (int i = 0; i < U; i++) {
-            row[i] = __ldg(reinterpret_cast<const uint4 *>(kv + (kv0 + tu + i) * D) + g);
-            z[i] = __ldg(gate + kv0 + tu + i);
-        }
-        if (small_needed) {
-            float zm = z[0];
+    for (int i = 0; i < UPT; i++) {
+        const int u = r + i * R;
+        const int64_t tu = t0 + (int64_t)u * U;
+        if (small_needed[i]) {
+            float zm = z[i][0];
 #pragma unroll
-            for (int i = 1; i < U; i++) zm = fmaxf(zm, z[i]);
+            for (int k = 1; k < U; k++) zm = fmaxf(zm, z[i][k]);
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             float den = 0.f;
 #pragma unroll
-            for (int i = 0; i < U; i++) {
-                const float w = expf(z[i] - zm);
-                den += w;
-                const uint32_t wd[4] = {row[i].x, row[i].y, row[i].z, row[i].w};
+            for (int k = 0; k < U; k++) {
+                const float wgt = expf(z[i][k] - zm);
+                den += wgt;
+                const uint32_t wd[4] = {row[i][k].x, row[i][k].y, row[i][k].z, row[i][k].w};
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    acc[2 * k] = fmaf(w, bf16_lo(wd[k]), acc[2 * k]);
-                    acc[2 * k + 1] = fmaf(w, bf16_hi(wd[k]), acc[2 * k + 1]);
+                for (int c = 0; c < 4; c++) {
+                    acc[2 * c] = fmaf(wgt, bf16_lo(wd[c]), acc[2 * c]);
+                    acc[2 * c + 1] = fmaf(wgt, bf16_hi(wd[c]), acc[2 * c + 1]);
                 }
             }
             const float inv = 1.f / den;
@@ -143,21 +161,22 @@ compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ c
             o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
             o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
             const int64_t e = cu_s[b] + tu / (MS > 0 ? MS : 1);
-            reinterpret_cast<uint4 *>(out_s + e * D)[g] = o;
+            reinterpret_cast<uint4 *>(out_s + e * D + col0)[g] = o;
         }
         if constexpr (NB > 0) {
-            if (big_read) {
+            if (big_read[i]) {
+                const int bb = (u * U) / MB;
 #pragma unroll
-                for (int i = 0; i < U; i++) {
-                    const float w = expf(z[i] - s_zmax[bb]);
-                    const uint32_t wd[4] = {row[i].x, row[i].y, row[i].z, row[i].w};
+                for (int k = 0; k < U; k++) {
+                    const float wgt = expf(z[i][k] - s_zmax[bb]);
+                    const uint32_t wd[4] = {row[i][k].x, row[i][k].y, row[i][k].z, row[i][k].w};
 #pragma unroll
-                    for (int k = 0; k < 4; k++) {
+                    for (int c = 0; c < 4; c++) {
 #pragma unroll
                         for (int q = 0; q < NB; q++) {
                             if (q == bb) {
-                                acc_b[q][2 * k] = fmaf(w, bf16_lo(wd[k]), acc_b[q][2 * k]);
-                                acc_b[q][2 * k + 1] = fmaf(w, bf16_hi(wd[k]), acc_b[q][2 * k + 1]);
+                                acc_b[q][2 * c] = fmaf(wgt, bf16_lo(wd[c]), acc_b[q][2 * c]);
+                                acc_b[q][2 * c + 1] = fmaf(wgt, bf16_hi(wd[c]), acc_b[q][2 * c + 1]);
                             }
                         }
                     }
@@ -171,20 +190,20 @@ compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ c
 #pragma unroll
         for (int bb = 0; bb < NB; bb++)
 #pragma unroll
-            for (int x = 0; x < 8; x++) s_red[(r * NB + bb) * D + g * 8 + x] = acc_b[bb][x];
+            for (int x = 0; x < 8; x++) s_red[(r * NB + bb) * CS + g * 8 + x] = acc_b[bb][x];
         __syncthreads();
-        for (int p = tid; p < NB * (D / 2); p += kCompressThreads) {
-            const int bb = p / (D / 2), x = 2 * (p % (D / 2));
+        for (int p = tid; p < NB * (CS / 2); p += kCompressThreads) {
+            const int bb = p / (CS / 2), x = 2 * (p % (CS / 2));
             if (!do_big[bb]) continue;
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
             for (int rr = 0; rr < R; rr++) {
-                s0 += s_red[(rr * NB + bb) * D + x];
-                s1 += s_red[(rr * NB + bb) * D + x + 1];
+                s0 += s_red[(rr * NB + bb) * CS + x];
+                s1 += s_red[(rr * NB + bb) * CS + x + 1];
             }
             const float inv = 1.f / s_zsum[bb];
             const int64_t e = cu_b[b] + (t0 + bb * MB) / MB;
-            reinterpret_cast<uint32_t *>(out_b + e * D)[x / 2] = pack_bf16x2(s0 * inv, s1 * inv);
+            reinterpret_cast<uint32_t *>(out_b + e * D + col0)[x / 2] = pack_bf16x2(s0 * inv, s1 * inv);
         }
     }
 }
@@ -197,9 +216,10 @@ cudaError_t launch_compress_t(const CompressArgs &a, cudaStream_t st)
     const int64_t spans = spans_kv < spans_q ? spans_kv : spans_q;
     if (spans <= 0 || a.batch <= 0) return cudaSuccess;
     if (spans > 65535) return cudaErrorInvalidConfiguration;   // > 8M tokens per sequence
-    dim3 grid((unsigned)a.batch, (unsigned)spans);
+    constexpr int slices = D / (D < kSliceCols ? D : kSliceCols);
+    dim3 grid((unsigned)a.batch, (unsigned)spans, (unsigned)slices);
     return launch_kernel("compress", compress_kernel<D, MS, MB>, grid, dim3(kCompressThreads), 0,
-                         st, a.cu_kv, a.cu_q, a.cu_small, a.cu_big, a.batch, a.kv, a.gate,
+                         st, false, a.cu_kv, a.cu_q, a.cu_small, a.cu_big, a.batch, a.kv, a.gate,
                          a.out_small, a.out_big, a.err);
 }
 

@@ -39,6 +39,7 @@ constexpr int kScanThreads = 256;
 constexpr int kScanChunk = 1024;      // entries per scan/filter CTA
 constexpr int kHistBits = 12;
 constexpr int kHistBins = 1 << kHistBits;
+constexpr int kFilterSmemCand = 3072;  // boundary candidates resolved in shared memory
 constexpr int kMetaWords = 8;         // per-query: ticket1, ticket2, n_sel, n_cand, bin, above
 constexpr int64_t kGroupBudget = int64_t(1) << 30;   // max workspace of the multi-CTA path
 
@@ -205,9 +206,9 @@ __device__ __forceinline__ void write_row_padding(int32_t *idx_row, float *score
     }
 }
 
-__device__ __forceinline__ bool entry_count_ok(const int64_t *cu_csa, const QueryPos &p, int ratio)
+__device__ __forceinline__ bool entry_count_ok(const int64_t *, const QueryPos &p, int ratio)
 {
-    return __ldg(cu_csa + p.b + 1) - __ldg(cu_csa + p.b) == p.L / ratio && p.t >= 0 && p.t < p.L;
+    return p.ne == p.L / ratio && p.t >= 0 && p.t < p.L;
 }
 
 // ---------------------------------------------------------------------------
@@ -228,7 +229,7 @@ index_topk_cta_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_
 
     const int tid = threadIdx.x;
     const int64_t qi = q_begin + blockIdx.x;
-    const QueryPos p = query_pos(cu_kv, cu_q, batch, qi);
+    const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);
     int32_t *idx_row = idx_out + qi * top_k;
     float *sc_row = score_out ? score_out + qi * top_k : nullptr;
     const int64_t n64 = (p.t + 1) / ratio;
@@ -238,7 +239,7 @@ index_topk_cta_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_
         return;
     }
     const int n = (int)n64;
-    const uint16_t *kbase = kI + __ldg(cu_csa + p.b) * DI;
+    const uint16_t *kbase = kI + p.e0 * DI;
 
     load_qsum<DI>(qI, qi, HI, s_q);
     __syncthreads();
@@ -313,10 +314,11 @@ index_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *_
     __shared__ uint32_t s_sum[2 * (kScanThreads / 32) + 1];
     __shared__ int s_last;
 
+    griddep_launch();   // the filter may launch now; it waits for this grid to finish
     const int tid = threadIdx.x;
     const int64_t qg = blockIdx.y;
     const int64_t qi = q_begin + qg;
-    const QueryPos p = query_pos(cu_kv, cu_q, batch, qi);
+    const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);
     const int64_t n = (p.t + 1) / ratio;
     const int64_t nchunks = chunks_of(n);
     if ((int64_t)blockIdx.x >= nchunks) return;
@@ -331,21 +333,47 @@ index_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *_
     load_qsum<DI>(qI, qi, HI, s_q);
     __syncthreads();
 
-    const uint16_t *kbase = kI + __ldg(cu_csa + p.b) * DI;
+    // Coalesced scan: LPR lanes read one key row (16 bytes each), so one warp
+    // load covers 32/LPR consecutive rows; the lanes' partial dot products are
+    // summed with shuffles.  Each warp owns a contiguous run of the chunk.
+    constexpr int LPR = DI / 8;                         // lanes per key row
+    constexpr int RPW = 32 / LPR;                       // rows per warp load
+    constexpr int ROWS_W = kScanChunk / (kScanThreads / 32);
+    constexpr int ITER = ROWS_W / RPW;
+    constexpr int UNR = ITER < 8 ? ITER : 8;
+    static_assert(ITER % UNR == 0, "scan unroll");
+    const int lane = tid & 31, warp = tid >> 5;
+    const int cg = lane % LPR, sub = lane / LPR;
+    float qv[8];
+#pragma unroll
+    for (int x = 0; x < 8; x++) qv[x] = s_q[cg * 8 + x];
+    const uint16_t *kbase = kI + p.e0 * DI;
     uint32_t *keys = w.keys + qg * w.key_stride;
-    const int64_t c0 = (int64_t)blockIdx.x * kScanChunk;
-    float sc[kScanChunk / kScanThreads];
+    const int64_t r0 = (int64_t)blockIdx.x * kScanChunk + warp * ROWS_W + sub;
+    for (int it0 = 0; it0 < ITER; it0 += UNR) {
+        uint4 v[UNR];
 #pragma unroll
-    for (int i = 0; i < kScanChunk / kScanThreads; i++) {
-        const int64_t j = c0 + i * kScanThreads + tid;
-        sc[i] = j < n ? score_row<DI>(kbase + j * DI, s_q) : 0.f;
-    }
+        for (int u = 0; u < UNR; u++) {
+            const int64_t j = r0 + (int64_t)(it0 + u) * RPW;
+            v[u] = j < n ? __ldg(reinterpret_cast<const uint4 *>(kbase + j * DI) + cg) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-    for (int i = 0; i < kScanChunk / kScanThreads; i++) {
-        const int64_t j = c0 + i * kScanThreads + tid;
-        const uint32_t key = score_key(sc[i]);
-        if (j < n) keys[j] = key;
-        hist_add(s_hist, key >> (32 - kHistBits), j < n);
+        for (int u = 0; u < UNR; u++) {
+            const int64_t j = r0 + (int64_t)(it0 + u) * RPW;
+            const uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                acc = fmaf(qv[2 * k], bf16_lo(wd[k]), acc);
+                acc = fmaf(qv[2 * k + 1], bf16_hi(wd[k]), acc);
+            }
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            const bool valid = cg == 0 && j < n;
+            const uint32_t key = score_key(acc);
+            if (valid) keys[j] = key;
+            hist_add(s_hist, key >> (32 - kHistBits), valid);
+        }
     }
     __syncthreads();
     uint32_t *ghist = w.hist + qg * kHistBins;
@@ -423,11 +451,14 @@ index_filter_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
     __shared__ int s_last;
     __shared__ int32_t s_idx[kMaxTopK];
     __shared__ uint32_t s_key[kMaxTopK];
+    __shared__ uint64_t s_cand[kFilterSmemCand];
 
+    griddep_launch();   // the attention after this kernel may launch now
+    griddep_wait();     // the scan's key rows, histograms and boundary bins are complete
     const int tid = threadIdx.x;
     const int64_t qg = blockIdx.y;
     const int64_t qi = q_begin + qg;
-    const QueryPos p = query_pos(cu_kv, cu_q, batch, qi);
+    const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);
     const int64_t n = (p.t + 1) / ratio;
     const int64_t nchunks = chunks_of(n);
     if ((int64_t)blockIdx.x >= nchunks) return;
@@ -461,6 +492,13 @@ index_filter_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
     const uint32_t n_cand = __ldcg(meta + 3);
     const int64_t k_eff = n < top_k ? n : top_k;
     const uint32_t need = (uint32_t)k_eff - __ldcg(meta + 5);   // from the candidates
+    // the candidates are read once into shared memory when they fit; the radix
+    // passes and the gather below then read them from there
+    const bool cand_smem = n_cand <= (uint32_t)kFilterSmemCand;
+    if (cand_smem)
+        for (uint32_t c = tid; c < n_cand; c += kScanThreads) s_cand[c] = __ldcg(cand + c);
+    __syncthreads();
+    auto cand_at = [&](uint32_t c) -> uint64_t { return cand_smem ? s_cand[c] : __ldcg(cand + c); };
     // composite keys of candidates share their top 12 bits; select on bits 51..0
     uint64_t prefix = 0, hmask = 0;
     bool take_none = need == 0;
@@ -473,7 +511,7 @@ index_filter_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
             __syncthreads();
             for (uint32_t base = 0; base < n_cand; base += kScanThreads) {
                 const uint32_t c = base + tid;
-                const uint64_t ck = c < n_cand ? __ldcg(cand + c) : 0ull;
+                const uint64_t ck = c < n_cand ? cand_at(c) : 0ull;
                 hist_add(s_hist, (uint32_t)((ck >> s) & dmask), c < n_cand && (ck & hmask) == prefix);
             }
             __syncthreads();
@@ -501,7 +539,7 @@ index_filter_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
     }
     if (!take_none) {
         for (uint32_t c = tid; c < n_cand; c += kScanThreads) {
-            const uint64_t ck = __ldcg(cand + c);
+            const uint64_t ck = cand_at(c);
             if ((ck & hmask) >= prefix) {
                 const uint32_t pos = atomicAdd(&s_cnt, 1u);
                 if (pos < kMaxTopK) {
@@ -559,6 +597,227 @@ index_filter_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
     }
 }
 
+// ---------------------------------------------------------------------------
+// path 3 (decode-sized batches, rows of up to kSelMaxN entries): a scan that
+// only streams, then one selecting CTA per query.
+//
+// index_chunk_scan_kernel: each CTA brings one 64 KiB chunk of indexer keys
+// into shared memory with a single bulk copy, scores its rows, stores their
+// keys and adds its histogram of the keys' top 12 bits into the query's
+// global histogram (reductions, nothing waits on them).
+//
+// index_select_kernel: one CTA per query holds the query's whole key row in
+// registers (a contiguous segment per thread) after one round trip, finds
+// the exact k-th key (the 12-bit histogram, then 8 + 8 + 4 more bits over
+// the keys of the boundary bin), and writes the selection in index order
+// with one block-wide scan.  It returns the histogram to zero.
+// ---------------------------------------------------------------------------
+constexpr int kChunkBytes = 64 * 1024;
+
+template <int DI>
+__global__ void __launch_bounds__(kScanThreads)
+index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                        const int64_t *__restrict__ cu_csa, int64_t q_begin, const uint16_t *__restrict__ qI,
+                        const uint16_t *__restrict__ kI, int HI, int ratio, WsD w, int *err)
+{
+    constexpr int ROWS = kChunkBytes / (2 * DI);
+    constexpr int LPR = DI / 8;                         // lanes per key row
+    constexpr int RPW = 32 / LPR;                       // rows per warp step
+    constexpr int NWARP = kScanThreads / 32;
+    extern __shared__ __align__(128) uint8_t s_rows[];
+    __shared__ float s_q[DI];
+    __shared__ uint32_t s_hist[kHistBins];
+    __shared__ __align__(8) uint64_t s_bar;
+
+    griddep_launch();   // the select kernel may launch; it waits for this grid
+    const int tid = threadIdx.x;
+    const int64_t qg = blockIdx.y;
+    const int64_t qi = q_begin + qg;
+    const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);
+    const int64_t n = (p.t + 1) / ratio;
+    const int64_t r0 = (int64_t)blockIdx.x * ROWS;
+    if (r0 >= n) return;
+    if (!entry_count_ok(cu_csa, p, ratio) || n > w.key_stride) return;   // reported by the select kernel
+    const int rows = (int)(n - r0 < ROWS ? n - r0 : ROWS);
+    const uint16_t *kbase = kI + (p.e0 + r0) * DI;
+    const uint32_t bar = smem_u32(&s_bar);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_expect_tx(bar, (uint32_t)rows * DI * 2);
+        bulk_g2s(smem_u32(s_rows), kbase, (uint32_t)rows * DI * 2, bar);
+    }
+    for (int i = tid; i < kHistBins; i += kScanThreads) s_hist[i] = 0;
+    load_qsum<DI>(qI, qi, HI, s_q);
+    __syncthreads();
+    const int lane = tid & 31, warp = tid >> 5;
+    const int cg = lane % LPR, sub = lane / LPR;
+    float qv[8];
+#pragma unroll
+    for (int x = 0; x < 8; x++) qv[x] = s_q[cg * 8 + x];
+    const bool landed = mbar_wait(bar, 0);
+    if (!landed) {
+        if (tid == 0) set_error(err, CSA_ERR_TIMEOUT);
+        return;   // histogram incomplete: the select kernel sees a count mismatch and pads the row
+    }
+    uint32_t *keys = w.keys + qg * w.key_stride + r0;
+    for (int rb = warp * RPW; rb < ROWS; rb += NWARP * RPW) {
+        const int row = rb + sub;
+        const bool in = row < rows;
+        const uint4 v = in ? *reinterpret_cast<const uint4 *>(s_rows + row * (2 * DI) + cg * 16) : make_uint4(0, 0, 0, 0);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            acc = fmaf(qv[2 * k], bf16_lo(wd[k]), acc);
+            acc = fmaf(qv[2 * k + 1], bf16_hi(wd[k]), acc);
+        }
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        const bool valid = cg == 0 && in;
+        const uint32_t key = score_key(acc);
+        if (valid) keys[row] = key;
+        hist_add(s_hist, key >> (32 - kHistBits), valid);
+    }
+    __syncthreads();
+    uint32_t *ghist = w.hist + qg * kHistBins;
+    for (int i = tid; i < kHistBins; i += kScanThreads) {
+        const uint32_t c = s_hist[i];
+        if (c) atomicAdd(ghist + i, c);
+    }
+}
+
+template <int NT, int KPT>
+__global__ void __launch_bounds__(NT, 1)
+index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                    const int64_t *__restrict__ cu_csa, int64_t q_begin, int ratio, int top_k, WsD w,
+                    int32_t *__restrict__ idx_out, float *__restrict__ score_out, int *err)
+{
+    constexpr int BPT = kHistBins / NT;                 // top-level bins per thread
+    static_assert(KPT % 4 == 0 && kHistBins % NT == 0, "select tiling");
+    __shared__ uint32_t s_hist[256];
+    __shared__ uint32_t s_w[2 * (NT / 32) + 1];
+    __shared__ uint32_t s_digit, s_above;
+
+    griddep_wait();   // every chunk's keys and histogram counts are in place
+    const int tid = threadIdx.x;
+    const int64_t qg = blockIdx.x;
+    const int64_t qi = q_begin + qg;
+    const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);
+    const int64_t n = (p.t + 1) / ratio;
+    int32_t *idx_row = idx_out + qi * top_k;
+    float *sc_row = score_out ? score_out + qi * top_k : nullptr;
+    uint32_t *ghist = w.hist + qg * kHistBins;
+    if (!entry_count_ok(cu_csa, p, ratio) || n > w.key_stride || n > (int64_t)NT * KPT) {
+        if (tid == 0) set_error(err, CSA_ERR_DEVICE);
+        write_row_padding(idx_row, sc_row, 0, top_k);
+        for (int i = tid; i < kHistBins; i += NT) ghist[i] = 0;
+        return;
+    }
+    // one round trip: this thread's key segment and its histogram bins
+    const uint32_t *krow = w.keys + qg * w.key_stride;
+    const int64_t seg0 = (int64_t)tid * KPT;
+    const int m = (int)(n - seg0 < 0 ? 0 : (n - seg0 < KPT ? n - seg0 : KPT));   // valid keys here
+    uint32_t key[KPT];
+#pragma unroll
+    for (int i = 0; i < KPT; i += 4) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (i < m) v = __ldcg(reinterpret_cast<const uint4 *>(krow + seg0 + i));
+        key[i] = v.x;
+        key[i + 1] = v.y;
+        key[i + 2] = v.z;
+        key[i + 3] = v.w;
+    }
+    uint32_t hc[BPT], hsum = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; i++) {
+        hc[i] = __ldcg(ghist + (kHistBins - 1 - BPT * tid - i));   // walked from the top bin down
+        hsum += hc[i];
+    }
+    const uint32_t k_eff = (uint32_t)(n < top_k ? n : top_k);
+    // level 1: the 12-bit bin that holds the k-th largest key
+    uint32_t tot;
+    const uint32_t excl = block_scan<NT>(hsum, s_w, tot);
+    if (k_eff > 0 && excl < k_eff && k_eff <= excl + hsum) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int i = 0; i < BPT; i++) {
+            if (acc + hc[i] >= k_eff) {
+                s_digit = (uint32_t)(kHistBins - 1 - BPT * tid - i);
+                s_above = acc;
+                break;
+            }
+            acc += hc[i];
+        }
+    }
+    __syncthreads();
+    // the histogram has been read: leave it zero for the next call
+#pragma unroll
+    for (int i = 0; i < BPT; i++) ghist[kHistBins - 1 - BPT * tid - i] = 0;
+    if (tot != (uint32_t)n) {   // a chunk did not land (reported by the scan)
+        write_row_padding(idx_row, sc_row, 0, top_k);
+        return;
+    }
+    uint32_t kstar = 0, need_eq = 0;
+    if (k_eff < (uint32_t)n) {
+        uint32_t prefix = s_digit << 20, pmask = 0xfff00000u, remaining = k_eff - s_above;
+        // levels 2-4 over the keys of the boundary bin: bits 19..12, 11..4, 3..0
+#pragma unroll 1
+        for (int level = 0; level < 3; level++) {
+            const int sh = level == 0 ? 12 : (level == 1 ? 4 : 0);
+            const uint32_t dm = level == 2 ? 0xfu : 0xffu;
+            for (int i = tid; i < 256; i += NT) s_hist[i] = 0;
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < KPT; i++)
+                if (i < m && (key[i] & pmask) == prefix) atomicAdd(&s_hist[(key[i] >> sh) & dm], 1u);
+            __syncthreads();
+            if (tid < 32) find_digit_256(s_hist, remaining, &s_digit, &s_above);
+            __syncthreads();
+            remaining -= s_above;
+            prefix |= s_digit << sh;
+            pmask |= dm << sh;
+            __syncthreads();
+        }
+        kstar = prefix;
+        need_eq = remaining;   // keys equal to kstar to take, lowest index first
+    } else {
+        need_eq = 0xffffffffu;   // take every key: kstar = 0 is below every valid key or equal to it
+    }
+    // ordered emission: a thread's keys are contiguous in index order
+    uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int i = 0; i < KPT; i++) {
+        n_gt += (i < m && key[i] > kstar) ? 1u : 0u;
+        n_eq += (i < m && key[i] == kstar) ? 1u : 0u;
+    }
+    uint32_t t1, t2;
+    const uint32_t gt_before = block_scan<NT>(n_gt, s_w, t1);
+    const uint32_t eq_before = block_scan<NT>(n_eq, s_w, t2);
+    uint32_t pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
+    uint32_t eq_rank = eq_before;
+#pragma unroll
+    for (int i = 0; i < KPT; i++) {
+        if (i >= m) continue;
+        bool take = key[i] > kstar;
+        if (key[i] == kstar) {
+            take = eq_rank < need_eq;
+            eq_rank++;
+        }
+        if (take) {
+            if (pos < (uint32_t)top_k) {
+                idx_row[pos] = (int32_t)(seg0 + i);
+                if (sc_row) sc_row[pos] = key_score(key[i]);
+            }
+            pos++;
+        }
+    }
+    write_row_padding(idx_row, sc_row, (int)k_eff, top_k);
+    if (tid == NT - 1 && pos != k_eff) set_error(err, CSA_ERR_DEVICE);
+}
+
+constexpr int64_t kSelMaxN = 512 * 64;    // longest row the select kernel holds (entries)
+
 bool use_cta_path(const IndexArgs &a)
 {
     const int64_t max_n = a.max_kv_len / a.ratio;
@@ -586,7 +845,7 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
         for (int64_t q0 = 0; q0 < a.total_q; q0 += 1 << 30) {
             const int64_t nq = a.total_q - q0 < (1 << 30) ? a.total_q - q0 : (1 << 30);
             cudaError_t e = launch_kernel("index_topk_cta", index_topk_cta_kernel<DI>, dim3((unsigned)nq),
-                                          dim3(kCtaThreads), smem, st, a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0,
+                                          dim3(kCtaThreads), smem, st, false, a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0,
                                           a.q_idx, a.k_idx, a.n_heads_idx, a.ratio, a.top_k, (int)nsm,
                                           a.idx_out, a.score_out, a.err);
             if (e != cudaSuccess) return e;
@@ -596,14 +855,35 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
     const int64_t gq = group_size(a);
     const int64_t nchunks = (max_n <= 0 ? 1 : (max_n + kScanChunk - 1) / kScanChunk);
     WsD w = carve_wsd(a.ws, gq, max_n < 1 ? 1 : max_n, a.top_k);
+    if (max_n <= kSelMaxN) {
+        constexpr int ROWS = kChunkBytes / (2 * DI);
+        const int64_t nch = max_n <= 0 ? 1 : (max_n + ROWS - 1) / ROWS;
+        for (int64_t q0 = 0; q0 < a.total_q; q0 += gq) {
+            const int64_t nq = a.total_q - q0 < gq ? a.total_q - q0 : gq;
+            cudaError_t e = launch_kernel("index_scan", index_chunk_scan_kernel<DI>, dim3((unsigned)nch, (unsigned)nq),
+                                          dim3(kScanThreads), (size_t)kChunkBytes, st, false, a.batch, a.cu_kv,
+                                          a.cu_q, a.cu_csa, q0, a.q_idx, a.k_idx, a.n_heads_idx, a.ratio, w, a.err);
+            if (e != cudaSuccess) return e;
+            if (max_n <= 1024 * 16)
+                e = launch_kernel("index_select", index_select_kernel<1024, 16>, dim3((unsigned)nq), dim3(1024), 0,
+                                  st, true, a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0, a.ratio, a.top_k, w, a.idx_out,
+                                  a.score_out, a.err);
+            else
+                e = launch_kernel("index_select", index_select_kernel<512, 64>, dim3((unsigned)nq), dim3(512), 0, st,
+                                  true, a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0, a.ratio, a.top_k, w, a.idx_out,
+                                  a.score_out, a.err);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     for (int64_t q0 = 0; q0 < a.total_q; q0 += gq) {
         const int64_t nq = a.total_q - q0 < gq ? a.total_q - q0 : gq;
         dim3 grid((unsigned)nchunks, (unsigned)nq);
-        cudaError_t e = launch_kernel("index_scan", index_scan_kernel<DI>, grid, dim3(kScanThreads), 0, st,
+        cudaError_t e = launch_kernel("index_scan", index_scan_kernel<DI>, grid, dim3(kScanThreads), 0, st, false,
                                       a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0, a.q_idx, a.k_idx, a.n_heads_idx,
                                       a.ratio, a.top_k, w, a.idx_out, a.score_out, a.err);
         if (e != cudaSuccess) return e;
-        e = launch_kernel("index_filter", index_filter_kernel, grid, dim3(kScanThreads), 0, st, a.batch, a.cu_kv,
+        e = launch_kernel("index_filter", index_filter_kernel, grid, dim3(kScanThreads), 0, st, true, a.batch, a.cu_kv,
                           a.cu_q, a.cu_csa, q0, a.ratio, a.top_k, w, a.idx_out, a.score_out, a.err);
         if (e != cudaSuccess) return e;
     }

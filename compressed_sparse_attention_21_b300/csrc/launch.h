@@ -17,9 +17,13 @@ void timing_record(const char *name, cudaEvent_t start, cudaEvent_t stop);
 // Raise a kernel's dynamic shared memory limit (remembered per kernel and device).
 cudaError_t ensure_smem_fn(const void *kern, size_t smem);
 
+// Launch `kern` on `st`.  With `pdl` the launch carries programmatic stream
+// serialisation: it may begin while the kernel before it on the stream is
+// still running, and must execute griddep_wait() before it touches anything
+// that kernel (or any earlier work) writes or reads.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(const char *name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                          cudaStream_t st, Args &&...args)
+                          cudaStream_t st, bool pdl, Args &&...args)
 {
     cudaError_t e = cudaSuccess;
     if (smem > 48 * 1024) {
@@ -33,8 +37,18 @@ cudaError_t launch_kernel(const char *name, void (*kern)(KArgs...), dim3 grid, d
         cudaEventCreate(&e1);
         cudaEventRecord(e0, st);
     }
-    kern<<<grid, block, smem, st>>>(std::forward<Args>(args)...);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (pdl && !timed) ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (timed) {
         cudaEventRecord(e1, st);
         timing_record(name, e0, e1);
@@ -64,6 +78,7 @@ struct IndexArgs {
     int batch;
     int max_kv_len, max_q_len;
     int64_t total_q;
+    bool pdl;             // the first kernel may overlap the stream's previous kernel
     const int64_t *cu_kv, *cu_q, *cu_csa;
     const uint16_t *q_idx, *k_idx;
     int n_heads_idx, d_idx, ratio, top_k;
@@ -98,10 +113,15 @@ struct AttendArgs {
     void *ws;
     size_t ws_bytes;
     int *err;
+    bool pdl;             // may overlap the stream's previous kernel
     int num_sms;          // SMs of the current device (sizes the split-KV grid)
     int sm_share;         // SMs this launch may count on (concurrent branches)
 };
 bool attend_supported(int n_heads, int d);
+// tcgen05 path (attend_tc.cu): d = 512, heads a multiple of 64, at least as
+// many 64-head units as SMs; needs no workspace.
+bool attend_tc_applicable(const AttendArgs &a);
+cudaError_t launch_attend_tc(const AttendArgs &a, cudaStream_t st);
 size_t attend_workspace_bytes(const AttendArgs &a);
 cudaError_t launch_attend(const AttendArgs &a, cudaStream_t st);
 
