@@ -296,13 +296,13 @@ attend_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__res
             const float m_old = s_m[row];
             const float m_new = fmaxf(m_old, mx);
             const bool none = m_new == -INFINITY;
-            const float alpha = none ? 1.f : exp2f(m_old - m_new);
+            const float alpha = none ? 1.f : fast_exp2(m_old - m_new);
             float sum = 0.f;
             uint32_t pk[C::CPT / 2];
 #pragma unroll
             for (int i = 0; i < C::CPT; i += 2) {
-                const float p0 = none ? 0.f : exp2f(s[i] - m_new);
-                const float p1 = none ? 0.f : exp2f(s[i + 1] - m_new);
+                const float p0 = none ? 0.f : fast_exp2(s[i] - m_new);
+                const float p1 = none ? 0.f : fast_exp2(s[i + 1] - m_new);
                 sum += p0 + p1;
                 pk[i / 2] = pack_bf16x2(p0, p1);
             }
@@ -418,7 +418,7 @@ attend_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__res
         float Lsum = 0.f;
         for (int s = 0; s < nsplit; s++) {
             const float ms = __ldcg(ml + (s * HT + row) * 2);
-            const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+            const float w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - M);
             s_wt[row * kMaxSplits + s] = w;
             Lsum += w * __ldcg(ml + (s * HT + row) * 2 + 1);
         }

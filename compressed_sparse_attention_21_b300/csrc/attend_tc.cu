@@ -12,7 +12,8 @@
 //     S^T[key, head] = K[key, :] . Q[head, :]       M = 128 keys, N = 64, K = 512
 //     O^T[d, head]  += K[key, d]^T . P^T[key, head]  M = 4 x 128 d,   N = 64, K = 128
 // The same shared-memory key tile is the K-major A operand of the first
-// product and the MN-major A operand of the second.  S^T takes 64 tensor-
+// product and the MN-major A operand of the second; P is stored key-major
+// (one 128-byte row of 64 heads per key) as the MN-major B operand.  S^T takes 64 tensor-
 // memory columns and O^T 256.
 //
 // Warp roles (256 threads): warps 0-3 run the softmax (thread i owns key i
@@ -40,7 +41,7 @@ constexpr int kRegions = kTcD / 64;          // 64-column regions of a 128-byte 
 constexpr int kProd = 96;                    // producer threads (warps 5-7)
 constexpr int kProdBase = 160;
 constexpr uint32_t kRegK = kTcKeys * 128;    // 16 KiB per key region
-constexpr uint32_t kRegQ = kTcHeads * 128;   // 8 KiB per query / P region
+constexpr uint32_t kRegQ = kTcHeads * 128;   // 8 KiB per query region
 constexpr int kTcIdxCap = 2048;
 constexpr float kTcLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;         // raise a head's maximum only beyond 2^8
@@ -191,10 +192,23 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
 
     if (warp >= 5) {
         // ------------------------------------------------------------ producers
+        // Thread pt copies chunk pc (16 bytes) of key rows pk0, pk0 + 12, ...:
+        // a warp covers four whole 128-byte row segments per instruction.  The
+        // row sources of a tile are looked up once; the eight regions are then
+        // issued back to back and published in order as they land.
         const int pt = tid - kProdBase;
+        const int pc = pt & 7, pk0 = pt >> 3;
+        constexpr int RSTEP = kProd / 8;                          // 12 rows per pass
+        constexpr int KPP = (kTcKeys + RSTEP - 1) / RSTEP;        // 11 rows per thread
         const uint16_t *qrow = q + (qi * H + (int64_t)hg * kTcHeads) * kTcD;
         bool ok = true;
         for (int t = 0; t < T && ok; t++) {
+            const uint16_t *src[KPP];
+#pragma unroll
+            for (int i = 0; i < KPP; i++) {
+                const int k = pk0 + RSTEP * i;
+                src[i] = k < kTcKeys ? tc_key_row<GATHER>(ks, t * kTcKeys + k) : nullptr;
+            }
 #pragma unroll 1
             for (int r = 0; r < kRegions; r++) {
                 if (t > 0 && (r & 1) == 0 && !mbar_wait(bar(BAR_KFREE + r / 2), (uint32_t)((t - 1) & 1))) {
@@ -203,41 +217,40 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
                     break;
                 }
                 if (t == 0)   // the Q region travels with the first tile's region
-                    for (int ch = pt; ch < kTcHeads * 8; ch += kProd) {
-                        const int h = ch >> 3, c = ch & 7;
-                        cp_async_16(sb + OFF_Q + r * kRegQ + h * 128 + ((c ^ (h & 7)) << 4),
-                                    qrow + (int64_t)h * kTcD + r * 64 + c * 8, 16);
+#pragma unroll
+                    for (int i = 0; i < (kTcHeads + RSTEP - 1) / RSTEP; i++) {
+                        const int h = pk0 + RSTEP * i;
+                        if (h < kTcHeads)
+                            cp_async_16(sb + OFF_Q + r * kRegQ + h * 128 + ((pc ^ (h & 7)) << 4),
+                                        qrow + (int64_t)h * kTcD + r * 64 + pc * 8, 16);
                     }
-                for (int ch = pt; ch < kTcKeys * 8; ch += kProd) {
-                    const int k = ch >> 3, c = ch & 7;
-                    const uint16_t *src = tc_key_row<GATHER>(ks, t * kTcKeys + k);
-                    cp_async_16(sb + OFF_K + r * kRegK + k * 128 + ((c ^ (k & 7)) << 4),
-                                src ? (const void *)(src + r * 64 + c * 8) : (const void *)kv, src ? 16 : 0);
+#pragma unroll
+                for (int i = 0; i < KPP; i++) {
+                    const int k = pk0 + RSTEP * i;
+                    if (k < kTcKeys)
+                        cp_async_16(sb + OFF_K + r * kRegK + k * 128 + ((pc ^ (k & 7)) << 4),
+                                    src[i] ? (const void *)(src[i] + r * 64 + pc * 8) : (const void *)kv,
+                                    src[i] ? 16 : 0);
                 }
                 cp_async_commit();
-                if (r >= 3) {
-                    cp_async_wait<3>();
-                    tc::fence_proxy_async();
-                    mbar_arrive(bar(BAR_KFULL + r - 3));
-                }
             }
             if (!ok) break;
-            cp_async_wait<2>();
-            tc::fence_proxy_async();
-            mbar_arrive(bar(BAR_KFULL + 5));
-            cp_async_wait<1>();
-            tc::fence_proxy_async();
-            mbar_arrive(bar(BAR_KFULL + 6));
-            cp_async_wait<0>();
-            tc::fence_proxy_async();
-            mbar_arrive(bar(BAR_KFULL + 7));
+            // publish the regions in order as their copies complete
+            cp_async_wait<7>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 0));
+            cp_async_wait<6>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 1));
+            cp_async_wait<5>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 2));
+            cp_async_wait<4>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 3));
+            cp_async_wait<3>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 4));
+            cp_async_wait<2>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 5));
+            cp_async_wait<1>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 6));
+            cp_async_wait<0>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 7));
         }
         cp_async_wait<0>();
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, kTcHeads, false, false);
-            constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, kTcHeads, true, false);
+            constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, kTcHeads, true, true);
             bool ok = true;
             for (int t = 0; t < T && ok; t++) {
                 if (t > 0 && !mbar_wait(bar(BAR_SFREE), (uint32_t)((t - 1) & 1))) {
@@ -269,7 +282,7 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
 #pragma unroll
                     for (int k8 = 0; k8 < 8; k8++) {
                         const uint64_t a = tc::sdesc_sw128(sb + OFF_K + 2 * m * kRegK + k8 * 2048, kRegK, 1024);
-                        const uint64_t b = tc::sdesc_sw128(sb + OFF_P + (k8 >> 2) * kRegQ + (k8 & 3) * 32, 16, 1024);
+                        const uint64_t b = tc::sdesc_sw128(sb + OFF_P + k8 * 2048, kRegK, 1024);
                         tc::mma_ss(tmem + TM_O + 64 * m, a, b, id_pv, t > 0 || k8 > 0);
                     }
                     tc::mma_commit(bar(BAR_KFREE + m));
@@ -322,7 +335,7 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
                 float m_new = m_old, alpha = 1.f;
                 if (M > m_old + kRescaleLog2 || (m_old == -INFINITY && M != -INFINITY)) {
                     m_new = M;
-                    alpha = exp2f(m_old - m_new);   // 0 when nothing was accumulated yet
+                    alpha = fast_exp2(m_old - m_new);   // 0 when nothing was accumulated yet
                     if (t > 0) s_flag[1] = 1;
                 }
                 s_mn[tid] = m_new;
@@ -349,15 +362,20 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
 #pragma unroll
             for (int h = 0; h < 64; h++) {
                 const float mn = s_mn[h];
-                s[h] = (mn == -INFINITY) ? 0.f : exp2f(s[h] - mn);
+                s[h] = (mn == -INFINITY) ? 0.f : fast_exp2(s[h] - mn);
             }
             {
-                uint8_t *reg = sP + (tid >> 6) * kRegQ;
-                const int ck = (tid & 63) >> 3, wi = (tid & 7) * 2;
+                // this key's 64 heads form one 128-byte swizzled row of the P tile
+                uint8_t *prow = sP + tid * 128;
 #pragma unroll
-                for (int h = 0; h < 64; h++)
-                    *reinterpret_cast<uint16_t *>(reg + h * 128 + ((ck ^ (h & 7)) << 4) + wi) =
-                        (uint16_t)f32_to_bf16_bits(s[h]);
+                for (int c = 0; c < 8; c++) {
+                    uint4 v;
+                    v.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
+                    v.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
+                    v.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
+                    v.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
+                    *reinterpret_cast<uint4 *>(prow + ((c ^ (tid & 7)) << 4)) = v;
+                }
             }
             warp_reduce64<false>(s, r0, r1);
             s_rsum[warp * 64 + 2 * lane] = r0;

@@ -83,9 +83,22 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f)
     return u >> 16;
 }
 
+// Two floats -> packed bf16 pair (lo in the low half), round to nearest even,
+// in one conversion instruction.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
-    return f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 2^x by the hardware approximation (ex2.approx: relative error about 2^-22;
+// 2^-inf = 0).  Used for softmax weights, which are rounded to bf16 afterwards.
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float r;
+    asm("ex2.approx.f32 %0, %1;\n" : "=f"(r) : "f"(x));
+    return r;
 }
 
 // Order-preserving map of an fp32 score onto uint32 (larger key = larger score);
