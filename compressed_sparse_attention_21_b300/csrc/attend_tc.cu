@@ -6,24 +6,26 @@
 // same as in attend.cu: selected (or all visible) entries plus the raw
 // tokens of the query's own open block.
 //
-// One CTA computes 64 heads of one query over all of its keys, 128 keys per
-// tile.  Keys are the M dimension of both products, so that every tensor-
-// memory accumulator keeps the 128-lane layout (lane = row):
-//     S^T[key, head] = K[key, :] . Q[head, :]       M = 128 keys, N = 64, K = 512
-//     O^T[d, head]  += K[key, d]^T . P^T[key, head]  M = 4 x 128 d,   N = 64, K = 128
-// The same shared-memory key tile is the K-major A operand of the first
-// product and the MN-major A operand of the second; P is stored key-major
-// (one 128-byte row of 64 heads per key) as the MN-major B operand.  S^T takes 64 tensor-
-// memory columns and O^T 256.
+// One CTA computes 64 heads of one query over all of its keys, in tiles of
+// 64 keys.  Keys are the M dimension of both products:
+//     S^T[key, head] = K[key, :] . Q[head, :]       M = 64 keys,      N = 64, K = 512
+//     O^T[d, head]  += K[key, d]^T . P^T[key, head]  M = 4 x 128 d,   N = 64, K = 64
+// The shared-memory key tile is the K-major A operand of the first product
+// and the MN-major A operand of the second; P is stored key-major (one
+// 128-byte row of 64 heads per key) as the MN-major B operand.  With M = 64
+// the accumulator row r sits in tensor-memory lane 32 (r / 16) + r % 16.
+// Two key stages, two S^T buffers and two P stages let the tensor core run
+// S^T of tile t+1 while the softmax of tile t proceeds, and the gather of a
+// stage overlap the other stage's products.  Tensor memory: S^T x 2 (64
+// columns each) and O^T (4 x 64 columns).
 //
-// Warp roles (256 threads): warps 0-3 run the softmax (thread i owns key i
-// of the tile, then row d = 128 m + i of the output), warp 4 lane 0 issues
-// the MMAs, warps 5-7 gather key rows into the swizzled tile with cp.async.
-// The tile is split in eight 64-column regions with their own barriers, so
-// the next tile's regions reload as soon as the products reading them are
-// done.  The running maximum of a head is raised only when a tile exceeds it
-// by more than 2^8 (then the accumulated O^T column and sum are rescaled);
-// the result is exact either way because the sum uses the same maximum.
+// Warp roles (352 threads): warps 0-3 softmax (thread (w, l) takes key
+// 16 w + l % 16 of the tile, heads 32 (l / 16) .. +31; afterwards row
+// d = 128 m + 32 w + l of the output), warp 4 lane 0 issues the MMAs, warps
+// 5-7 gather even tiles and warps 8-10 odd tiles with cp.async.  The
+// running maximum of a head is raised only when a tile exceeds it by more
+// than 2^8 (the accumulated O^T column and sum are then rescaled); the
+// result is exact either way because the sum uses the same maximum.
 // Every wait is bounded: one that runs out reports CSA_ERR_TIMEOUT.
 #include "common.cuh"
 #include "launch.h"
@@ -33,54 +35,54 @@ namespace csa {
 
 namespace {
 
-constexpr int kTcThreads = 256;
-constexpr int kTcKeys = 128;                 // keys per tile (M)
+constexpr int kTcThreads = 352;
+constexpr int kTcKeys = 64;                  // keys per tile (M of S^T)
 constexpr int kTcHeads = 64;                 // heads per CTA (N)
 constexpr int kTcD = 512;
 constexpr int kRegions = kTcD / 64;          // 64-column regions of a 128-byte swizzled row
-constexpr int kProd = 96;                    // producer threads (warps 5-7)
-constexpr int kProdBase = 160;
-constexpr uint32_t kRegK = kTcKeys * 128;    // 16 KiB per key region
-constexpr uint32_t kRegQ = kTcHeads * 128;   // 8 KiB per query region
+constexpr int kProd = 96;                    // producer threads per group (3 warps)
+constexpr int kProdBase = 160;               // first producer thread (warp 5)
+constexpr uint32_t kReg = 64 * 128;          // 8 KiB: 64 rows x 128 bytes
+constexpr uint32_t kStage = kRegions * kReg; // 64 KiB key stage
 constexpr int kTcIdxCap = 2048;
 constexpr float kTcLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;         // raise a head's maximum only beyond 2^8
 
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + kRegions * kRegQ;      // 64 KiB
-constexpr uint32_t OFF_P = OFF_K + kRegions * kRegK;      // + 128 KiB
-constexpr uint32_t OFF_BAR = OFF_P + 2 * kRegQ;           // + 16 KiB
-constexpr int BAR_KFULL = 0, BAR_KFREE = 8, BAR_SFULL = 12, BAR_SFREE = 13, BAR_PFULL = 14, BAR_OFULL = 15;
+constexpr uint32_t OFF_Q = 0;                              // 8 regions x (64 heads x 128 B)
+constexpr uint32_t OFF_K = OFF_Q + kStage;                 // 2 stages x 8 regions x (64 keys x 128 B)
+constexpr uint32_t OFF_P = OFF_K + 2 * kStage;             // 2 stages x (64 keys x 128 B)
+constexpr uint32_t OFF_BAR = OFF_P + 2 * kReg;
+// barriers: kfull[2], kfree[2] (P V of the stage's tile done), sfull[2], sfree[2], pfull[2], ofull
+constexpr int BAR_KFULL = 0, BAR_KFREE = 2, BAR_SFULL = 4, BAR_SFREE = 6, BAR_PFULL = 8, BAR_OFULL = 10;
 constexpr uint32_t OFF_MISC = OFF_BAR + 16 * 8;
-// misc: tmem slot, flags, per-head m / l / new max / alpha, per-warp tile max and sum
-constexpr uint32_t MISC_TMEM = 0, MISC_FLAG = 4, MISC_M = 16, MISC_L = MISC_M + 256, MISC_MN = MISC_L + 256,
+constexpr uint32_t MISC_TMEM = 0, MISC_FLAG = 4, MISC_M = 32, MISC_L = MISC_M + 256, MISC_MN = MISC_L + 256,
                    MISC_AL = MISC_MN + 256, MISC_RMAX = MISC_AL + 256, MISC_RSUM = MISC_RMAX + 1024,
                    MISC_END = MISC_RSUM + 1024;
 constexpr uint32_t OFF_IDX = OFF_MISC + MISC_END;
 constexpr uint32_t kTcSmem = OFF_IDX + kTcIdxCap * 4 + 1024;   // + alignment slack
 static_assert(kTcSmem <= 232448, "shared memory per CTA");
 
-constexpr uint32_t TM_S = 0;     // S^T: columns 0..63
-constexpr uint32_t TM_O = 64;    // O^T block m: columns 64 + 64 m .. +63
+constexpr uint32_t TM_S = 0;     // S^T buffer s: columns 64 s .. 64 s + 63 (M = 64 lane layout)
+constexpr uint32_t TM_O = 128;   // O^T block m: columns 128 + 64 m .. +63
 constexpr uint32_t kTmemCols = 512;
 
-// Butterfly reduction of 64 values per lane over the 32 lanes of a warp: on
-// return lane L holds the result for heads 2L and 2L+1 in r0, r1.
+// Reduce 32 values per lane over the 16 lanes of a half-warp (xor 8, 4, 2, 1):
+// on return lane l holds the result for values 2 (l % 16) and 2 (l % 16) + 1.
 template <bool MAX>
-__device__ __forceinline__ void warp_reduce64(const float *v, float &r0, float &r1)
+__device__ __forceinline__ void halfwarp_reduce32(const float *v, float &r0, float &r1)
 {
     const int lane = threadIdx.x & 31;
-    float a[32];
+    float a[16];
 #pragma unroll
-    for (int j = 0; j < 32; j++) {
-        const bool up = lane & 16;
-        const float keep = up ? v[32 + j] : v[j];
-        const float send = up ? v[j] : v[32 + j];
-        const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+    for (int j = 0; j < 16; j++) {
+        const bool up = lane & 8;
+        const float keep = up ? v[16 + j] : v[j];
+        const float send = up ? v[j] : v[16 + j];
+        const float got = __shfl_xor_sync(0xffffffffu, send, 8);
         a[j] = MAX ? fmaxf(keep, got) : keep + got;
     }
 #pragma unroll
-    for (int o = 8, half = 16; o >= 1; o >>= 1, half >>= 1) {
+    for (int o = 4, half = 8; o >= 1; o >>= 1, half >>= 1) {
 #pragma unroll
         for (int j = 0; j < half; j++) {
             const bool up = lane & o;
@@ -136,8 +138,7 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
     const QueryPos p = query_pos(cu_kv, cu_q, cu_ent, batch, qi);
     const int64_t n_vis = (p.t + 1) / ratio;
     const int r_tail = (int)((p.t + 1) % ratio);
-    const bool bad = p.t < 0 || p.t >= p.L || p.L > max_kv_len ||
-                     p.ne != p.L / ratio;
+    const bool bad = p.t < 0 || p.t >= p.L || p.L > max_kv_len || p.ne != p.L / ratio;
     if (bad) {
         if (tid == 0) set_error(err, CSA_ERR_DEVICE);
         return;
@@ -163,11 +164,13 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
     volatile int *s_flag = reinterpret_cast<volatile int *>(misc + MISC_FLAG);
 
     if (tid == 0) {
-        for (int r = 0; r < kRegions; r++) mbar_init(bar(BAR_KFULL + r), kProd);
-        for (int m = 0; m < 4; m++) mbar_init(bar(BAR_KFREE + m), 1);
-        mbar_init(bar(BAR_SFULL), 1);
-        mbar_init(bar(BAR_SFREE), 128);
-        mbar_init(bar(BAR_PFULL), 128);
+        for (int s = 0; s < 2; s++) {
+            mbar_init(bar(BAR_KFULL + s), kProd);
+            mbar_init(bar(BAR_KFREE + s), 1);
+            mbar_init(bar(BAR_SFULL + s), 1);
+            mbar_init(bar(BAR_SFREE + s), 128);
+            mbar_init(bar(BAR_PFULL + s), 128);
+        }
         mbar_init(bar(BAR_OFULL), 1);
         fence_mbar_init();
     }
@@ -192,141 +195,165 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
 
     if (warp >= 5) {
         // ------------------------------------------------------------ producers
-        // Thread pt copies chunk pc (16 bytes) of key rows pk0, pk0 + 12, ...:
-        // a warp covers four whole 128-byte row segments per instruction.  The
-        // row sources of a tile are looked up once; the eight regions are then
-        // issued back to back and published in order as they land.
-        const int pt = tid - kProdBase;
+        // Group g (warps 5-7: g = 0, warps 8-10: g = 1) fills stage g with tiles
+        // g, g + 2, ...  Thread pt copies chunk pc (16 bytes) of rows pk0,
+        // pk0 + 12, ...: a warp moves four whole 128-byte row segments per
+        // instruction.
+        const int g = warp >= 8 ? 1 : 0;
+        const int pt = tid - kProdBase - g * kProd;
         const int pc = pt & 7, pk0 = pt >> 3;
         constexpr int RSTEP = kProd / 8;                          // 12 rows per pass
-        constexpr int KPP = (kTcKeys + RSTEP - 1) / RSTEP;        // 11 rows per thread
-        const uint16_t *qrow = q + (qi * H + (int64_t)hg * kTcHeads) * kTcD;
+        constexpr int KPP = (kTcKeys + RSTEP - 1) / RSTEP;        // 6 rows per thread
+        const uint32_t stage = sb + OFF_K + g * kStage;
         bool ok = true;
-        for (int t = 0; t < T && ok; t++) {
-            const uint16_t *src[KPP];
+        for (int t = g; t < T && ok; t += 2) {
+            if (t >= 2 && !mbar_wait(bar(BAR_KFREE + g), (uint32_t)(((t - 2) >> 1) & 1))) {
+                set_error(err, CSA_ERR_TIMEOUT);
+                ok = false;
+                break;
+            }
+            if (t == 0) {   // the Q tile travels with the first key tile
+                const uint16_t *qrow = q + (qi * H + (int64_t)hg * kTcHeads) * kTcD;
+#pragma unroll
+                for (int i = 0; i < KPP; i++) {
+                    const int h = pk0 + RSTEP * i;
+                    if (h < kTcHeads)
+#pragma unroll
+                        for (int r = 0; r < kRegions; r++)
+                            cp_async_16(sb + OFF_Q + r * kReg + h * 128 + ((pc ^ (h & 7)) << 4),
+                                        qrow + (int64_t)h * kTcD + r * 64 + pc * 8, 16);
+                }
+            }
 #pragma unroll
             for (int i = 0; i < KPP; i++) {
                 const int k = pk0 + RSTEP * i;
-                src[i] = k < kTcKeys ? tc_key_row<GATHER>(ks, t * kTcKeys + k) : nullptr;
-            }
-#pragma unroll 1
-            for (int r = 0; r < kRegions; r++) {
-                if (t > 0 && (r & 1) == 0 && !mbar_wait(bar(BAR_KFREE + r / 2), (uint32_t)((t - 1) & 1))) {
-                    set_error(err, CSA_ERR_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-                if (t == 0)   // the Q region travels with the first tile's region
+                if (k < kTcKeys) {
+                    const uint16_t *src = tc_key_row<GATHER>(ks, t * kTcKeys + k);
 #pragma unroll
-                    for (int i = 0; i < (kTcHeads + RSTEP - 1) / RSTEP; i++) {
-                        const int h = pk0 + RSTEP * i;
-                        if (h < kTcHeads)
-                            cp_async_16(sb + OFF_Q + r * kRegQ + h * 128 + ((pc ^ (h & 7)) << 4),
-                                        qrow + (int64_t)h * kTcD + r * 64 + pc * 8, 16);
-                    }
-#pragma unroll
-                for (int i = 0; i < KPP; i++) {
-                    const int k = pk0 + RSTEP * i;
-                    if (k < kTcKeys)
-                        cp_async_16(sb + OFF_K + r * kRegK + k * 128 + ((pc ^ (k & 7)) << 4),
-                                    src[i] ? (const void *)(src[i] + r * 64 + pc * 8) : (const void *)kv,
-                                    src[i] ? 16 : 0);
+                    for (int r = 0; r < kRegions; r++)
+                        cp_async_16(stage + r * kReg + k * 128 + ((pc ^ (k & 7)) << 4),
+                                    src ? (const void *)(src + r * 64 + pc * 8) : (const void *)kv, src ? 16 : 0);
                 }
-                cp_async_commit();
             }
-            if (!ok) break;
-            // publish the regions in order as their copies complete
-            cp_async_wait<7>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 0));
-            cp_async_wait<6>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 1));
-            cp_async_wait<5>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 2));
-            cp_async_wait<4>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 3));
-            cp_async_wait<3>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 4));
-            cp_async_wait<2>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 5));
-            cp_async_wait<1>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 6));
-            cp_async_wait<0>(); tc::fence_proxy_async(); mbar_arrive(bar(BAR_KFULL + 7));
+            cp_async_commit();
+            cp_async_wait<0>();
+            tc::fence_proxy_async();
+            mbar_arrive(bar(BAR_KFULL + g));
         }
         cp_async_wait<0>();
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
+        // S(t) and PV(t) are each issued in tile order; the issuer polls both
+        // and issues whichever is ready first (S(t) needs tile t and a free S
+        // buffer, PV(t) needs P(t)), so neither the gather of the next tile nor
+        // the softmax of the current one stalls the other product.
         if (lane == 0) {
-            constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, kTcHeads, false, false);
+            constexpr uint32_t id_qk = tc::idesc_bf16_f32(64, kTcHeads, false, false);
             constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, kTcHeads, true, true);
+            const uint64_t qa0 = tc::sdesc_sw128(sb + OFF_K, 16, 1024);
+            const uint64_t qb0 = tc::sdesc_sw128(sb + OFF_Q, 16, 1024);
+            const uint64_t pa0 = tc::sdesc_sw128(sb + OFF_K, kReg, 1024);
+            const uint64_t pb0 = tc::sdesc_sw128(sb + OFF_P, kReg, 1024);
             bool ok = true;
-            for (int t = 0; t < T && ok; t++) {
-                if (t > 0 && !mbar_wait(bar(BAR_SFREE), (uint32_t)((t - 1) & 1))) {
+            int nq = 0, np = 0;                       // next S tile, next PV tile
+            uint64_t idle0 = global_ns();
+            while (np < T) {
+                bool did = false;
+                if (nq < T && nq <= np + 1) {
+                    const int sidx = nq & 1;
+                    if ((nq < 2 || mbar_test(bar(BAR_SFREE + sidx), (uint32_t)(((nq - 2) >> 1) & 1))) &&
+                        mbar_test(bar(BAR_KFULL + sidx), (uint32_t)((nq >> 1) & 1))) {
+                        tc::fence_after_sync();
+                        // descriptors advance by adding (byte offset >> 4) to the address field
+                        const uint64_t a0 = qa0 + (uint64_t)((sidx * kStage) >> 4);
+                        const uint32_t dS = tmem + TM_S + 64 * sidx;
+#pragma unroll
+                        for (int j = 0; j < kTcD / 16; j++) {
+                            const uint64_t off = (uint64_t)(((j >> 2) * kReg + (j & 3) * 32) >> 4);
+                            tc::mma_ss(dS, a0 + off, qb0 + off, id_qk, j != 0);
+                        }
+                        tc::mma_commit(bar(BAR_SFULL + sidx));
+                        nq++;
+                        did = true;
+                    }
+                }
+                if (np < nq) {
+                    const int sidx = np & 1;
+                    if (mbar_test(bar(BAR_PFULL + sidx), (uint32_t)((np >> 1) & 1))) {
+                        tc::fence_after_sync();
+                        const uint64_t a0 = pa0 + (uint64_t)((sidx * kStage) >> 4);
+                        const uint64_t b0 = pb0 + (uint64_t)((sidx * kReg) >> 4);
+#pragma unroll
+                        for (int m = 0; m < 4; m++)
+#pragma unroll
+                            for (int k4 = 0; k4 < kTcKeys / 16; k4++)
+                                tc::mma_ss(tmem + TM_O + 64 * m, a0 + (uint64_t)((2 * m * kReg + k4 * 2048) >> 4),
+                                           b0 + (uint64_t)((k4 * 2048) >> 4), id_pv, np > 0 || k4 > 0);
+                        tc::mma_commit(bar(BAR_KFREE + sidx));
+                        np++;
+                        did = true;
+                    }
+                }
+                if (did) {
+                    idle0 = global_ns();
+                } else if (global_ns() - idle0 > kWaitLimitNs) {
                     ok = false;
                     break;
-                }
-                for (int r = 0; r < kRegions && ok; r++) {
-                    if (!mbar_wait(bar(BAR_KFULL + r), (uint32_t)(t & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int ks4 = 0; ks4 < 4; ks4++) {
-                        const uint64_t a = tc::sdesc_sw128(sb + OFF_K + r * kRegK + ks4 * 32, 16, 1024);
-                        const uint64_t b = tc::sdesc_sw128(sb + OFF_Q + r * kRegQ + ks4 * 32, 16, 1024);
-                        tc::mma_ss(tmem + TM_S, a, b, id_qk, (r | ks4) != 0);
-                    }
-                }
-                if (!ok) break;
-                tc::mma_commit(bar(BAR_SFULL));
-                if (!mbar_wait(bar(BAR_PFULL), (uint32_t)(t & 1))) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-#pragma unroll 1
-                for (int m = 0; m < 4; m++) {
-#pragma unroll
-                    for (int k8 = 0; k8 < 8; k8++) {
-                        const uint64_t a = tc::sdesc_sw128(sb + OFF_K + 2 * m * kRegK + k8 * 2048, kRegK, 1024);
-                        const uint64_t b = tc::sdesc_sw128(sb + OFF_P + k8 * 2048, kRegK, 1024);
-                        tc::mma_ss(tmem + TM_O + 64 * m, a, b, id_pv, t > 0 || k8 > 0);
-                    }
-                    tc::mma_commit(bar(BAR_KFREE + m));
                 }
             }
             if (!ok) set_error(err, CSA_ERR_TIMEOUT);
             // every issued product completes before the CTA ends
             tc::mma_commit(bar(BAR_OFULL));
             if (!mbar_wait(bar(BAR_OFULL), 0)) set_error(err, CSA_ERR_TIMEOUT);
-            s_flag[2] = ok ? 1 : 0;
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax (128 threads)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        uint8_t *sP = sm + OFF_P;
+        const int hh = lane >> 4;                 // head half: heads 32 hh .. 32 hh + 31
+        const int key = 16 * warp + (lane & 15);  // key of the tile this thread takes
         bool ok = true;
-        for (int t = 0; t < T; t++) {
-            if (tid == 0) s_flag[0] = mbar_wait(bar(BAR_SFULL), (uint32_t)(t & 1)) ? 1 : 0;
+        // tid 0 waits on `b` with `parity`, then every softmax thread learns the outcome
+        auto wait_all = [&](int b, uint32_t parity) -> bool {
+            if (tid == 0) s_flag[0] = mbar_wait(bar(b), parity) ? 1 : 0;
             tc::named_bar(1, 128);
-            if (!s_flag[0]) {
+            const bool r = s_flag[0] != 0;
+            tc::named_bar(1, 128);
+            return r;
+        };
+        for (int t = 0; t < T; t++) {
+            const int sidx = t & 1;
+            if (!wait_all(BAR_SFULL + sidx, (uint32_t)((t >> 1) & 1))) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            float s[64];
-            tc::tmem_ld32(tmem + lane_base + TM_S, s);
-            tc::tmem_ld32(tmem + lane_base + TM_S + 32, s + 32);
+            float v[64];
+            tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sidx, v);
+            tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sidx + 32, v + 32);
             tc::tmem_wait_ld();
             tc::fence_before_sync();
-            mbar_arrive(bar(BAR_SFREE));
-
-            const int slot = t * kTcKeys + tid;
+            mbar_arrive(bar(BAR_SFREE + sidx));
+            // lanes 0-15 hold the tile's rows: hand heads 32-63 to lanes 16-31
+            float s[32];
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                const float other = __shfl_xor_sync(0xffffffffu, v[32 + j], 16);
+                s[j] = hh ? other : v[j];
+            }
+            const int slot = t * kTcKeys + key;
             bool valid = slot < ks.n_keys;
             if (GATHER && valid && slot < ks.n_main) {
                 const int e = ks.idx[slot];
                 valid = e >= 0 && (int64_t)e < ks.n_vis;
             }
 #pragma unroll
-            for (int h = 0; h < 64; h++) s[h] = valid ? s[h] * scale_log2 : -INFINITY;
+            for (int j = 0; j < 32; j++) s[j] = valid ? s[j] * scale_log2 : -INFINITY;
             float r0, r1;
-            warp_reduce64<true>(s, r0, r1);
-            s_rmax[warp * 64 + 2 * lane] = r0;
-            s_rmax[warp * 64 + 2 * lane + 1] = r1;
+            halfwarp_reduce32<true>(s, r0, r1);
+            const int h2 = 32 * hh + 2 * (lane & 15);
+            s_rmax[warp * 64 + h2] = r0;
+            s_rmax[warp * 64 + h2 + 1] = r1;
             if (tid == 0) s_flag[1] = 0;
             tc::named_bar(1, 128);
             if (tid < kTcHeads) {
@@ -342,44 +369,49 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
                 s_al[tid] = alpha;
             }
             tc::named_bar(1, 128);
-            if (s_flag[1]) {
-                // O^T columns of the raised heads scale by alpha (the previous
-                // tile's products are complete: S^T of this tile was committed after them)
+            const bool rescale = s_flag[1] != 0;
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                const float mn = s_mn[32 * hh + j];
+                s[j] = (mn == -INFINITY) ? 0.f : fast_exp2(s[j] - mn);
+            }
+            // P V of the previous tile must be done: it read this P stage two
+            // tiles ago and the O^T columns are rescaled below
+            if (t >= 1 && !wait_all(BAR_KFREE + ((t - 1) & 1), (uint32_t)(((t - 1) >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            {
+                uint8_t *prow = sm + OFF_P + sidx * kReg + key * 128;
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const int ch = 4 * hh + c;
+                    uint4 w;
+                    w.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
+                    w.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
+                    w.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
+                    w.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
+                    *reinterpret_cast<uint4 *>(prow + ((ch ^ (key & 7)) << 4)) = w;
+                }
+            }
+            if (rescale) {
+                tc::fence_after_sync();
 #pragma unroll 1
                 for (int c = 0; c < 8; c++) {
-                    float v[32];
+                    float o[32];
                     const uint32_t ta = tmem + lane_base + TM_O + 32 * c;
-                    tc::tmem_ld32(ta, v);
+                    tc::tmem_ld32(ta, o);
                     tc::tmem_wait_ld();
                     const float *al = s_al + 32 * (c & 1);
 #pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] *= al[j];
-                    tc::tmem_st32(ta, v);
+                    for (int j = 0; j < 32; j++) o[j] *= al[j];
+                    tc::tmem_st32(ta, o);
                 }
                 tc::tmem_wait_st();
             }
-            // P^T[head][key] in bf16 into the swizzled B tile; row sums
-#pragma unroll
-            for (int h = 0; h < 64; h++) {
-                const float mn = s_mn[h];
-                s[h] = (mn == -INFINITY) ? 0.f : fast_exp2(s[h] - mn);
-            }
-            {
-                // this key's 64 heads form one 128-byte swizzled row of the P tile
-                uint8_t *prow = sP + tid * 128;
-#pragma unroll
-                for (int c = 0; c < 8; c++) {
-                    uint4 v;
-                    v.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
-                    v.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
-                    v.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
-                    v.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
-                    *reinterpret_cast<uint4 *>(prow + ((c ^ (tid & 7)) << 4)) = v;
-                }
-            }
-            warp_reduce64<false>(s, r0, r1);
-            s_rsum[warp * 64 + 2 * lane] = r0;
-            s_rsum[warp * 64 + 2 * lane + 1] = r1;
+            halfwarp_reduce32<false>(s, r0, r1);
+            s_rsum[warp * 64 + h2] = r0;
+            s_rsum[warp * 64 + h2 + 1] = r1;
             tc::fence_proxy_async();
             tc::fence_before_sync();
             tc::named_bar(1, 128);
@@ -388,18 +420,17 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
                 s_l[tid] = s_l[tid] * s_al[tid] + ls;
                 s_m[tid] = s_mn[tid];
             }
-            mbar_arrive(bar(BAR_PFULL));
+            mbar_arrive(bar(BAR_PFULL + sidx));
         }
         // epilogue: O^T / l -> out[head][d] (bf16), lse
-        if (tid == 0) s_flag[0] = ok ? (mbar_wait(bar(BAR_OFULL), 0) ? 1 : 0) : 0;
-        tc::named_bar(1, 128);
-        if (s_flag[0]) {
+        const bool done = ok && wait_all(BAR_OFULL, 0);
+        if (done) {
             tc::fence_after_sync();
             uint16_t *orow = out + (qi * H + (int64_t)hg * kTcHeads) * kTcD;
 #pragma unroll 1
             for (int c = 0; c < 8; c++) {
-                float v[32];
-                tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, v);
+                float o[32];
+                tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
                 tc::tmem_wait_ld();
                 const int d = 128 * (c >> 1) + tid;
                 const int h0 = 32 * (c & 1);
@@ -407,7 +438,7 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
                 for (int j = 0; j < 32; j++) {
                     const float l = s_l[h0 + j];
                     const float inv = l > 0.f ? 1.f / l : 0.f;
-                    orow[(int64_t)(h0 + j) * kTcD + d] = (uint16_t)f32_to_bf16_bits(v[j] * inv);
+                    orow[(int64_t)(h0 + j) * kTcD + d] = (uint16_t)f32_to_bf16_bits(o[j] * inv);
                 }
             }
             if (lse && tid < kTcHeads)

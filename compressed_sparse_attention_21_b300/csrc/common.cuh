@@ -197,6 +197,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
                  : "memory");
     return ok != 0;
 }
+// Non-blocking test of the phase with `parity`.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
 // Wait for the phase with `parity` to complete; gives up (returns false)
 // after kWaitLimitNs of wall time.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
