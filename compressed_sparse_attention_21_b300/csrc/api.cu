@@ -349,8 +349,8 @@ csa_status_t lightning_index_topk_static(const csa_layout *layout, const csa_bf1
     CSA_TRY(check_index(layout, q_idx, k_idx, n_heads_idx, d_idx, ratio, top_k, idx_out, score_out));
     IndexArgs a = index_args(layout, q_idx, k_idx, n_heads_idx, d_idx, ratio, top_k, idx_out, score_out, nullptr, 0,
                              nullptr);
-    // the whole problem must fit the library-owned scratch (checked before any CUDA call)
-    if (index_workspace_bytes(a) > kIndexStaticScratchBytes) return CSA_ERR_WORKSPACE;
+    // the problem must fit the library-owned scratch (checked before any CUDA call)
+    if (index_static_need_bytes(a) > kIndexStaticScratchBytes) return CSA_ERR_WORKSPACE;
     int *err = nullptr;
     CSA_TRY(error_word(&err));
     void *scratch = nullptr;

@@ -227,6 +227,73 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
+// Warp 0: in a 256-bin histogram walked from the top bin down, find the bin
+// that holds the `remaining`-th largest element; report it and the count of
+// elements in higher bins.
+__device__ __forceinline__ void find_digit_256(const uint32_t *hist, uint32_t remaining, uint32_t *out_digit,
+                                               uint32_t *out_above)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t c[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        c[i] = hist[255 - 8 * lane - i];
+        sum += c[i];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const uint32_t excl = incl - sum;
+    if (excl < remaining && remaining <= incl) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            if (acc + c[i] >= remaining) {
+                *out_digit = 255 - 8 * lane - i;
+                *out_above = acc;
+                break;
+            }
+            acc += c[i];
+        }
+    }
+}
+
+// CTA-wide exclusive scan of one value per thread; returns the prefix and
+// the total.  s_w holds 2 * NT/32 + 1 words.
+template <int NT>
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *s_w, uint32_t &total)
+{
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) s_w[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t t = lane < NW ? s_w[lane] : 0u;
+        uint32_t ti = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o) ti += u;
+        }
+        if (lane < NW) s_w[NW + lane] = ti - t;
+        if (lane == 31) s_w[2 * NW] = ti;
+    }
+    __syncthreads();
+    total = s_w[2 * NW];
+    const uint32_t r = s_w[NW + warp] + incl - v;
+    __syncthreads();   // s_w may be reused right away
+    return r;
+}
+
 // Programmatic dependent launch.  griddep_wait() blocks until every grid this
 // one depends on has completed and its memory is visible (a no-op for a
 // launch without a programmatic dependency); griddep_launch() lets the grids

@@ -1,0 +1,496 @@
+// Lightning indexer + top-k for prefill-sized batches ("DeepSeek-V4 core
+// architecture", §2.2 CSA step 2: a light scorer rates each query against
+// every compressed entry and only the top-k entries are kept).
+//
+// The per-query scan re-reads a sequence's indexer keys once per query; here
+// a persistent CTA takes 16 consecutive queries of a sequence at a time and
+// streams the sequence's keys through shared memory once for all 16:
+//
+//  1. Scores on the tensor cores.  The head-summed query (fp32) is split into
+//     three bf16 terms (hi + mid + lo, exact to 2^-27 relative) and
+//     s = sum_terms term . k is accumulated in fp32 by mma.m16n8k16 (16
+//     queries x 8 entries per product, products exact).  This is the fp32
+//     score of the definition up to fp32 rounding order.
+//  2. A threshold per query from 256 evenly spaced entries: the sampled score
+//     expected to have about 2k entries above it.  While the keys stream by,
+//     only entries at or above the threshold are kept as candidates.
+//  3. Exact selection among the candidates: the k-th largest key by a 4 x 8-bit
+//     radix select, then every kept entry finds its output slot from prefix
+//     counts over bitmaps of the entries above and equal to it (index order,
+//     ties to the lower index).
+//  A query whose candidates turn out fewer than min(k, n) or more than the
+//  buffer holds (a sample that misjudged the distribution, many equal
+//  scores) is selected exactly from all of its scores instead.  The result
+//  never depends on the sample; only the amount of work does.
+#include "common.cuh"
+#include "launch.h"
+
+namespace csa {
+
+namespace {
+
+constexpr int kBQ = 16;              // queries per block (M of one m16n8k16 tile)
+constexpr int kBT = 512;             // threads: 16 warps x 16 entries = one chunk
+constexpr int kBRows = 256;          // entries per chunk
+constexpr int kBSample = 256;        // sampled entries for the threshold
+constexpr int kBCap = 4096;          // candidates kept per query
+constexpr int kBMaxN = 32768;        // longest row: bitmaps of 1024 words
+constexpr int kBMaxK = 1024;
+constexpr int kBWords = kBMaxN / 32;
+constexpr int kBFallKeys = kBMaxN / kBT;   // keys per thread of the exact fallback
+constexpr size_t kBSlotBytes = (size_t)kBQ * kBCap * 8;   // candidate slot of one persistent CTA
+
+template <int DI>
+struct BCfg {
+    static constexpr int RB = 2 * DI;            // bytes of a key row
+    static constexpr int PRB = RB + 16;          // padded row stride: ldmatrix without bank conflicts
+    static constexpr int CPR = RB / 16;          // 16-byte chunks per row
+    static constexpr int KS = DI / 16;           // k-steps of 16
+    static constexpr uint32_t buf_bytes = kBRows * PRB;
+    // shared-memory layout (bytes)
+    static constexpr uint32_t off_buf = 0;                                   // 2 chunk buffers
+    static constexpr uint32_t off_qs = off_buf + 2 * buf_bytes;              // [16][DI] fp32 head sums
+    static constexpr uint32_t off_skey = off_qs + kBQ * DI * 4;              // [16][256] sampled keys
+    static constexpr uint32_t off_gt = off_skey + kBQ * kBSample * 4;        // bitmaps and their prefixes
+    static constexpr uint32_t off_eq = off_gt + kBWords * 4;
+    static constexpr uint32_t off_pre = off_eq + kBWords * 4;                // packed (gt << 16 | eq) prefix
+    static constexpr uint32_t off_end = off_pre + kBWords * 4;
+    static constexpr size_t smem = off_end;
+};
+
+struct BlockQ {           // per-query record of the current block
+    int b;                // sequence
+    int n;                // visible entries
+    int64_t e0;           // first entry row of the sequence
+    int ok;               // layout consistent
+};
+
+// m16n8k16 bf16 fragments of the 16 x DI head-summed queries, split in three
+// bf16 terms: a[ks][term][4].
+template <int DI>
+__device__ __forceinline__ void load_a_frags(const float *qs, uint32_t (&a)[DI / 16][3][4])
+{
+    const int lane = threadIdx.x & 31, g = lane >> 2, c4 = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < DI / 16; ks++) {
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const int row = g + (r & 1) * 8;
+            const int col = ks * 16 + 2 * c4 + (r >> 1) * 8;
+            float x0 = qs[row * DI + col], x1 = qs[row * DI + col + 1];
+#pragma unroll
+            for (int term = 0; term < 3; term++) {
+                const uint32_t p = pack_bf16x2(x0, x1);
+                a[ks][term][r] = p;
+                x0 -= bf16_lo(p);
+                x1 -= bf16_hi(p);
+            }
+        }
+    }
+}
+
+// Scores of the 16 queries against the 16 entries this warp owns in a chunk
+// buffer (rows 16 w .. 16 w + 15): s[tile][4] in C-fragment order.
+template <int DI>
+__device__ __forceinline__ void warp_scores(uint32_t buf, const uint32_t (&a)[DI / 16][3][4], float (&s)[2][4])
+{
+    using C = BCfg<DI>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int t = 0; t < 2; t++) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+    const int row = warp * 16 + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+    for (int ks = 0; ks < DI / 16; ks++) {
+        uint32_t b0, b1, b2, b3;
+        const int ch = ks * 2 + ((lane >> 3) & 1);
+        ldmatrix_x4(buf + row * C::PRB + ch * 16, b0, b1, b2, b3);
+#pragma unroll
+        for (int term = 0; term < 3; term++) {
+            mma_bf16_16816(s[0], a[ks][term], b0, b1);
+            mma_bf16_16816(s[1], a[ks][term], b2, b3);
+        }
+    }
+}
+
+// Copy key rows into a padded chunk buffer; row r of the buffer takes entry
+// row src_row(r) of the sequence, or zeros when src_row(r) < 0.
+template <int DI, typename RowOf>
+__device__ __forceinline__ void load_rows(uint32_t buf, const uint16_t *kseq, RowOf src_row, const uint16_t *safe)
+{
+    using C = BCfg<DI>;
+    for (int i = threadIdx.x; i < kBRows * C::CPR; i += kBT) {
+        const int r = i / C::CPR, c = i % C::CPR;
+        const int64_t e = src_row(r);
+        cp_async_16(buf + r * C::PRB + c * 16, e >= 0 ? (const void *)(kseq + e * DI + c * 8) : (const void *)safe,
+                    e >= 0 ? 16 : 0);
+    }
+}
+
+// Exact selection of one query's top-k among the (key, entry) pairs that
+// `src` hands out: src(i, key, ent) for i < NPT gives this thread's i-th pair
+// (false when there is none).  Writes the row of idx/score in index order.
+template <int NPT, typename Src>
+__device__ void select_write(Src src, int n, int top_k, uint8_t *sm_gt, uint8_t *sm_eq, uint8_t *sm_pre,
+                             uint32_t *s_hist, uint32_t *s_w, uint32_t *s_dig, int32_t *idx_row, float *sc_row)
+{
+    const int tid = threadIdx.x;
+    uint32_t *gt = reinterpret_cast<uint32_t *>(sm_gt);
+    uint32_t *eq = reinterpret_cast<uint32_t *>(sm_eq);
+    uint32_t *pre = reinterpret_cast<uint32_t *>(sm_pre);
+    const uint32_t k_eff = (uint32_t)(n < top_k ? n : top_k);
+    // k-th largest key: four 8-bit radix levels
+    uint32_t prefix = 0, pmask = 0, remaining = k_eff;
+    for (int sh = 24; sh >= 0 && k_eff > 0; sh -= 8) {
+        for (int i = tid; i < 256; i += kBT) s_hist[i] = 0;
+        __syncthreads();
+#pragma unroll 1
+        for (int i = 0; i < NPT; i++) {
+            uint32_t key;
+            int32_t ent;
+            if (src(i, key, ent) && (key & pmask) == prefix) atomicAdd(&s_hist[(key >> sh) & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid < 32) find_digit_256(s_hist, remaining, &s_dig[0], &s_dig[1]);
+        __syncthreads();
+        remaining -= s_dig[1];
+        prefix |= s_dig[0] << sh;
+        pmask |= 255u << sh;
+        __syncthreads();
+    }
+    const uint32_t kstar = prefix, need_eq = remaining;
+    // bitmaps of the entries above and equal to the k-th key
+    const int words = (n + 31) >> 5;
+    for (int i = tid; i < words; i += kBT) {
+        gt[i] = 0;
+        eq[i] = 0;
+    }
+    __syncthreads();
+    if (k_eff > 0) {
+#pragma unroll 1
+        for (int i = 0; i < NPT; i++) {
+            uint32_t key;
+            int32_t ent;
+            if (!src(i, key, ent)) continue;
+            if (key > kstar) atomicOr(&gt[ent >> 5], 1u << (ent & 31));
+            else if (key == kstar) atomicOr(&eq[ent >> 5], 1u << (ent & 31));
+        }
+    }
+    __syncthreads();
+    // exclusive prefix of (popc gt << 16 | popc eq) over the words, two words per thread
+    {
+        const int w0 = 2 * tid, w1 = 2 * tid + 1;
+        const uint32_t v0 = w0 < words ? ((uint32_t)__popc(gt[w0]) << 16) | (uint32_t)__popc(eq[w0]) : 0u;
+        const uint32_t v1 = w1 < words ? ((uint32_t)__popc(gt[w1]) << 16) | (uint32_t)__popc(eq[w1]) : 0u;
+        uint32_t tot;
+        const uint32_t ex = block_scan<kBT>(v0 + v1, s_w, tot);
+        if (w0 < words) pre[w0] = ex;
+        if (w1 < words) pre[w1] = ex + v0;
+    }
+    __syncthreads();
+    if (k_eff > 0) {
+#pragma unroll 1
+        for (int i = 0; i < NPT; i++) {
+            uint32_t key;
+            int32_t e;
+            if (!src(i, key, e)) continue;
+            const int w = e >> 5;
+            const uint32_t below = (1u << (e & 31)) - 1u;
+            const uint32_t gt_before = (pre[w] >> 16) + (uint32_t)__popc(gt[w] & below);
+            const uint32_t eq_before = (pre[w] & 0xffffu) + (uint32_t)__popc(eq[w] & below);
+            bool take = false;
+            uint32_t pos = 0;
+            if (key > kstar) {
+                take = true;
+                pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
+            } else if (key == kstar && eq_before < need_eq) {
+                take = true;
+                pos = gt_before + eq_before;
+            }
+            if (take && pos < (uint32_t)top_k) {
+                idx_row[pos] = e;
+                if (sc_row) sc_row[pos] = key_score(key);
+            }
+        }
+    }
+    for (int i = (int)k_eff + tid; i < top_k; i += kBT) {
+        idx_row[i] = -1;
+        if (sc_row) sc_row[i] = -INFINITY;
+    }
+    __syncthreads();
+}
+
+template <int DI>
+__global__ void __launch_bounds__(kBT, 1)
+index_block_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                   const int64_t *__restrict__ cu_csa, int64_t total_q, const uint16_t *__restrict__ qI,
+                   const uint16_t *__restrict__ kI, int HI, int ratio, int top_k, uint64_t *__restrict__ cand_ws,
+                   int32_t *__restrict__ idx_out, float *__restrict__ score_out, int *err)
+{
+    using C = BCfg<DI>;
+    extern __shared__ __align__(128) uint8_t sm[];
+    __shared__ BlockQ s_q[kBQ];
+    __shared__ uint32_t s_tau[kBQ], s_cnt[kBQ];
+    __shared__ uint32_t s_hist[256];
+    __shared__ uint32_t s_w[2 * (kBT / 32) + 1];
+    __shared__ uint32_t s_dig[2];
+    __shared__ int s_need_sample;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, c4 = lane & 3;
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t buf0 = sbase + C::off_buf, buf1 = buf0 + C::buf_bytes;
+    float *qs = reinterpret_cast<float *>(sm + C::off_qs);
+    uint32_t *skey = reinterpret_cast<uint32_t *>(sm + C::off_skey);
+    uint64_t *cand = cand_ws + (int64_t)blockIdx.x * kBQ * kBCap;
+    const int64_t nblocks = (total_q + kBQ - 1) / kBQ;
+
+    for (int64_t blk = blockIdx.x; blk < nblocks; blk += gridDim.x) {
+        const int64_t q0 = blk * kBQ;
+        const int nqb = (int)(total_q - q0 < kBQ ? total_q - q0 : kBQ);
+        // ---- the block's queries ----
+        if (warp < kBQ) {
+            const int64_t qi = q0 + (warp < nqb ? warp : 0);
+            const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);
+            if (lane == 0) {
+                BlockQ r;
+                r.b = p.b;
+                r.n = (int)((p.t + 1) / ratio);
+                r.e0 = p.e0;
+                r.ok = warp < nqb && p.ne == p.L / ratio && p.t >= 0 && p.t < p.L && r.n <= kBMaxN;
+                s_q[warp] = r;
+            }
+        }
+        for (int i = tid; i < kBQ * DI; i += kBT) {
+            const int qq = i / DI, d = i % DI;
+            float acc = 0.f;
+            if (qq < nqb)
+                for (int h = 0; h < HI; h++) acc += bf16_lo(__ldg(qI + ((q0 + qq) * HI + h) * DI + d));
+            qs[i] = acc;
+        }
+        __syncthreads();
+        uint32_t afr[DI / 16][3][4];
+        load_a_frags<DI>(qs, afr);
+
+        // ---- one pass per sequence present in the block (nearly always one) ----
+        for (int ga = 0; ga < nqb;) {
+            int gz = ga + 1;
+            while (gz < nqb && s_q[gz].b == s_q[ga].b) gz++;
+            int n_max = 0;
+            for (int i = ga; i < gz; i++)
+                if (s_q[i].ok && s_q[i].n > n_max) n_max = s_q[i].n;
+            const int64_t e0 = s_q[ga].e0;
+            const uint16_t *kseq = kI + e0 * DI;
+            // thresholds: keep everything when the row fits the candidate buffer
+            if (tid < kBQ) {
+                s_tau[tid] = 0u;
+                s_cnt[tid] = 0u;
+            }
+            if (tid == 0) {
+                int need = 0;
+                for (int i = ga; i < gz; i++) need |= (s_q[i].ok && s_q[i].n > kBCap);
+                s_need_sample = need;
+            }
+            __syncthreads();
+            if (s_need_sample) {
+                // sampled rows j_s = s * n_max / 256 of the sequence
+                load_rows<DI>(buf0, kseq, [&](int r) -> int64_t { return (int64_t)r * n_max / kBSample; }, kI);
+                cp_async_commit();
+                cp_async_wait<0>();
+                __syncthreads();
+                float sc[2][4];
+                warp_scores<DI>(buf0, afr, sc);
+#pragma unroll
+                for (int t = 0; t < 2; t++)
+#pragma unroll
+                    for (int r = 0; r < 4; r++) {
+                        const int qq = g + (r >> 1) * 8;
+                        const int s_i = warp * 16 + t * 8 + 2 * c4 + (r & 1);
+                        const int64_t j = (int64_t)s_i * n_max / kBSample;
+                        const bool v = qq >= ga && qq < gz && s_q[qq].ok && j < s_q[qq].n;
+                        skey[qq * kBSample + s_i] = v ? score_key(sc[t][r]) : 0u;
+                    }
+                __syncthreads();
+                // rank select: 32 threads per query, 8 samples each
+                {
+                    const int qq = tid >> 5;
+                    const BlockQ &Q = s_q[qq];
+                    if (qq >= ga && qq < gz && Q.ok && Q.n > kBCap) {
+                        int m = (int)(((int64_t)kBSample * 2 * top_k + Q.n - 1) / Q.n);
+                        if (m < 1) m = 1;
+                        if (m <= kBSample) {
+                            const uint32_t *kk = skey + qq * kBSample;
+                            for (int i = 0; i < 8; i++) {
+                                const int s_i = lane * 8 + i;
+                                const uint32_t mine = kk[s_i];
+                                int rank = 0;
+                                for (int o = 0; o < kBSample; o++) {
+                                    const uint32_t other = kk[o];
+                                    rank += (other > mine) || (other == mine && o < s_i);
+                                }
+                                if (rank == m - 1) s_tau[qq] = mine;
+                            }
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+            // ---- stream the keys, keep candidates ----
+            const int nchunks = (n_max + kBRows - 1) / kBRows;
+            if (nchunks > 0) {
+                load_rows<DI>(buf0, kseq, [&](int r) -> int64_t { return r < n_max ? r : -1; }, kI);
+                cp_async_commit();
+            }
+            for (int c = 0; c < nchunks; c++) {
+                const uint32_t cur = (c & 1) ? buf1 : buf0, nxt = (c & 1) ? buf0 : buf1;
+                if (c + 1 < nchunks) {
+                    const int base = (c + 1) * kBRows;
+                    load_rows<DI>(nxt, kseq, [&](int r) -> int64_t { return base + r < n_max ? base + r : -1; },
+                                  kI);
+                }
+                cp_async_commit();
+                cp_async_wait<1>();
+                __syncthreads();
+                float sc[2][4];
+                warp_scores<DI>(cur, afr, sc);
+#pragma unroll
+                for (int t = 0; t < 2; t++)
+#pragma unroll
+                    for (int r = 0; r < 4; r++) {
+                        const int qq = g + (r >> 1) * 8;
+                        const int e = c * kBRows + warp * 16 + t * 8 + 2 * c4 + (r & 1);
+                        if (qq < ga || qq >= gz || !s_q[qq].ok || e >= s_q[qq].n) continue;
+                        const uint32_t key = score_key(sc[t][r]);
+                        if (key >= s_tau[qq]) {
+                            const uint32_t pos = atomicAdd(&s_cnt[qq], 1u);
+                            if (pos < (uint32_t)kBCap) cand[qq * kBCap + pos] = ((uint64_t)key << 32) | (uint32_t)e;
+                        }
+                    }
+                __syncthreads();
+            }
+            cp_async_wait<0>();
+            __syncthreads();
+            // ---- exact selection, query by query ----
+            for (int qq = ga; qq < gz; qq++) {
+                const BlockQ Q = s_q[qq];
+                const int64_t qi = q0 + qq;
+                int32_t *idx_row = idx_out + qi * top_k;
+                float *sc_row = score_out ? score_out + qi * top_k : nullptr;
+                if (!Q.ok) {
+                    if (tid == 0) set_error(err, CSA_ERR_DEVICE);
+                    for (int i = tid; i < top_k; i += kBT) {
+                        idx_row[i] = -1;
+                        if (sc_row) sc_row[i] = -INFINITY;
+                    }
+                    continue;
+                }
+                const uint32_t cnt = s_cnt[qq];
+                const uint32_t k_eff = (uint32_t)(Q.n < top_k ? Q.n : top_k);
+                if (cnt >= k_eff && cnt <= (uint32_t)kBCap) {
+                    constexpr int KPT = kBCap / kBT;
+                    uint64_t cv[KPT];
+#pragma unroll
+                    for (int i = 0; i < KPT; i++) {
+                        const uint32_t c = tid + i * kBT;
+                        cv[i] = c < cnt ? __ldcg(cand + qq * kBCap + c) : ~0ull;
+                    }
+                    auto src = [&](int i, uint32_t &key, int32_t &ent) -> bool {
+                        uint64_t v = 0;
+#pragma unroll
+                        for (int j = 0; j < KPT; j++)
+                            if (j == i) v = cv[j];
+                        key = (uint32_t)(v >> 32);
+                        ent = (int32_t)(uint32_t)v;
+                        return v != ~0ull;
+                    };
+                    select_write<KPT>(src, Q.n, top_k, sm + C::off_gt, sm + C::off_eq, sm + C::off_pre, s_hist, s_w,
+                                      s_dig, idx_row, sc_row);
+                } else {
+                    // exact fallback: every score of this query, recomputed when needed
+                    const float *qv = qs + qq * DI;
+                    const int n = Q.n;
+                    auto src = [&](int i, uint32_t &key, int32_t &ent) -> bool {
+                        const int e = tid * kBFallKeys + i;
+                        ent = e;
+                        if (e >= n) return false;
+                        const uint16_t *kr = kseq + (int64_t)e * DI;
+                        float acc = 0.f;
+                        for (int d = 0; d < DI; d += 2) {
+                            const uint32_t w2 = __ldg(reinterpret_cast<const uint32_t *>(kr + d));
+                            acc = fmaf(qv[d], bf16_lo(w2), acc);
+                            acc = fmaf(qv[d + 1], bf16_hi(w2), acc);
+                        }
+                        key = score_key(acc);
+                        return true;
+                    };
+                    select_write<kBFallKeys>(src, n, top_k, sm + C::off_gt, sm + C::off_eq, sm + C::off_pre, s_hist,
+                                             s_w, s_dig, idx_row, sc_row);
+                }
+            }
+            ga = gz;
+            __syncthreads();
+        }
+        __syncthreads();
+    }
+}
+
+int g_sms_cache[64];
+
+int device_sms()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!g_sms_cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g_sms_cache[dev] = n;
+    }
+    return g_sms_cache[dev];
+}
+
+template <int DI>
+cudaError_t launch_block_t(const IndexArgs &a, cudaStream_t st)
+{
+    using C = BCfg<DI>;
+    const int64_t nblocks = (a.total_q + kBQ - 1) / kBQ;
+    const int64_t sms = device_sms();
+    // one candidate slot per CTA: as many persistent CTAs as the workspace holds
+    int64_t grid = nblocks < sms ? nblocks : sms;
+    const int64_t slots = (int64_t)(a.ws_bytes / kBSlotBytes);
+    if (grid > slots) grid = slots;
+    if (grid < 1) return cudaErrorInvalidValue;
+    return launch_kernel("index_block", index_block_kernel<DI>, dim3((unsigned)grid), dim3(kBT), C::smem, st, false, a.batch,
+                         a.cu_kv, a.cu_q, a.cu_csa, a.total_q, a.q_idx, a.k_idx, a.n_heads_idx, a.ratio, a.top_k,
+                         reinterpret_cast<uint64_t *>(a.ws), a.idx_out, a.score_out, a.err);
+}
+
+}  // namespace
+
+bool index_block_applicable(const IndexArgs &a)
+{
+    const int64_t max_n = a.max_kv_len / a.ratio;
+    return a.total_q >= 1024 && max_n <= kBMaxN && a.top_k <= kBMaxK &&
+           (a.d_idx == 32 || a.d_idx == 64 || a.d_idx == 128);
+}
+
+size_t index_block_ws_bytes(const IndexArgs &a)
+{
+    const int64_t nblocks = (a.total_q + kBQ - 1) / kBQ;
+    const int64_t sms = device_sms();
+    const int64_t grid = nblocks < sms ? nblocks : sms;
+    return (size_t)grid * kBSlotBytes;
+}
+
+size_t index_block_min_ws_bytes() { return kBSlotBytes; }
+
+cudaError_t launch_index_block(const IndexArgs &a, cudaStream_t st)
+{
+    if (a.total_q <= 0) return cudaSuccess;
+    switch (a.d_idx) {
+    case 32: return launch_block_t<32>(a, st);
+    case 64: return launch_block_t<64>(a, st);
+    case 128: return launch_block_t<128>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace csa

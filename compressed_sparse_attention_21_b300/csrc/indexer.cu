@@ -131,73 +131,6 @@ __device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t bin, bool vali
     if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(hist + bin, (uint32_t)__popc(peers));
 }
 
-// Warp 0: in a 256-bin histogram walked from the top bin down, find the bin
-// that holds the `remaining`-th largest element; report it and the count of
-// elements in higher bins.
-__device__ __forceinline__ void find_digit_256(const uint32_t *hist, uint32_t remaining, uint32_t *out_digit,
-                                               uint32_t *out_above)
-{
-    const int lane = threadIdx.x & 31;
-    uint32_t c[8], sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-        c[i] = hist[255 - 8 * lane - i];
-        sum += c[i];
-    }
-    uint32_t incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    const uint32_t excl = incl - sum;
-    if (excl < remaining && remaining <= incl) {
-        uint32_t acc = excl;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            if (acc + c[i] >= remaining) {
-                *out_digit = 255 - 8 * lane - i;
-                *out_above = acc;
-                break;
-            }
-            acc += c[i];
-        }
-    }
-}
-
-// CTA-wide exclusive scan of one value per thread; returns the prefix and
-// the total.  s_w holds 2 * NT/32 + 1 words.
-template <int NT>
-__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *s_w, uint32_t &total)
-{
-    constexpr int NW = NT / 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-    }
-    if (lane == 31) s_w[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const uint32_t t = lane < NW ? s_w[lane] : 0u;
-        uint32_t ti = t;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t u = __shfl_up_sync(0xffffffffu, ti, o);
-            if (lane >= o) ti += u;
-        }
-        if (lane < NW) s_w[NW + lane] = ti - t;
-        if (lane == 31) s_w[2 * NW] = ti;
-    }
-    __syncthreads();
-    total = s_w[2 * NW];
-    const uint32_t r = s_w[NW + warp] + incl - v;
-    __syncthreads();   // s_w may be reused right away
-    return r;
-}
-
 __device__ __forceinline__ void write_row_padding(int32_t *idx_row, float *score_row_out, int from, int top_k)
 {
     for (int i = from + threadIdx.x; i < top_k; i += blockDim.x) {
@@ -839,6 +772,7 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
 {
     if (a.total_q <= 0) return cudaSuccess;
     const int64_t max_n = a.max_kv_len / a.ratio;
+    if (index_block_applicable(a)) return launch_index_block(a, st);
     if (use_cta_path(a)) {
         const int64_t nsm = max_n < 1 ? 1 : max_n;
         const size_t smem = (size_t)nsm * 4;
@@ -900,7 +834,9 @@ bool index_supported(int n_heads_idx, int d_idx, int top_k)
 
 size_t index_workspace_bytes(const IndexArgs &a)
 {
-    if (a.total_q <= 0 || use_cta_path(a)) return 0;
+    if (a.total_q <= 0) return 0;
+    if (index_block_applicable(a)) return index_block_ws_bytes(a);
+    if (use_cta_path(a)) return 0;
     const int64_t max_n = a.max_kv_len / a.ratio;
     return (size_t)wsd_total_bytes(group_size(a), max_n < 1 ? 1 : max_n, a.top_k);
 }
@@ -951,9 +887,15 @@ cudaError_t index_static_scratch(void **ptr)
     return cudaSuccess;
 }
 
+size_t index_static_need_bytes(const IndexArgs &a)
+{
+    if (a.total_q > 0 && index_block_applicable(a)) return index_block_min_ws_bytes();
+    return index_workspace_bytes(a);
+}
+
 size_t index_static_zero_bytes(const IndexArgs &a)
 {
-    if (a.total_q <= 0 || use_cta_path(a)) return 0;
+    if (a.total_q <= 0 || index_block_applicable(a) || use_cta_path(a)) return 0;
     const int64_t gq = group_size(a);
     return (size_t)(align_up(gq * kHistBins * 4, 256) + align_up(gq * kMetaWords * 4, 256));
 }

@@ -89,6 +89,12 @@ struct IndexArgs {
     int *err;
 };
 bool index_supported(int n_heads_idx, int d_idx, int top_k);
+// prefill-sized batches (index_block.cu): tensor-core score tiles, sampled
+// threshold, exact selection among the candidates
+bool index_block_applicable(const IndexArgs &a);
+size_t index_block_ws_bytes(const IndexArgs &a);      // for a full grid of persistent CTAs
+size_t index_block_min_ws_bytes();                      // one CTA (the kernel fits its grid to ws_bytes)
+cudaError_t launch_index_block(const IndexArgs &a, cudaStream_t st);
 size_t index_workspace_bytes(const IndexArgs &a);
 cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t st);
 // Library-owned scratch of lightning_index_topk_static (see indexer.cu):
@@ -97,6 +103,7 @@ cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t st);
 constexpr size_t kIndexStaticScratchBytes = CSA_INDEX_STATIC_SCRATCH_BYTES;
 cudaError_t index_static_scratch(void **ptr);
 size_t index_static_zero_bytes(const IndexArgs &a);
+size_t index_static_need_bytes(const IndexArgs &a);   // smallest scratch the call can run in
 
 // ---- attention ----
 struct AttendArgs {

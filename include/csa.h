@@ -144,8 +144,9 @@ csa_status_t hca_compress(const csa_layout *layout, const csa_bf16 *kv, const fl
  *   (n_heads_idx, d_idx) in {(2,32), (4,64)} or any n_heads_idx <= 16 with
  *   d_idx in {32, 64, 128};  1 <= top_k <= 2048.
  * The full score matrix is never written out: decode-sized batches keep one
- * score row per query in the workspace; prefill-sized batches keep it in
- * shared memory.
+ * score row per query in the workspace; prefill-sized batches stream the
+ * keys once per 16 queries and keep only candidate entries (about 2k per
+ * query) in the workspace.
  * ------------------------------------------------------------------------- */
 csa_status_t lightning_index_topk(const csa_layout *layout, const csa_bf16 *q_idx,
                                   const csa_bf16 *k_idx, int n_heads_idx, int d_idx,
@@ -170,10 +171,12 @@ csa_status_t csa_index_workspace_size(const csa_layout *layout, int n_heads_idx,
  *
  *   - Arguments, layout and outputs are those of lightning_index_topk; the
  *     caller still provides q_idx, k_idx, idx_out and score_out.
- *   - A problem whose workspace (csa_index_workspace_size) exceeds
- *     CSA_INDEX_STATIC_SCRATCH_BYTES is rejected with CSA_ERR_WORKSPACE
- *     before anything is launched.  Prefill-sized batches (total_q >= 1024
- *     and at most 40960 entries per sequence) need no scratch at all.
+ *   - A decode-sized problem whose workspace (csa_index_workspace_size)
+ *     exceeds CSA_INDEX_STATIC_SCRATCH_BYTES is rejected with
+ *     CSA_ERR_WORKSPACE before anything is launched.  Prefill-sized batches
+ *     (total_q >= 1024, at most 32768 entries per sequence, top_k <= 1024)
+ *     run with as many candidate buffers as the scratch holds (fewer CTAs
+ *     than with a full workspace; the same results).
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current).  Make that first call before
  *     any stream capture.

@@ -134,9 +134,12 @@ def test_index_topk_cta_path(HI, dI, k):
     _check_index(p, idx, score)
 
 
-@pytest.mark.parametrize("queries", ["decode", "prefill"])
+@pytest.mark.parametrize("queries", ["decode", "prefill", "prefill_overflow"])
 def test_index_topk_all_ties_lowest_index_wins(queries):
-    lengths = [3000, 4100] if queries == "prefill" else [3000, 4100, 9000]
+    # prefill_overflow: rows longer than the prefill path's candidate buffer, all
+    # scores equal, so the exact fallback selection must run
+    lengths = {"prefill": [3000, 4100], "decode": [3000, 4100, 9000], "prefill_overflow": [17000]}[queries]
+    queries = "prefill" if queries.startswith("prefill") else queries
     p = problem(lengths, lengths if queries == "prefill" else [1] * len(lengths), HI=2, dI=32, k=64, seed=13)
     p["kI"] = torch.ones_like(p["kI"])      # every entry scores the same
     g = P.GpuProblem(p)
