@@ -305,7 +305,7 @@ index_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *_
             const bool valid = cg == 0 && j < n;
             const uint32_t key = score_key(acc);
             if (valid) keys[j] = key;
-            hist_add(s_hist, key >> (32 - kHistBits), valid);
+            if (valid) atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);   // few lanes per step: no aggregation
         }
     }
     __syncthreads();
@@ -610,7 +610,7 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
         const bool valid = cg == 0 && in;
         const uint32_t key = score_key(acc);
         if (valid) keys[row] = key;
-        hist_add(s_hist, key >> (32 - kHistBits), valid);
+        if (valid) atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);   // few lanes per step: no aggregation
     }
     __syncthreads();
     uint32_t *ghist = w.hist + qg * kHistBins;
