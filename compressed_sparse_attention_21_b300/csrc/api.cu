@@ -24,7 +24,7 @@ struct DeviceState {
     bool ready = false;
     int *err = nullptr;
     cudaStream_t aux = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr, cdone = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, sdone = nullptr;
     int num_sms = 0;
 };
 
@@ -48,7 +48,7 @@ csa_status_t device_state(DeviceState **out)
         if (cudaStreamCreateWithFlags(&s.aux, cudaStreamNonBlocking) != cudaSuccess) return CSA_ERR_CUDA;
         if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
         if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
-        if (cudaEventCreateWithFlags(&s.cdone, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
+        if (cudaEventCreateWithFlags(&s.sdone, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
         s.ready = true;
     }
     *out = &s;
@@ -138,6 +138,7 @@ IndexArgs index_args(const csa_layout *L, const csa_bf16 *q_idx, const csa_bf16 
     a.max_q_len = L->max_q_len;
     a.total_q = L->total_q;
     a.pdl = false;
+    a.scan_done = nullptr;
     a.cu_kv = L->cu_kv;
     a.cu_q = L->cu_q;
     a.cu_csa = L->cu_csa;
@@ -451,15 +452,18 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
     if (L->total_q == 0) return CSA_OK;
     char *ws = static_cast<char *>(p->ws);
 
-    // Streams.  The caller's stream `st` runs the CSA branch (indexer, top-k,
-    // sparse attention); the helper stream runs the compression and then the
-    // HCA branch.  The indexer reads no compressed entry, so it overlaps the
-    // compression; the sparse attention waits for both.
+    // Streams.  The caller's stream `st` runs the compression and the CSA
+    // branch (indexer, top-k, sparse attention) as one chain of dependent
+    // launches: the key scan reads no compressed entry and overlaps the
+    // compression, each later kernel starts while its predecessor finishes.
+    // The helper stream runs the HCA branch once the key scan (the part of
+    // the indexer that fills the GPU) is done, so it overlaps the top-k
+    // selection and the sparse attention.
     if (cudaEventRecord(ds->fork, st) != cudaSuccess) return CSA_ERR_CUDA;
     if (cudaStreamWaitEvent(ds->aux, ds->fork, 0) != cudaSuccess) return CSA_ERR_CUDA;
 
-    // a1 on the helper stream: compression of the blocks closed by this call's query positions
-    csa_status_t s_h = CSA_OK;
+    // a1: compression of the blocks closed by this call's query positions
+    csa_status_t s_c = CSA_OK;
     if (compress) {
         CompressArgs a;
         std::memset(&a, 0, sizeof a);
@@ -479,29 +483,35 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
             a.ratio_big = p->ratio_hca;
             a.cu_big = L->cu_hca;
             a.out_big = p->hca_cache;
-            s_h = from_cuda(launch_compress(a, ds->aux));
+            s_c = from_cuda(launch_compress(a, st));
         } else {
-            s_h = compress_impl(L, true, p->kv, p->gate, p->d, p->ratio_csa, p->csa_cache, ds->aux);
-            if (s_h == CSA_OK)
-                s_h = compress_impl(L, false, p->kv, p->gate, p->d, p->ratio_hca, p->hca_cache, ds->aux);
+            s_c = compress_impl(L, true, p->kv, p->gate, p->d, p->ratio_csa, p->csa_cache, st);
+            if (s_c == CSA_OK) s_c = compress_impl(L, false, p->kv, p->gate, p->d, p->ratio_hca, p->hca_cache, st);
         }
     }
-    const bool c1 = cudaEventRecord(ds->cdone, ds->aux) == cudaSuccess;
 
-    // a5 on the helper stream (may overlap the compression's tail; waits for it on the device)
+    // a2 + a3 (records sdone once every key is scored)
+    if (s_c == CSA_OK) {
+        IndexArgs ia = index_args(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k,
+                                  p->idx_out, p->score_out, w_idx ? ws : nullptr, w_idx, ds->err);
+        ia.scan_done = ds->sdone;
+        ia.pdl = compress;
+        s_c = from_cuda(launch_index_topk(ia, st));
+    } else {
+        cudaEventRecord(ds->sdone, st);
+    }
+
+    // a5 on the helper stream, behind the compression and the key scan
+    const bool c1 = cudaStreamWaitEvent(ds->aux, ds->sdone, 0) == cudaSuccess;
+    csa_status_t s_h = s_c;
     if (s_h == CSA_OK) {
         AttendArgs ha = attend_args(L, L->cu_hca, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d,
                                     p->ratio_hca, 0, p->scale, p->o_hca, p->lse_hca,
                                     w_hc ? ws + w_idx + w_sp : nullptr, w_hc, ds->err, ds->num_sms, ds->num_sms);
-        ha.pdl = compress;
         s_h = from_cuda(launch_attend(ha, ds->aux));
     }
 
-    // a2 + a3 on the caller's stream, then a4 once the compression is done
-    IndexArgs ia = index_args(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k, p->idx_out,
-                              p->score_out, w_idx ? ws : nullptr, w_idx, ds->err);
-    csa_status_t s_c = from_cuda(launch_index_topk(ia, st));
-    const bool c2 = cudaStreamWaitEvent(st, ds->cdone, 0) == cudaSuccess;
+    // a4, launched behind the selection
     if (s_c == CSA_OK) {
         AttendArgs sa = attend_args(L, L->cu_csa, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d,
                                     p->ratio_csa, p->top_k, p->scale, p->o_csa, p->lse_csa,
@@ -514,7 +524,7 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
     const bool j2 = cudaStreamWaitEvent(st, ds->join, 0) == cudaSuccess;
     if (s_c != CSA_OK) return s_c;
     if (s_h != CSA_OK) return s_h;
-    return (c1 && c2 && j1 && j2) ? CSA_OK : CSA_ERR_CUDA;
+    return (c1 && j1 && j2) ? CSA_OK : CSA_ERR_CUDA;
 }
 
 csa_status_t csa_workspace_init(void *ws, size_t ws_bytes, csa_stream_t stream)

@@ -579,7 +579,8 @@ bool attend_supported(int n_heads, int d)
 
 size_t attend_workspace_bytes(const AttendArgs &a)
 {
-    if (a.total_q <= 0 || attend_tc_applicable(a)) return 0;
+    if (a.total_q <= 0) return 0;
+    if (attend_tc_applicable(a)) return attend_tc_workspace_bytes(a);
     return ws_bytes_for(a, make_plan(a), nullptr);
 }
 

@@ -6,8 +6,10 @@
 // same as in attend.cu: selected (or all visible) entries plus the raw
 // tokens of the query's own open block.
 //
-// One CTA computes 64 heads of one query over all of its keys, in tiles of
-// 64 keys.  Keys are the M dimension of both products:
+// One CTA computes 64 heads of one query over one split of its keys (all of
+// them when there are at least as many 64-head units as SMs; decode splits a
+// query's keys over several CTAs), in tiles of 64 keys.  Keys are the M
+// dimension of both products:
 //     S^T[key, head] = K[key, :] . Q[head, :]       M = 64 keys,      N = 64, K = 512
 //     O^T[d, head]  += K[key, d]^T . P^T[key, head]  M = 4 x 128 d,   N = 64, K = 64
 // The shared-memory key tile is the K-major A operand of the first product
@@ -26,6 +28,10 @@
 // running maximum of a head is raised only when a tile exceeds it by more
 // than 2^8 (the accumulated O^T column and sum are then rescaled); the
 // result is exact either way because the sum uses the same maximum.
+// A split of a query that has several writes its unnormalised O (fp32,
+// [head][d], staged in the idle key stages and stored with one bulk copy)
+// and each head's (max, sum); attend_tc_merge_kernel, launched behind it,
+// combines the splits: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 // Every wait is bounded: one that runs out reports CSA_ERR_TIMEOUT.
 #include "common.cuh"
 #include "launch.h"
@@ -119,13 +125,23 @@ __device__ __forceinline__ const uint16_t *tc_key_row(const TcKeys &ks, int slot
     return nullptr;
 }
 
+// Keys of the query at `p` (selected or visible entries, then the raw tail).
+template <bool GATHER>
+__device__ __forceinline__ int tc_key_count(const QueryPos &p, int ratio, int top_k)
+{
+    const int64_t n_vis = (p.t + 1) / ratio;
+    const int n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
+    return n_main + (int)((p.t + 1) % ratio);
+}
+
 template <bool GATHER>
 __global__ void __launch_bounds__(kTcThreads, 1)
 attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
                  const int64_t *__restrict__ cu_ent, const uint16_t *__restrict__ q,
                  const uint16_t *__restrict__ entries, const uint16_t *__restrict__ kv,
                  const int32_t *__restrict__ idx, int H, int ratio, int top_k, float scale_log2, int max_kv_len,
-                 uint16_t *__restrict__ out, float *__restrict__ lse, int *err)
+                 int kps, int nsplit_max, uint16_t *__restrict__ out, float *__restrict__ lse,
+                 float *__restrict__ part_o, float2 *__restrict__ part_ml, int *err)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -133,7 +149,10 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
     uint8_t *sm = smem_raw + (sb - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t qi = blockIdx.x;
-    const int hg = blockIdx.y;
+    const int HG = H / kTcHeads;
+    const int hg = blockIdx.y % HG;
+    const int split = blockIdx.y / HG;
+    griddep_launch();   // the merge kernel may launch; it waits for this grid
 
     const QueryPos p = query_pos(cu_kv, cu_q, cu_ent, batch, qi);
     const int64_t n_vis = (p.t + 1) / ratio;
@@ -150,7 +169,11 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
     ks.n_vis = n_vis;
     ks.n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
     ks.n_keys = ks.n_main + r_tail;
-    const int T = (ks.n_keys + kTcKeys - 1) / kTcKeys;
+    const int nsplit = (ks.n_keys + kps - 1) / kps;
+    if (split >= nsplit) return;   // this query has fewer keys than the longest one
+    const int key0 = split * kps;
+    const int key1 = min(ks.n_keys, key0 + kps);
+    const int T = (key1 - key0 + kTcKeys - 1) / kTcKeys;
 
     const uint32_t bar0 = sb + OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -186,10 +209,13 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
 
     // the selection and the entries come from earlier kernels
     griddep_wait();
-    if (GATHER && ks.n_main <= kTcIdxCap) {
-        int32_t *s_idx = reinterpret_cast<int32_t *>(sm + OFF_IDX);
-        for (int i = tid; i < ks.n_main; i += kTcThreads) s_idx[i] = __ldg(ks.idx + i);
-        ks.idx = s_idx;
+    if (GATHER) {   // this split's part of the selection
+        const int i1 = min(key1, ks.n_main);
+        if (i1 - key0 <= kTcIdxCap) {
+            int32_t *s_idx = reinterpret_cast<int32_t *>(sm + OFF_IDX);
+            for (int i = key0 + tid; i < i1; i += kTcThreads) s_idx[i - key0] = __ldg(ks.idx + i);
+            ks.idx = s_idx - key0;
+        }
     }
     __syncthreads();
 
@@ -228,7 +254,7 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
             for (int i = 0; i < KPP; i++) {
                 const int k = pk0 + RSTEP * i;
                 if (k < kTcKeys) {
-                    const uint16_t *src = tc_key_row<GATHER>(ks, t * kTcKeys + k);
+                    const uint16_t *src = tc_key_row<GATHER>(ks, key0 + t * kTcKeys + k);
 #pragma unroll
                     for (int r = 0; r < kRegions; r++)
                         cp_async_16(stage + r * kReg + k * 128 + ((pc ^ (k & 7)) << 4),
@@ -341,7 +367,7 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
                 const float other = __shfl_xor_sync(0xffffffffu, v[32 + j], 16);
                 s[j] = hh ? other : v[j];
             }
-            const int slot = t * kTcKeys + key;
+            const int slot = key0 + t * kTcKeys + key;
             bool valid = slot < ks.n_keys;
             if (GATHER && valid && slot < ks.n_main) {
                 const int e = ks.idx[slot];
@@ -424,7 +450,31 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
         }
         // epilogue: O^T / l -> out[head][d] (bf16), lse
         const bool done = ok && wait_all(BAR_OFULL, 0);
-        if (done) {
+        if (done && nsplit > 1) {
+            // partial result: unnormalised O^T -> [head][d] fp32 in the key
+            // stages (every product is done with them), one bulk store
+            tc::fence_after_sync();
+            float *stg = reinterpret_cast<float *>(sm + OFF_K);
+#pragma unroll 1
+            for (int c = 0; c < 8; c++) {
+                float o[32];
+                tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
+                tc::tmem_wait_ld();
+                const int d = 128 * (c >> 1) + tid;
+                const int h0 = 32 * (c & 1);
+#pragma unroll
+                for (int j = 0; j < 32; j++) stg[(h0 + j) * kTcD + d] = o[j];
+            }
+            tc::fence_proxy_async();
+            tc::named_bar(1, 128);
+            const int64_t slot = ((qi * HG + hg) * nsplit_max + split) * kTcHeads;
+            if (tid == 0) {
+                bulk_s2g(part_o + slot * kTcD, sb + OFF_K, kTcHeads * kTcD * 4);
+                bulk_commit();
+                bulk_wait_all();
+            }
+            if (tid < kTcHeads) part_ml[slot + tid] = make_float2(s_m[tid], s_l[tid]);
+        } else if (done) {
             tc::fence_after_sync();
             uint16_t *orow = out + (qi * H + (int64_t)hg * kTcHeads) * kTcD;
 #pragma unroll 1
@@ -453,27 +503,144 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
     if (warp == 4) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// Combines the splits of the queries that have more than one.  CTA (i, h)
+// takes head h of query i; thread c holds columns 4 c .. 4 c + 3 and keeps
+// the loads of up to kMergeBatch splits in flight at once (the partial
+// results are read from L2, so the merge is bound by how many loads are in
+// flight).  One 4-warp CTA fits beside a resident attention CTA, so the
+// grid, launched early, waits on every SM.
+constexpr int kMergeThreads = kTcD / 4;
+constexpr int kMergeBatch = 8;
+
+template <bool GATHER>
+__global__ void __launch_bounds__(kMergeThreads, 8)
+attend_tc_merge_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                       const int64_t *__restrict__ cu_ent, int H, int ratio, int top_k, int kps, int nsplit_max,
+                       const float *__restrict__ part_o, const float2 *__restrict__ part_ml,
+                       uint16_t *__restrict__ out, float *__restrict__ lse)
+{
+    const int c = threadIdx.x;
+    const int64_t qi = blockIdx.x;
+    const int head = blockIdx.y;
+    const QueryPos p = query_pos(cu_kv, cu_q, cu_ent, batch, qi);
+    if (p.t < 0 || p.t >= p.L || p.ne != p.L / ratio) return;   // reported by the attention kernel
+    const int nsplit = (tc_key_count<GATHER>(p, ratio, top_k) + kps - 1) / kps;
+    if (nsplit <= 1) return;   // written by the attention kernel itself
+    griddep_wait();            // the partial results are complete
+    const int64_t base = (qi * (H / kTcHeads) + head / kTcHeads) * nsplit_max * kTcHeads + head % kTcHeads;
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; s++) M = fmaxf(M, __ldcg(part_ml + base + (int64_t)s * kTcHeads).x);
+    float Ls = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 *po = reinterpret_cast<const float4 *>(part_o + base * kTcD) + c;
+    for (int s0 = 0; s0 < nsplit; s0 += kMergeBatch) {
+        float4 v[kMergeBatch];
+        float2 ml[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; u++) {
+            if (s0 + u < nsplit) {
+                v[u] = __ldcg(po + (int64_t)(s0 + u) * kTcHeads * (kTcD / 4));
+                ml[u] = __ldcg(part_ml + base + (int64_t)(s0 + u) * kTcHeads);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; u++) {
+            if (s0 + u < nsplit) {
+                const float w = ml[u].x == -INFINITY ? 0.f : fast_exp2(ml[u].x - M);
+                Ls = fmaf(w, ml[u].y, Ls);
+                acc.x = fmaf(w, v[u].x, acc.x);
+                acc.y = fmaf(w, v[u].y, acc.y);
+                acc.z = fmaf(w, v[u].z, acc.z);
+                acc.w = fmaf(w, v[u].w, acc.w);
+            }
+        }
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2 *>(out + (qi * H + head) * (int64_t)kTcD + 4 * c) = pk;
+    if (lse && c == 0) lse[qi * H + head] = (M + log2f(Ls)) * kTcLn2;
+}
+
+// Key splits.  With fewer 64-head units than SMs, a unit's tiles are spread
+// over as many CTAs as keep the grid within one wave of `share` CTAs.
+struct TcPlan {
+    int kps;          // keys per split (a multiple of the tile)
+    int nsplit_max;   // splits of the query with the most keys
+};
+
+TcPlan tc_plan(const AttendArgs &a)
+{
+    const int share = a.sm_share > 0 ? a.sm_share : (a.num_sms > 0 ? a.num_sms : 148);
+    const int64_t units = a.total_q * (a.n_heads / kTcHeads);
+    const int64_t max_vis = a.max_kv_len / a.ratio;
+    int64_t mk = (a.idx ? (max_vis < a.top_k ? max_vis : a.top_k) : max_vis) + (a.ratio - 1);
+    if (mk > a.max_kv_len) mk = a.max_kv_len;   // the tail never exceeds the sequence
+    if (mk < 1) mk = 1;
+    const int64_t tiles = (mk + kTcKeys - 1) / kTcKeys;
+    int64_t want = units >= share ? 1 : share / units;
+    if (want > tiles) want = tiles;
+    if (want > 64) want = 64;   // the merge holds two splits per lane
+    if (want < 1) want = 1;
+    const int64_t tps = (tiles + want - 1) / want;
+    TcPlan pl;
+    pl.kps = (int)(tps * kTcKeys);
+    pl.nsplit_max = (int)((tiles + tps - 1) / tps);
+    return pl;
+}
+
+size_t tc_ws_bytes(const AttendArgs &a, const TcPlan &pl, float **part_o, float2 **part_ml)
+{
+    if (pl.nsplit_max <= 1) {
+        if (part_o) *part_o = nullptr;
+        if (part_ml) *part_ml = nullptr;
+        return 0;
+    }
+    const size_t slots = (size_t)a.total_q * (a.n_heads / kTcHeads) * pl.nsplit_max * kTcHeads;
+    const size_t ml = (slots * sizeof(float2) + 255) / 256 * 256;
+    if (part_ml) *part_ml = reinterpret_cast<float2 *>(a.ws);
+    if (part_o) *part_o = reinterpret_cast<float *>(static_cast<char *>(a.ws) + ml);
+    return ml + slots * kTcD * sizeof(float);
+}
+
+template <bool GATHER>
+cudaError_t launch_tc(const AttendArgs &a, cudaStream_t st)
+{
+    const TcPlan pl = tc_plan(a);
+    float *part_o = nullptr;
+    float2 *part_ml = nullptr;
+    tc_ws_bytes(a, pl, &part_o, &part_ml);
+    const int HG = a.n_heads / kTcHeads;
+    if ((int64_t)HG * pl.nsplit_max > 65535) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)a.total_q, (unsigned)(HG * pl.nsplit_max));
+    const float scale_log2 = a.scale * 1.4426950408889634f;
+    cudaError_t e = launch_kernel(GATHER ? "sparse_attend" : "dense_attend", attend_tc_kernel<GATHER>, grid,
+                                  dim3(kTcThreads), kTcSmem, st, a.pdl, a.batch, a.cu_kv, a.cu_q, a.cu_ent, a.q,
+                                  a.entries, a.kv, a.idx, a.n_heads, a.ratio, a.top_k, scale_log2, a.max_kv_len,
+                                  pl.kps, pl.nsplit_max, a.out, a.lse, part_o, part_ml, a.err);
+    if (e != cudaSuccess || pl.nsplit_max <= 1) return e;
+    const dim3 mgrid((unsigned)a.total_q, (unsigned)a.n_heads);
+    return launch_kernel(GATHER ? "sparse_merge" : "dense_merge", attend_tc_merge_kernel<GATHER>, mgrid,
+                         dim3(kMergeThreads), 0, st, true, a.batch, a.cu_kv, a.cu_q, a.cu_ent, a.n_heads,
+                         a.ratio, a.top_k, pl.kps, pl.nsplit_max, (const float *)part_o, (const float2 *)part_ml,
+                         a.out, a.lse);
+}
+
 }  // namespace
 
 bool attend_tc_applicable(const AttendArgs &a)
 {
-    const int share = a.num_sms > 0 ? a.num_sms : 148;
-    return a.d == kTcD && a.n_heads % kTcHeads == 0 && a.total_q * (a.n_heads / kTcHeads) >= share &&
-           (a.idx == nullptr || a.top_k <= kTcIdxCap) && a.total_q <= 0x7fffffffLL;
+    return a.d == kTcD && a.n_heads % kTcHeads == 0 && (a.idx == nullptr || a.top_k <= kTcIdxCap) &&
+           a.total_q <= 0x7fffffffLL;
 }
+
+size_t attend_tc_workspace_bytes(const AttendArgs &a) { return tc_ws_bytes(a, tc_plan(a), nullptr, nullptr); }
 
 cudaError_t launch_attend_tc(const AttendArgs &a, cudaStream_t st)
 {
     if (a.total_q <= 0) return cudaSuccess;
-    const dim3 grid((unsigned)a.total_q, (unsigned)(a.n_heads / kTcHeads));
-    const float scale_log2 = a.scale * 1.4426950408889634f;
-    if (a.idx)
-        return launch_kernel("sparse_attend", attend_tc_kernel<true>, grid, dim3(kTcThreads), kTcSmem, st, a.pdl,
-                             a.batch, a.cu_kv, a.cu_q, a.cu_ent, a.q, a.entries, a.kv, a.idx, a.n_heads, a.ratio,
-                             a.top_k, scale_log2, a.max_kv_len, a.out, a.lse, a.err);
-    return launch_kernel("dense_attend", attend_tc_kernel<false>, grid, dim3(kTcThreads), kTcSmem, st, a.pdl,
-                         a.batch, a.cu_kv, a.cu_q, a.cu_ent, a.q, a.entries, a.kv, a.idx, a.n_heads, a.ratio,
-                         a.top_k, scale_log2, a.max_kv_len, a.out, a.lse, a.err);
+    return a.idx ? launch_tc<true>(a, st) : launch_tc<false>(a, st);
 }
 
 }  // namespace csa

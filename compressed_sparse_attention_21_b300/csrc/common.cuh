@@ -227,6 +227,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
+// Bulk copy shared -> global (16-byte aligned addresses, size a multiple of
+// 16), tracked by the issuing thread's bulk group.  Shared-memory writes of
+// other threads must be ordered before it with fence.proxy.async and a barrier.
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// every bulk group of this thread complete (its global writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 // Warp 0: in a 256-bin histogram walked from the top bin down, find the bin
 // that holds the `remaining`-th largest element; report it and the count of
 // elements in higher bins.
@@ -292,6 +304,36 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *s_w, uint32
     const uint32_t r = s_w[NW + warp] + incl - v;
     __syncthreads();   // s_w may be reused right away
     return r;
+}
+
+// Thread-block clusters: rank within the cluster, the cluster-wide barrier
+// (release/acquire: shared-memory writes before it are visible to the peers
+// after it), and loads from a peer CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// the two halves of cluster_sync: arrive early, wait later
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
+// address of the same shared-memory location in the CTA of cluster rank `rank`
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // Programmatic dependent launch.  griddep_wait() blocks until every grid this

@@ -15,9 +15,11 @@
 //    order (ties resolved by rank among equal keys);
 //  * multi-CTA (decode-sized batches or long rows): many CTAs per query scan
 //    the indexer keys (the HBM-bound part), write the key row to the
-//    workspace and build a 4096-bin histogram of the keys' top 12 bits; the
-//    last CTA of a query (atomic ticket, no waiting) locates the bin that
-//    holds the k-th key.  A second kernel keeps everything above that bin,
+//    workspace and build a 4096-bin histogram of the keys' top 12 bits.
+//    For rows of up to kSelMaxN entries a cluster of CTAs per query then
+//    selects from the key row (path 3 below).  Longer rows: the last scan
+//    CTA of a query (atomic ticket, no waiting) locates the bin that holds
+//    the k-th key; a second kernel keeps everything above that bin,
 //    collects the bin's members as candidates, and its last CTA per query
 //    resolves them with a radix select on (key, index), then sorts the k
 //    winners by index.
@@ -40,6 +42,9 @@ constexpr int kScanChunk = 1024;      // entries per scan/filter CTA
 constexpr int kHistBits = 12;
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kFilterSmemCand = 3072;  // boundary candidates resolved in shared memory
+constexpr int kSelCluster = 8;        // CTAs per query in the select cluster
+constexpr int kSelCandCta = 512;      // boundary-bin members one select CTA ranks directly
+constexpr int kSelCandTotal = 2048;   // ... and the whole cluster
 constexpr int kMetaWords = 8;         // per-query: ticket1, ticket2, n_sel, n_cand, bin, above
 constexpr int64_t kGroupBudget = int64_t(1) << 30;   // max workspace of the multi-CTA path
 
@@ -532,35 +537,44 @@ index_filter_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
 
 // ---------------------------------------------------------------------------
 // path 3 (decode-sized batches, rows of up to kSelMaxN entries): a scan that
-// only streams, then one selecting CTA per query.
+// only streams, then one selecting cluster per query.
 //
-// index_chunk_scan_kernel: each CTA brings one 64 KiB chunk of indexer keys
-// into shared memory with a single bulk copy, scores its rows, stores their
-// keys and adds its histogram of the keys' top 12 bits into the query's
-// global histogram (reductions, nothing waits on them).
+// index_chunk_scan_kernel: each CTA takes a run of 32 KiB chunks of one
+// query's indexer keys, streamed through a ring of three shared-memory stages
+// by bulk copies (two CTAs per SM keep six chunks in flight), scores their
+// rows, stores their keys and adds its histogram of the keys' top 12 bits
+// into the query's global histogram (reductions, nothing waits on them).
 //
-// index_select_kernel: one CTA per query holds the query's whole key row in
-// registers (a contiguous segment per thread) after one round trip, finds
-// the exact k-th key (the 12-bit histogram, then 8 + 8 + 4 more bits over
-// the keys of the boundary bin), and writes the selection in index order
-// with one block-wide scan.  It returns the histogram to zero.
+// index_select_kernel: a cluster of kSelCluster CTAs per query holds the
+// query's whole key row in registers (consecutive segments per CTA, a
+// contiguous segment per thread) after one round trip.  Every CTA finds the
+// 12-bit bin of the k-th key from the histogram and publishes its keys in
+// that bin as (key, index) candidates; each CTA then gathers the cluster's
+// candidates through distributed shared memory and ranks its own among them
+// (key descending, index ascending), which decides the boundary exactly.
+// With more candidates than the lists hold (heavy ties) the bin is refined
+// 8 + 8 + 4 bits at a time instead, the CTAs' histograms summed over the
+// cluster.  The selection is written in index order after a block-wide scan
+// and a cluster-wide prefix of the CTAs' counts.  The cluster returns the
+// histogram to zero.
 // ---------------------------------------------------------------------------
-constexpr int kChunkBytes = 64 * 1024;
+constexpr int kChunkBytes = 32 * 1024;
+constexpr int kScanStages = 3;   // chunks in flight per CTA (two CTAs per SM)
 
 template <int DI>
-__global__ void __launch_bounds__(kScanThreads)
+__global__ void __launch_bounds__(kScanThreads, 2)
 index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
                         const int64_t *__restrict__ cu_csa, int64_t q_begin, const uint16_t *__restrict__ qI,
-                        const uint16_t *__restrict__ kI, int HI, int ratio, WsD w, int *err)
+                        const uint16_t *__restrict__ kI, int HI, int ratio, int cpc, WsD w, int *err)
 {
     constexpr int ROWS = kChunkBytes / (2 * DI);
     constexpr int LPR = DI / 8;                         // lanes per key row
     constexpr int RPW = 32 / LPR;                       // rows per warp step
     constexpr int NWARP = kScanThreads / 32;
-    extern __shared__ __align__(128) uint8_t s_rows[];
+    extern __shared__ __align__(128) uint8_t s_rows[];  // kScanStages chunks
     __shared__ float s_q[DI];
     __shared__ uint32_t s_hist[kHistBins];
-    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ __align__(8) uint64_t s_bar[kScanStages];
 
     griddep_launch();   // the select kernel may launch; it waits for this grid
     const int tid = threadIdx.x;
@@ -568,17 +582,25 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
     const int64_t qi = q_begin + qg;
     const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);
     const int64_t n = (p.t + 1) / ratio;
-    const int64_t r0 = (int64_t)blockIdx.x * ROWS;
-    if (r0 >= n) return;
-    if (!entry_count_ok(cu_csa, p, ratio) || n > w.key_stride) return;   // reported by the select kernel
-    const int rows = (int)(n - r0 < ROWS ? n - r0 : ROWS);
-    const uint16_t *kbase = kI + (p.e0 + r0) * DI;
-    const uint32_t bar = smem_u32(&s_bar);
+    const int64_t r_begin = (int64_t)blockIdx.x * cpc * ROWS;
+    if (r_begin >= n || !entry_count_ok(cu_csa, p, ratio) || n > w.key_stride) {   // (errors: reported by the select)
+        griddep_wait();
+        return;
+    }
+    const int64_t r_end = n - r_begin < (int64_t)cpc * ROWS ? n : r_begin + (int64_t)cpc * ROWS;
+    const int nchunks = (int)((r_end - r_begin + ROWS - 1) / ROWS);
+    const uint16_t *kbase = kI + (p.e0 + r_begin) * DI;
+    auto rows_of = [&](int c) { return (int)(r_end - r_begin - (int64_t)c * ROWS < ROWS ? r_end - r_begin - (int64_t)c * ROWS : ROWS); };
+    auto issue = [&](int c) {
+        const int s = c % kScanStages;
+        const uint32_t bytes = (uint32_t)rows_of(c) * DI * 2;
+        mbar_expect_tx(smem_u32(s_bar + s), bytes);
+        bulk_g2s(smem_u32(s_rows + s * kChunkBytes), kbase + (int64_t)c * ROWS * DI, bytes, smem_u32(s_bar + s));
+    };
     if (tid == 0) {
-        mbar_init(bar, 1);
+        for (int s = 0; s < kScanStages; s++) mbar_init(smem_u32(s_bar + s), 1);
         fence_mbar_init();
-        mbar_expect_tx(bar, (uint32_t)rows * DI * 2);
-        bulk_g2s(smem_u32(s_rows), kbase, (uint32_t)rows * DI * 2, bar);
+        for (int c = 0; c < nchunks && c < kScanStages; c++) issue(c);
     }
     for (int i = tid; i < kHistBins; i += kScanThreads) s_hist[i] = 0;
     load_qsum<DI>(qI, qi, HI, s_q);
@@ -588,36 +610,50 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
     float qv[8];
 #pragma unroll
     for (int x = 0; x < 8; x++) qv[x] = s_q[cg * 8 + x];
-    const bool landed = mbar_wait(bar, 0);
-    if (!landed) {
-        if (tid == 0) set_error(err, CSA_ERR_TIMEOUT);
-        return;   // histogram incomplete: the select kernel sees a count mismatch and pads the row
-    }
-    uint32_t *keys = w.keys + qg * w.key_stride + r0;
-    for (int rb = warp * RPW; rb < ROWS; rb += NWARP * RPW) {
-        const int row = rb + sub;
-        const bool in = row < rows;
-        const uint4 v = in ? *reinterpret_cast<const uint4 *>(s_rows + row * (2 * DI) + cg * 16) : make_uint4(0, 0, 0, 0);
-        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            acc = fmaf(qv[2 * k], bf16_lo(wd[k]), acc);
-            acc = fmaf(qv[2 * k + 1], bf16_hi(wd[k]), acc);
+    uint32_t *keys = w.keys + qg * w.key_stride + r_begin;
+    for (int c = 0; c < nchunks; c++) {
+        const int s = c % kScanStages;
+        const bool landed = mbar_wait(smem_u32(s_bar + s), (uint32_t)((c / kScanStages) & 1));
+        if (__syncthreads_or(!landed)) {
+            // the histogram stays incomplete: the select kernel sees a count
+            // mismatch and pads the row
+            if (tid == 0) set_error(err, CSA_ERR_TIMEOUT);
+            griddep_wait();
+            return;
         }
+        const int rows = rows_of(c);
+        const uint8_t *src = s_rows + s * kChunkBytes;
+        uint32_t *kc = keys + (int64_t)c * ROWS;
+        for (int rb = warp * RPW; rb < ROWS; rb += NWARP * RPW) {
+            const int row = rb + sub;
+            const bool in = row < rows;
+            const uint4 v = in ? *reinterpret_cast<const uint4 *>(src + row * (2 * DI) + cg * 16) : make_uint4(0, 0, 0, 0);
+            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+            float acc = 0.f;
 #pragma unroll
-        for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        const bool valid = cg == 0 && in;
-        const uint32_t key = score_key(acc);
-        if (valid) keys[row] = key;
-        if (valid) atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);   // few lanes per step: no aggregation
+            for (int k = 0; k < 4; k++) {
+                acc = fmaf(qv[2 * k], bf16_lo(wd[k]), acc);
+                acc = fmaf(qv[2 * k + 1], bf16_hi(wd[k]), acc);
+            }
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            const bool valid = cg == 0 && in;
+            const uint32_t key = score_key(acc);
+            if (valid) kc[row] = key;
+            if (valid) atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);   // few lanes per step: no aggregation
+        }
+        __syncthreads();   // stage s has been read
+        if (tid == 0 && c + kScanStages < nchunks) issue(c + kScanStages);
     }
-    __syncthreads();
     uint32_t *ghist = w.hist + qg * kHistBins;
     for (int i = tid; i < kHistBins; i += kScanThreads) {
-        const uint32_t c = s_hist[i];
-        if (c) atomicAdd(ghist + i, c);
+        const uint32_t cnt = s_hist[i];
+        if (cnt) atomicAdd(ghist + i, cnt);
     }
+    // Launched behind another kernel (IndexArgs::pdl), this grid reads nothing
+    // that kernel writes, but completes only after it: whatever waits for this
+    // grid may rely on the earlier one too.
+    griddep_wait();
 }
 
 template <int NT, int KPT>
@@ -626,31 +662,41 @@ index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
                     const int64_t *__restrict__ cu_csa, int64_t q_begin, int ratio, int top_k, WsD w,
                     int32_t *__restrict__ idx_out, float *__restrict__ score_out, int *err)
 {
+    constexpr int CL = kSelCluster;
     constexpr int BPT = kHistBins / NT;                 // top-level bins per thread
-    static_assert(KPT % 4 == 0 && kHistBins % NT == 0, "select tiling");
-    __shared__ uint32_t s_hist[256];
+    static_assert(KPT % 4 == 0 && BPT % 4 == 0 && NT >= 256 && kHistBins % CL == 0, "select tiling");
+    static_assert(kSelCandTotal * 8 <= kHistBins * 4, "the candidate list reuses the histogram stage");
+    __shared__ __align__(16) uint32_t s_big[kHistBins];   // the histogram, then the cluster's candidates
+    __shared__ uint32_t s_cand[kSelCandCta];              // this CTA's keys in the boundary bin
+    __shared__ uint32_t s_ncand;                          // read by the peers
+    __shared__ uint32_t s_hist[2][256];                   // fallback refinement histograms (read by the peers)
+    __shared__ uint32_t s_tot[256];
+    __shared__ uint32_t s_cnt[2];                         // this CTA's (greater, equal) counts (read by the peers)
+    __shared__ uint32_t s_off[2];
+    __shared__ uint32_t s_coff[CL + 1];
     __shared__ uint32_t s_w[2 * (NT / 32) + 1];
-    __shared__ uint32_t s_digit, s_above;
+    __shared__ uint32_t s_digit, s_above, s_bin;
 
-    griddep_wait();   // every chunk's keys and histogram counts are in place
     const int tid = threadIdx.x;
-    const int64_t qg = blockIdx.x;
+    const uint32_t rank = cluster_rank();
+    const int64_t qg = blockIdx.y;
     const int64_t qi = q_begin + qg;
-    const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);
+    griddep_launch();   // the attention after this kernel may launch; it waits for this grid
+    const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);   // layout arrays: inputs of the call
+    if (tid == 0) s_ncand = 0;
+    static_assert(NT * KPT < 65536, "per-CTA counts are packed in 16 bits");
+    griddep_wait();   // every chunk's keys and histogram counts are in place
     const int64_t n = (p.t + 1) / ratio;
     int32_t *idx_row = idx_out + qi * top_k;
     float *sc_row = score_out ? score_out + qi * top_k : nullptr;
     uint32_t *ghist = w.hist + qg * kHistBins;
-    if (!entry_count_ok(cu_csa, p, ratio) || n > w.key_stride || n > (int64_t)NT * KPT) {
-        if (tid == 0) set_error(err, CSA_ERR_DEVICE);
-        write_row_padding(idx_row, sc_row, 0, top_k);
-        for (int i = tid; i < kHistBins; i += NT) ghist[i] = 0;
-        return;
-    }
-    // one round trip: this thread's key segment and its histogram bins
+    // every test below gives the same answer in all CTAs of the cluster
+    const bool bad = !entry_count_ok(cu_csa, p, ratio) || n > w.key_stride || n > (int64_t)CL * NT * KPT;
+
+    // one round trip: this thread's key segment and the histogram (coalesced, into shared memory)
+    const int64_t seg0 = ((int64_t)rank * NT + tid) * KPT;
+    const int m = bad ? 0 : (int)(n - seg0 < 0 ? 0 : (n - seg0 < KPT ? n - seg0 : KPT));   // valid keys here
     const uint32_t *krow = w.keys + qg * w.key_stride;
-    const int64_t seg0 = (int64_t)tid * KPT;
-    const int m = (int)(n - seg0 < 0 ? 0 : (n - seg0 < KPT ? n - seg0 : KPT));   // valid keys here
     uint32_t key[KPT];
 #pragma unroll
     for (int i = 0; i < KPT; i += 4) {
@@ -661,12 +707,21 @@ index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
         key[i + 2] = v.z;
         key[i + 3] = v.w;
     }
+    for (int i = tid; i < kHistBins / 4; i += NT)
+        reinterpret_cast<uint4 *>(s_big)[i] = bad ? make_uint4(0, 0, 0, 0) : __ldcg(reinterpret_cast<const uint4 *>(ghist) + i);
+    __syncthreads();
+    // thread t takes bins 4095 - BPT t - i, i < BPT (walked from the top bin down)
     uint32_t hc[BPT], hsum = 0;
 #pragma unroll
-    for (int i = 0; i < BPT; i++) {
-        hc[i] = __ldcg(ghist + (kHistBins - 1 - BPT * tid - i));   // walked from the top bin down
-        hsum += hc[i];
+    for (int j = 0; j < BPT / 4; j++) {
+        const uint4 v = reinterpret_cast<const uint4 *>(s_big)[(kHistBins - BPT * (tid + 1)) / 4 + j];
+        hc[BPT - 1 - 4 * j] = v.x;
+        hc[BPT - 2 - 4 * j] = v.y;
+        hc[BPT - 3 - 4 * j] = v.z;
+        hc[BPT - 4 - 4 * j] = v.w;
     }
+#pragma unroll
+    for (int i = 0; i < BPT; i++) hsum += hc[i];
     const uint32_t k_eff = (uint32_t)(n < top_k ? n : top_k);
     // level 1: the 12-bit bin that holds the k-th largest key
     uint32_t tot;
@@ -678,65 +733,158 @@ index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
             if (acc + hc[i] >= k_eff) {
                 s_digit = (uint32_t)(kHistBins - 1 - BPT * tid - i);
                 s_above = acc;
+                s_bin = hc[i];
                 break;
             }
             acc += hc[i];
         }
     }
     __syncthreads();
-    // the histogram has been read: leave it zero for the next call
+    const bool partial = !bad && tot == (uint32_t)n && k_eff < (uint32_t)n;   // the boundary bin is split
+    const uint32_t b1 = s_digit;
+    // this CTA's members of the boundary bin
+    if (partial) {
 #pragma unroll
-    for (int i = 0; i < BPT; i++) ghist[kHistBins - 1 - BPT * tid - i] = 0;
-    if (tot != (uint32_t)n) {   // a chunk did not land (reported by the scan)
-        write_row_padding(idx_row, sc_row, 0, top_k);
+        for (int i = 0; i < KPT; i++) {
+            if (i < m && (key[i] >> 20) == b1) {
+                const uint32_t slot = atomicAdd(&s_ncand, 1u);
+                if (slot < (uint32_t)kSelCandCta) s_cand[slot] = key[i];
+            }
+        }
+    }
+    cluster_sync();   // the histogram has been read everywhere; candidate counts are published
+    for (int i = (int)rank * (kHistBins / CL) + tid; i < (int)(rank + 1) * (kHistBins / CL); i += NT) ghist[i] = 0;
+    if (bad || tot != (uint32_t)n) {   // a layout error, or a chunk that did not land (reported by the scan)
+        if (bad && rank == 0 && tid == 0) set_error(err, CSA_ERR_DEVICE);
+        if (rank == 0) write_row_padding(idx_row, sc_row, 0, top_k);
+        cluster_sync();   // no CTA leaves while a peer may still read its counts
         return;
     }
-    uint32_t kstar = 0, need_eq = 0;
-    if (k_eff < (uint32_t)n) {
-        uint32_t prefix = s_digit << 20, pmask = 0xfff00000u, remaining = k_eff - s_above;
-        // levels 2-4 over the keys of the boundary bin: bits 19..12, 11..4, 3..0
-#pragma unroll 1
-        for (int level = 0; level < 3; level++) {
-            const int sh = level == 0 ? 12 : (level == 1 ? 4 : 0);
-            const uint32_t dm = level == 2 ? 0xfu : 0xffu;
-            for (int i = tid; i < 256; i += NT) s_hist[i] = 0;
-            __syncthreads();
+    // the k-th key kstar: keys above it are taken, keys equal to it lowest index first
+    uint32_t kstar = 0, need_eq = 0xffffffffu;   // default: every key (kstar = 0 is at or below all of them)
+    if (partial) {
+        uint32_t remaining = k_eff - s_above;
+        if (tid < 32) {   // lane r reads rank r's count; a warp scan gives the offsets
+            const uint32_t c = tid < CL ? ld_cluster_u32(cluster_map(smem_u32(&s_ncand), (uint32_t)tid)) : 0u;
+            uint32_t incl = c;
 #pragma unroll
-            for (int i = 0; i < KPT; i++)
-                if (i < m && (key[i] & pmask) == prefix) atomicAdd(&s_hist[(key[i] >> sh) & dm], 1u);
-            __syncthreads();
-            if (tid < 32) find_digit_256(s_hist, remaining, &s_digit, &s_above);
-            __syncthreads();
-            remaining -= s_above;
-            prefix |= s_digit << sh;
-            pmask |= dm << sh;
-            __syncthreads();
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += v;
+            }
+            if (tid <= CL) s_coff[tid] = incl - c;
         }
+        __syncthreads();
+        bool fits = s_coff[CL] <= (uint32_t)kSelCandTotal;
+        for (int r = 0; r < CL; r++) fits = fits && s_coff[r + 1] - s_coff[r] <= (uint32_t)kSelCandCta;
+        uint32_t prefix = b1 << 20, pmask = 0xfff00000u;
+        bool whole = s_bin == remaining;   // the boundary bin is taken whole
+        if (!whole && fits) {
+            // gather the cluster's boundary-bin keys, then refine them here
+            // 8 + 8 + 4 bits at a time (every CTA reaches the same answer)
+            const uint32_t total = s_coff[CL];
+            uint32_t *all = s_big;
+            for (uint32_t i = tid; i < total; i += NT) {
+                int r = 0;
+                while (i >= s_coff[r + 1]) r++;
+                all[i] = ld_cluster_u32(cluster_map(smem_u32(s_cand + (i - s_coff[r])), (uint32_t)r));
+            }
+#pragma unroll 1
+            for (int level = 0; level < 3 && !whole; level++) {
+                const int sh = level == 0 ? 12 : (level == 1 ? 4 : 0);
+                const uint32_t dm = level == 2 ? 0xfu : 0xffu;
+                for (int i = tid; i < 256; i += NT) s_tot[i] = 0;
+                __syncthreads();
+                for (uint32_t i = tid; i < total; i += NT) {
+                    const uint32_t k = all[i];
+                    if ((k & pmask) == prefix) atomicAdd(&s_tot[(k >> sh) & dm], 1u);
+                }
+                __syncthreads();
+                if (tid < 32) find_digit_256(s_tot, remaining, &s_digit, &s_above);
+                __syncthreads();
+                remaining -= s_above;
+                prefix |= s_digit << sh;
+                pmask |= dm << sh;
+                whole = s_tot[s_digit] == remaining;
+                __syncthreads();   // s_digit, s_above and s_tot are rewritten by the next level
+            }
+        } else if (!whole) {
+            // many members (heavy ties): the same refinement over the keys in
+            // registers, the CTAs' histograms summed through distributed shared memory
+#pragma unroll 1
+            for (int level = 0; level < 3 && !whole; level++) {
+                const int sh = level == 0 ? 12 : (level == 1 ? 4 : 0);
+                const uint32_t dm = level == 2 ? 0xfu : 0xffu;
+                uint32_t *h = s_hist[level & 1];
+                for (int i = tid; i < 256; i += NT) h[i] = 0;
+                __syncthreads();
+#pragma unroll
+                for (int i = 0; i < KPT; i++)
+                    if (i < m && (key[i] & pmask) == prefix) atomicAdd(&h[(key[i] >> sh) & dm], 1u);
+                cluster_sync();
+                if (tid < 256) {
+                    const uint32_t a = smem_u32(h + tid);
+                    uint32_t t = 0;
+#pragma unroll
+                    for (int r = 0; r < CL; r++) t += ld_cluster_u32(cluster_map(a, (uint32_t)r));
+                    s_tot[tid] = t;
+                }
+                __syncthreads();
+                if (tid < 32) find_digit_256(s_tot, remaining, &s_digit, &s_above);
+                __syncthreads();
+                remaining -= s_above;
+                prefix |= s_digit << sh;
+                pmask |= dm << sh;
+                whole = s_tot[s_digit] == remaining;
+                __syncthreads();   // s_digit, s_above and s_tot are rewritten by the next level
+            }
+        }
+        // whole: every key at or above `prefix` (its lower bits zero) is taken
         kstar = prefix;
-        need_eq = remaining;   // keys equal to kstar to take, lowest index first
-    } else {
-        need_eq = 0xffffffffu;   // take every key: kstar = 0 is below every valid key or equal to it
+        need_eq = whole ? 0xffffffffu : remaining;
     }
-    // ordered emission: a thread's keys are contiguous in index order
+    // ordered emission: a thread's keys are contiguous in index order, and the
+    // CTAs of the cluster hold consecutive segments
     uint32_t n_gt = 0, n_eq = 0;
 #pragma unroll
     for (int i = 0; i < KPT; i++) {
         n_gt += (i < m && key[i] > kstar) ? 1u : 0u;
         n_eq += (i < m && key[i] == kstar) ? 1u : 0u;
     }
-    uint32_t t1, t2;
-    const uint32_t gt_before = block_scan<NT>(n_gt, s_w, t1);
-    const uint32_t eq_before = block_scan<NT>(n_eq, s_w, t2);
-    uint32_t pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
-    uint32_t eq_rank = eq_before;
+    uint32_t t_both;   // (greater, equal) counts packed 16 + 16 bits: at most NT * KPT <= 65536 keys per CTA
+    const uint32_t both_before = block_scan<NT>((n_eq << 16) | n_gt, s_w, t_both);
+    const uint32_t gt_before = both_before & 0xffffu, eq_before = both_before >> 16;
+    if (tid == 0) {
+        s_cnt[0] = t_both & 0xffffu;
+        s_cnt[1] = t_both >> 16;
+    }
+    cluster_sync();
+    if (tid < 32) {   // lane r < rank reads rank r's counts
+        uint32_t g = 0, e = 0;
+        if ((uint32_t)tid < rank) {
+            g = ld_cluster_u32(cluster_map(smem_u32(s_cnt), (uint32_t)tid));
+            e = ld_cluster_u32(cluster_map(smem_u32(s_cnt + 1), (uint32_t)tid));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            e += __shfl_xor_sync(0xffffffffu, e, o);
+        }
+        if (tid == 0) {
+            s_off[0] = g;
+            s_off[1] = e;
+        }
+    }
+    cluster_arrive();   // this CTA reads no peer from here on (waited for at the end)
+    __syncthreads();
+    const uint32_t eq0 = s_off[1] + eq_before;
+    uint32_t pos = s_off[0] + gt_before + (eq0 < need_eq ? eq0 : need_eq);
+    uint32_t eq_rank = eq0;
 #pragma unroll
     for (int i = 0; i < KPT; i++) {
         if (i >= m) continue;
         bool take = key[i] > kstar;
-        if (key[i] == kstar) {
-            take = eq_rank < need_eq;
-            eq_rank++;
-        }
+        if (key[i] == kstar) take = eq_rank++ < need_eq;
         if (take) {
             if (pos < (uint32_t)top_k) {
                 idx_row[pos] = (int32_t)(seg0 + i);
@@ -745,11 +893,12 @@ index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
             pos++;
         }
     }
-    write_row_padding(idx_row, sc_row, (int)k_eff, top_k);
-    if (tid == NT - 1 && pos != k_eff) set_error(err, CSA_ERR_DEVICE);
+    if (rank == 0) write_row_padding(idx_row, sc_row, (int)k_eff, top_k);
+    if (rank == CL - 1 && tid == NT - 1 && pos != k_eff) set_error(err, CSA_ERR_DEVICE);
+    cluster_wait();   // the peers have read this CTA's counts and candidates
 }
 
-constexpr int64_t kSelMaxN = 512 * 64;    // longest row the select kernel holds (entries)
+constexpr int64_t kSelMaxN = (int64_t)kSelCluster * 1024 * 32;   // longest row the select cluster holds (entries)
 
 bool use_cta_path(const IndexArgs &a)
 {
@@ -767,11 +916,42 @@ int64_t group_size(const IndexArgs &a)
     return g < a.total_q ? g : a.total_q;
 }
 
+int device_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+
+// The select cluster for rows of up to max_n entries: kSelCluster CTAs of NT
+// threads holding KPT keys each.
+cudaError_t launch_select(const IndexArgs &a, int64_t max_n, int64_t q0, int64_t nq, const WsD &w, cudaStream_t st)
+{
+    const dim3 grid((unsigned)kSelCluster, (unsigned)nq);
+    auto go = [&](auto kern, int nt) {
+        return launch_kernel_cluster("index_select", kern, grid, dim3(nt), 0, st, true, (unsigned)kSelCluster,
+                                     a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0, a.ratio, a.top_k, w, a.idx_out,
+                                     a.score_out, a.err);
+    };
+    if (max_n <= kSelCluster * 256 * 8) return go(index_select_kernel<256, 8>, 256);
+    if (max_n <= kSelCluster * 256 * 16) return go(index_select_kernel<256, 16>, 256);
+    if (max_n <= kSelCluster * 512 * 32) return go(index_select_kernel<512, 32>, 512);
+    return go(index_select_kernel<1024, 32>, 1024);
+}
+
 template <int DI>
 cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
 {
     if (a.total_q <= 0) return cudaSuccess;
     const int64_t max_n = a.max_kv_len / a.ratio;
+    // scan_done: after the last key scan of the multi-kernel paths; the
+    // single-kernel paths mark it up front (their kernel holds the GPU to the end)
+    auto mark = [&]() -> cudaError_t { return a.scan_done ? cudaEventRecord(a.scan_done, st) : cudaSuccess; };
+    if (index_block_applicable(a) || use_cta_path(a)) {
+        cudaError_t e = mark();
+        if (e != cudaSuccess) return e;
+    }
     if (index_block_applicable(a)) return launch_index_block(a, st);
     if (use_cta_path(a)) {
         const int64_t nsm = max_n < 1 ? 1 : max_n;
@@ -792,20 +972,21 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
     if (max_n <= kSelMaxN) {
         constexpr int ROWS = kChunkBytes / (2 * DI);
         const int64_t nch = max_n <= 0 ? 1 : (max_n + ROWS - 1) / ROWS;
+        // chunks per CTA: the group's chunks over about two CTAs per SM
+        const int64_t slots = 2 * (int64_t)device_sms();
         for (int64_t q0 = 0; q0 < a.total_q; q0 += gq) {
             const int64_t nq = a.total_q - q0 < gq ? a.total_q - q0 : gq;
-            cudaError_t e = launch_kernel("index_scan", index_chunk_scan_kernel<DI>, dim3((unsigned)nch, (unsigned)nq),
-                                          dim3(kScanThreads), (size_t)kChunkBytes, st, false, a.batch, a.cu_kv,
-                                          a.cu_q, a.cu_csa, q0, a.q_idx, a.k_idx, a.n_heads_idx, a.ratio, w, a.err);
+            int64_t cpc = (nq * nch + slots - 1) / slots;
+            if (cpc < 1) cpc = 1;
+            if (cpc > nch) cpc = nch;
+            const int64_t gx = (nch + cpc - 1) / cpc;
+            cudaError_t e = launch_kernel("index_scan", index_chunk_scan_kernel<DI>, dim3((unsigned)gx, (unsigned)nq),
+                                          dim3(kScanThreads), (size_t)kScanStages * kChunkBytes, st, a.pdl, a.batch,
+                                          a.cu_kv, a.cu_q, a.cu_csa, q0, a.q_idx, a.k_idx, a.n_heads_idx, a.ratio,
+                                          (int)cpc, w, a.err);
+            if (e == cudaSuccess && q0 + nq >= a.total_q) e = mark();
             if (e != cudaSuccess) return e;
-            if (max_n <= 1024 * 16)
-                e = launch_kernel("index_select", index_select_kernel<1024, 16>, dim3((unsigned)nq), dim3(1024), 0,
-                                  st, true, a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0, a.ratio, a.top_k, w, a.idx_out,
-                                  a.score_out, a.err);
-            else
-                e = launch_kernel("index_select", index_select_kernel<512, 64>, dim3((unsigned)nq), dim3(512), 0, st,
-                                  true, a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0, a.ratio, a.top_k, w, a.idx_out,
-                                  a.score_out, a.err);
+            e = launch_select(a, max_n, q0, nq, w, st);
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
@@ -816,6 +997,7 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
         cudaError_t e = launch_kernel("index_scan", index_scan_kernel<DI>, grid, dim3(kScanThreads), 0, st, false,
                                       a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0, a.q_idx, a.k_idx, a.n_heads_idx,
                                       a.ratio, a.top_k, w, a.idx_out, a.score_out, a.err);
+        if (e == cudaSuccess && q0 + nq >= a.total_q) e = mark();
         if (e != cudaSuccess) return e;
         e = launch_kernel("index_filter", index_filter_kernel, grid, dim3(kScanThreads), 0, st, true, a.batch, a.cu_kv,
                           a.cu_q, a.cu_csa, q0, a.ratio, a.top_k, w, a.idx_out, a.score_out, a.err);

@@ -21,9 +21,22 @@ cudaError_t ensure_smem_fn(const void *kern, size_t smem);
 // serialisation: it may begin while the kernel before it on the stream is
 // still running, and must execute griddep_wait() before it touches anything
 // that kernel (or any earlier work) writes or reads.
+// Like launch_kernel, with thread-block clusters of `cluster_x` CTAs along x
+// (grid.x a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_cluster(const char *name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t st, bool pdl, unsigned cluster_x, Args &&...args);
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(const char *name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                           cudaStream_t st, bool pdl, Args &&...args)
+{
+    return launch_kernel_cluster(name, kern, grid, block, smem, st, pdl, 1u, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_cluster(const char *name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t st, bool pdl, unsigned cluster_x, Args &&...args)
 {
     cudaError_t e = cudaSuccess;
     if (smem > 48 * 1024) {
@@ -42,11 +55,22 @@ cudaError_t launch_kernel(const char *name, void (*kern)(KArgs...), dim3 grid, d
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    if (pdl && !timed) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        na++;
+    }
+    if (cluster_x > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cluster_x;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        na++;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = (pdl && !timed) ? 1 : 0;
+    cfg.numAttrs = na;
     e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (timed) {
@@ -78,7 +102,8 @@ struct IndexArgs {
     int batch;
     int max_kv_len, max_q_len;
     int64_t total_q;
-    bool pdl;             // the first kernel may overlap the stream's previous kernel
+    bool pdl;             // the key scan of the multi-kernel paths may overlap the stream's previous kernel
+    cudaEvent_t scan_done;  // if set: recorded on the stream once every key has been scored
     const int64_t *cu_kv, *cu_q, *cu_csa;
     const uint16_t *q_idx, *k_idx;
     int n_heads_idx, d_idx, ratio, top_k;
@@ -125,9 +150,11 @@ struct AttendArgs {
     int sm_share;         // SMs this launch may count on (concurrent branches)
 };
 bool attend_supported(int n_heads, int d);
-// tcgen05 path (attend_tc.cu): d = 512, heads a multiple of 64, at least as
-// many 64-head units as SMs; needs no workspace.
+// tcgen05 path (attend_tc.cu): d = 512, heads a multiple of 64; decode-sized
+// batches split each query's keys over several CTAs and merge the partial
+// results (workspace: the partial outputs).
 bool attend_tc_applicable(const AttendArgs &a);
+size_t attend_tc_workspace_bytes(const AttendArgs &a);
 cudaError_t launch_attend_tc(const AttendArgs &a, cudaStream_t st);
 size_t attend_workspace_bytes(const AttendArgs &a);
 cudaError_t launch_attend(const AttendArgs &a, cudaStream_t st);

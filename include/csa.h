@@ -49,11 +49,11 @@
  *   - The first call on a device creates one helper stream and three events
  *     for that device (hybrid_attend runs its two branches concurrently on
  *     them).  Make that first call outside any CUDA graph capture.
- *   - Inside hybrid_attend and lightning_index_topk, kernels that follow
- *     another kernel of the same call may be launched with programmatic
- *     dependent launch (they start early and wait on the device for their
- *     predecessor).  The first kernel of every call waits for all earlier
- *     work on the caller's stream in the ordinary way.
+ *   - Inside a call, kernels that follow another kernel of the same call may
+ *     be launched with programmatic dependent launch (they start early and
+ *     wait on the device for their predecessor).  The first kernel of every
+ *     call waits for all earlier work on the caller's stream in the ordinary
+ *     way.
  */
 #ifndef CSA_H
 #define CSA_H

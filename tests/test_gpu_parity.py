@@ -160,7 +160,8 @@ def test_index_topk_all_ties_lowest_index_wins(queries):
 @pytest.mark.parametrize("H,d", [(8, 128), (8, 512), (64, 512), (128, 512), (64, 128)])
 @pytest.mark.parametrize("mode", ["decode", "prefill"])
 def test_attend_parity(H, d, mode):
-    lengths = [1, 3, 4, 129, 1000, 5003] if mode == "decode" else [1, 130, 257]
+    # decode: 20000 gives the dense branch 188 keys, split over several CTAs
+    lengths = [1, 3, 4, 129, 1000, 5003, 20000] if mode == "decode" else [1, 130, 257]
     n_q = [1] * len(lengths) if mode == "decode" else lengths
     k = 64 if mode == "prefill" else 128
     p = problem(lengths, n_q, H=H, d=d, k=k, seed=H + d)
