@@ -257,17 +257,40 @@ csa_status_t compress_impl(const csa_layout *L, bool csa_side, const csa_bf16 *k
     return from_cuda(launch_compress(a, st));
 }
 
+// SMs of the two attention branches, which run at the same time in a decode
+// step: in proportion to their largest key counts, so that both split-KV
+// grids fit on the GPU together.
+void hybrid_shares(const csa_hybrid_params *p, int num_sms, int *sparse_share, int *dense_share)
+{
+    const csa_layout *L = &p->layout;
+    const int64_t Lmax = L->max_kv_len;
+    int64_t ks = Lmax / p->ratio_csa;
+    if (ks > p->top_k) ks = p->top_k;
+    ks += p->ratio_csa - 1;
+    int64_t kd = Lmax / p->ratio_hca + p->ratio_hca - 1;
+    ks = ks < Lmax ? ks : Lmax;
+    kd = kd < Lmax ? kd : Lmax;
+    const int n = num_sms > 0 ? num_sms : 148;
+    int64_t d = ks + kd > 0 ? (int64_t)n * kd / (ks + kd) : n / 2;
+    if (d < n / 8) d = n / 8;
+    if (d > n - n / 8) d = n - n / 8;
+    *dense_share = (int)d;
+    *sparse_share = n - (int)d;
+}
+
 size_t hybrid_ws_parts(const csa_hybrid_params *p, size_t *idx_ws, size_t *sp_ws, size_t *hc_ws, int num_sms)
 {
+    int sh_s = 0, sh_d = 0;
+    hybrid_shares(p, num_sms, &sh_s, &sh_d);
     const csa_layout *L = &p->layout;
     IndexArgs ia = index_args(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k, nullptr,
                               nullptr, nullptr, 0, nullptr);
     AttendArgs sa = attend_args(L, L->cu_csa, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d,
                                 p->ratio_csa, p->top_k, p->scale, nullptr, nullptr, nullptr, 0, nullptr, num_sms,
-                                num_sms);
+                                sh_s);
     sa.idx = reinterpret_cast<const int32_t *>(1);   // sparse plan
     AttendArgs ha = attend_args(L, L->cu_hca, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca,
-                                0, p->scale, nullptr, nullptr, nullptr, 0, nullptr, num_sms, num_sms);
+                                0, p->scale, nullptr, nullptr, nullptr, 0, nullptr, num_sms, sh_d);
     *idx_ws = align_ws(index_workspace_bytes(ia));
     *sp_ws = align_ws(attend_workspace_bytes(sa));
     *hc_ws = align_ws(attend_workspace_bytes(ha));
@@ -501,13 +524,16 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
         cudaEventRecord(ds->sdone, st);
     }
 
+    int sh_s = 0, sh_d = 0;
+    hybrid_shares(p, ds->num_sms, &sh_s, &sh_d);
+
     // a5 on the helper stream, behind the compression and the key scan
     const bool c1 = cudaStreamWaitEvent(ds->aux, ds->sdone, 0) == cudaSuccess;
     csa_status_t s_h = s_c;
     if (s_h == CSA_OK) {
         AttendArgs ha = attend_args(L, L->cu_hca, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d,
                                     p->ratio_hca, 0, p->scale, p->o_hca, p->lse_hca,
-                                    w_hc ? ws + w_idx + w_sp : nullptr, w_hc, ds->err, ds->num_sms, ds->num_sms);
+                                    w_hc ? ws + w_idx + w_sp : nullptr, w_hc, ds->err, ds->num_sms, sh_d);
         s_h = from_cuda(launch_attend(ha, ds->aux));
     }
 
@@ -515,7 +541,7 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
     if (s_c == CSA_OK) {
         AttendArgs sa = attend_args(L, L->cu_csa, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d,
                                     p->ratio_csa, p->top_k, p->scale, p->o_csa, p->lse_csa,
-                                    w_sp ? ws + w_idx : nullptr, w_sp, ds->err, ds->num_sms, ds->num_sms);
+                                    w_sp ? ws + w_idx : nullptr, w_sp, ds->err, ds->num_sms, sh_s);
         sa.pdl = true;
         s_c = from_cuda(launch_attend(sa, st));
     }

@@ -134,13 +134,21 @@ __device__ __forceinline__ int tc_key_count(const QueryPos &p, int ratio, int to
     return n_main + (int)((p.t + 1) % ratio);
 }
 
+// A query with T key tiles runs in min(nsplit_max, T) splits; split s takes
+// tiles [s T / ns, (s + 1) T / ns).
+__device__ __forceinline__ int tc_nsplit(int n_keys, int nsplit_max)
+{
+    const int T = (n_keys + kTcKeys - 1) / kTcKeys;
+    return T < nsplit_max ? T : nsplit_max;
+}
+
 template <bool GATHER>
 __global__ void __launch_bounds__(kTcThreads, 1)
 attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
                  const int64_t *__restrict__ cu_ent, const uint16_t *__restrict__ q,
                  const uint16_t *__restrict__ entries, const uint16_t *__restrict__ kv,
                  const int32_t *__restrict__ idx, int H, int ratio, int top_k, float scale_log2, int max_kv_len,
-                 int kps, int nsplit_max, uint16_t *__restrict__ out, float *__restrict__ lse,
+                 int nsplit_max, uint16_t *__restrict__ out, float *__restrict__ lse,
                  float *__restrict__ part_o, float2 *__restrict__ part_ml, int *err)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -152,7 +160,6 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
     const int HG = H / kTcHeads;
     const int hg = blockIdx.y % HG;
     const int split = blockIdx.y / HG;
-    griddep_launch();   // the merge kernel may launch; it waits for this grid
 
     const QueryPos p = query_pos(cu_kv, cu_q, cu_ent, batch, qi);
     const int64_t n_vis = (p.t + 1) / ratio;
@@ -169,11 +176,13 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
     ks.n_vis = n_vis;
     ks.n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
     ks.n_keys = ks.n_main + r_tail;
-    const int nsplit = (ks.n_keys + kps - 1) / kps;
-    if (split >= nsplit) return;   // this query has fewer keys than the longest one
-    const int key0 = split * kps;
-    const int key1 = min(ks.n_keys, key0 + kps);
-    const int T = (key1 - key0 + kTcKeys - 1) / kTcKeys;
+    const int nsplit = tc_nsplit(ks.n_keys, nsplit_max);
+    if (split >= nsplit) return;   // this query has fewer key tiles than splits
+    const int T_all = (ks.n_keys + kTcKeys - 1) / kTcKeys;
+    const int t0 = (int)((int64_t)split * T_all / nsplit), t1 = (int)((int64_t)(split + 1) * T_all / nsplit);
+    const int key0 = t0 * kTcKeys;
+    const int key1 = min(ks.n_keys, t1 * kTcKeys);
+    const int T = t1 - t0;
 
     const uint32_t bar0 = sb + OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -499,6 +508,11 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
     }
     tc::fence_before_sync();
     __syncthreads();
+    // The merge kernel may launch once every CTA is here (or has exited); the
+    // first thread of a CTA to execute the trigger fires it, so it follows the
+    // barrier.  Launched earlier, the merge CTAs would wait on SMs that
+    // attention CTAs need.
+    griddep_launch();
     tc::fence_after_sync();
     if (warp == 4) tc::tmem_dealloc(tmem, kTmemCols);
 }
@@ -515,7 +529,7 @@ constexpr int kMergeBatch = 8;
 template <bool GATHER>
 __global__ void __launch_bounds__(kMergeThreads, 8)
 attend_tc_merge_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
-                       const int64_t *__restrict__ cu_ent, int H, int ratio, int top_k, int kps, int nsplit_max,
+                       const int64_t *__restrict__ cu_ent, int H, int ratio, int top_k, int nsplit_max,
                        const float *__restrict__ part_o, const float2 *__restrict__ part_ml,
                        uint16_t *__restrict__ out, float *__restrict__ lse)
 {
@@ -524,7 +538,7 @@ attend_tc_merge_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64
     const int head = blockIdx.y;
     const QueryPos p = query_pos(cu_kv, cu_q, cu_ent, batch, qi);
     if (p.t < 0 || p.t >= p.L || p.ne != p.L / ratio) return;   // reported by the attention kernel
-    const int nsplit = (tc_key_count<GATHER>(p, ratio, top_k) + kps - 1) / kps;
+    const int nsplit = tc_nsplit(tc_key_count<GATHER>(p, ratio, top_k), nsplit_max);
     if (nsplit <= 1) return;   // written by the attention kernel itself
     griddep_wait();            // the partial results are complete
     const int64_t base = (qi * (H / kTcHeads) + head / kTcHeads) * nsplit_max * kTcHeads + head % kTcHeads;
@@ -563,11 +577,10 @@ attend_tc_merge_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64
     if (lse && c == 0) lse[qi * H + head] = (M + log2f(Ls)) * kTcLn2;
 }
 
-// Key splits.  With fewer 64-head units than SMs, a unit's tiles are spread
-// over as many CTAs as keep the grid within one wave of `share` CTAs.
+// Key splits.  With fewer 64-head units than `share` SMs, a unit's tiles are
+// spread over as many CTAs as keep the grid within one wave of `share` CTAs.
 struct TcPlan {
-    int kps;          // keys per split (a multiple of the tile)
-    int nsplit_max;   // splits of the query with the most keys
+    int nsplit_max;   // splits of a query with at least that many key tiles
 };
 
 TcPlan tc_plan(const AttendArgs &a)
@@ -581,12 +594,10 @@ TcPlan tc_plan(const AttendArgs &a)
     const int64_t tiles = (mk + kTcKeys - 1) / kTcKeys;
     int64_t want = units >= share ? 1 : share / units;
     if (want > tiles) want = tiles;
-    if (want > 64) want = 64;   // the merge holds two splits per lane
+    if (want > 64) want = 64;   // the merge reads at most 64 splits
     if (want < 1) want = 1;
-    const int64_t tps = (tiles + want - 1) / want;
     TcPlan pl;
-    pl.kps = (int)(tps * kTcKeys);
-    pl.nsplit_max = (int)((tiles + tps - 1) / tps);
+    pl.nsplit_max = (int)want;
     return pl;
 }
 
@@ -618,12 +629,15 @@ cudaError_t launch_tc(const AttendArgs &a, cudaStream_t st)
     cudaError_t e = launch_kernel(GATHER ? "sparse_attend" : "dense_attend", attend_tc_kernel<GATHER>, grid,
                                   dim3(kTcThreads), kTcSmem, st, a.pdl, a.batch, a.cu_kv, a.cu_q, a.cu_ent, a.q,
                                   a.entries, a.kv, a.idx, a.n_heads, a.ratio, a.top_k, scale_log2, a.max_kv_len,
-                                  pl.kps, pl.nsplit_max, a.out, a.lse, part_o, part_ml, a.err);
+                                  pl.nsplit_max, a.out, a.lse, part_o, part_ml, a.err);
     if (e != cudaSuccess || pl.nsplit_max <= 1) return e;
+    // The merge overlaps the attention's tail only on a dependent-launch chain
+    // (a.pdl); otherwise its many small CTAs, launched early, would wait on
+    // SMs that other work on the GPU needs.
     const dim3 mgrid((unsigned)a.total_q, (unsigned)a.n_heads);
     return launch_kernel(GATHER ? "sparse_merge" : "dense_merge", attend_tc_merge_kernel<GATHER>, mgrid,
-                         dim3(kMergeThreads), 0, st, true, a.batch, a.cu_kv, a.cu_q, a.cu_ent, a.n_heads,
-                         a.ratio, a.top_k, pl.kps, pl.nsplit_max, (const float *)part_o, (const float2 *)part_ml,
+                         dim3(kMergeThreads), 0, st, a.pdl, a.batch, a.cu_kv, a.cu_q, a.cu_ent, a.n_heads,
+                         a.ratio, a.top_k, pl.nsplit_max, (const float *)part_o, (const float2 *)part_ml,
                          a.out, a.lse);
 }
 

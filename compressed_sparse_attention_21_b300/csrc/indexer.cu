@@ -681,7 +681,6 @@ index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
     const uint32_t rank = cluster_rank();
     const int64_t qg = blockIdx.y;
     const int64_t qi = q_begin + qg;
-    griddep_launch();   // the attention after this kernel may launch; it waits for this grid
     const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);   // layout arrays: inputs of the call
     if (tid == 0) s_ncand = 0;
     static_assert(NT * KPT < 65536, "per-CTA counts are packed in 16 bits");
@@ -876,6 +875,10 @@ index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
         }
     }
     cluster_arrive();   // this CTA reads no peer from here on (waited for at the end)
+    // The attention after this kernel may launch now (it waits for this grid
+    // on the device).  Triggered this late so that its CTAs do not sit on SMs
+    // the concurrent dense branch could use.
+    griddep_launch();
     __syncthreads();
     const uint32_t eq0 = s_off[1] + eq_before;
     uint32_t pos = s_off[0] + gt_before + (eq0 < need_eq ? eq0 : need_eq);
