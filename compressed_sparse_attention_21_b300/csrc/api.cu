@@ -156,7 +156,7 @@ IndexArgs index_args(const csa_layout *L, const csa_bf16 *q_idx, const csa_bf16 
     return a;
 }
 
-AttendArgs attend_args(const csa_layout *L, const int64_t *cu_ent, const csa_bf16 *q, const csa_bf16 *entries,
+AttendArgs attend_args(const csa_layout *L, bool csa_side, const csa_bf16 *q, const csa_bf16 *entries,
                        const csa_bf16 *kv, const int32_t *idx, int H, int d, int ratio, int top_k, float scale,
                        csa_bf16 *out, float *lse, void *ws, size_t ws_bytes, int *err, int num_sms, int sm_share)
 {
@@ -167,7 +167,9 @@ AttendArgs attend_args(const csa_layout *L, const int64_t *cu_ent, const csa_bf1
     a.total_q = L->total_q;
     a.cu_kv = L->cu_kv;
     a.cu_q = L->cu_q;
-    a.cu_ent = cu_ent;
+    a.cu_ent = csa_side ? L->cu_csa : L->cu_hca;
+    a.n_ent_rows = csa_side ? L->total_csa : L->total_hca;
+    a.n_kv_rows = L->total_kv;
     a.q = q;
     a.entries = entries;
     a.kv = kv;
@@ -285,11 +287,11 @@ size_t hybrid_ws_parts(const csa_hybrid_params *p, size_t *idx_ws, size_t *sp_ws
     const csa_layout *L = &p->layout;
     IndexArgs ia = index_args(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k, nullptr,
                               nullptr, nullptr, 0, nullptr);
-    AttendArgs sa = attend_args(L, L->cu_csa, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d,
+    AttendArgs sa = attend_args(L, true, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d,
                                 p->ratio_csa, p->top_k, p->scale, nullptr, nullptr, nullptr, 0, nullptr, num_sms,
                                 sh_s);
     sa.idx = reinterpret_cast<const int32_t *>(1);   // sparse plan
-    AttendArgs ha = attend_args(L, L->cu_hca, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca,
+    AttendArgs ha = attend_args(L, false, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca,
                                 0, p->scale, nullptr, nullptr, nullptr, 0, nullptr, num_sms, sh_d);
     *idx_ws = align_ws(index_workspace_bytes(ia));
     *sp_ws = align_ws(attend_workspace_bytes(sa));
@@ -399,7 +401,7 @@ csa_status_t csa_attend_workspace_size(const csa_layout *layout, int n_heads, in
     if (!attend_supported(n_heads, d)) return CSA_ERR_UNSUPPORTED;
     DeviceState *ds = nullptr;
     CSA_TRY(device_state(&ds));
-    AttendArgs a = attend_args(layout, sparse ? layout->cu_csa : layout->cu_hca, nullptr, nullptr, nullptr,
+    AttendArgs a = attend_args(layout, sparse, nullptr, nullptr, nullptr,
                                sparse ? reinterpret_cast<const int32_t *>(1) : nullptr, n_heads, d, ratio, top_k,
                                1.f, nullptr, nullptr, nullptr, 0, nullptr, ds->num_sms, ds->num_sms);
     *bytes = align_ws(attend_workspace_bytes(a));
@@ -414,7 +416,7 @@ csa_status_t sparse_mqa_attend(const csa_layout *layout, const csa_bf16 *q, cons
     CSA_TRY(check_attend(layout, true, q, csa_entries, kv, idx, n_heads, d, ratio, top_k, out, lse));
     DeviceState *ds = nullptr;
     CSA_TRY(device_state(&ds));
-    AttendArgs a = attend_args(layout, layout->cu_csa, q, csa_entries, kv, idx, n_heads, d, ratio, top_k, scale,
+    AttendArgs a = attend_args(layout, true, q, csa_entries, kv, idx, n_heads, d, ratio, top_k, scale,
                                out, lse, ws, ws_bytes, ds->err, ds->num_sms, ds->num_sms);
     const size_t need = attend_workspace_bytes(a);
     if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return CSA_ERR_WORKSPACE;
@@ -428,7 +430,7 @@ csa_status_t hca_dense_attend(const csa_layout *layout, const csa_bf16 *q, const
     CSA_TRY(check_attend(layout, false, q, hca_entries, kv, nullptr, n_heads, d, ratio, 0, out, lse));
     DeviceState *ds = nullptr;
     CSA_TRY(device_state(&ds));
-    AttendArgs a = attend_args(layout, layout->cu_hca, q, hca_entries, kv, nullptr, n_heads, d, ratio, 0, scale,
+    AttendArgs a = attend_args(layout, false, q, hca_entries, kv, nullptr, n_heads, d, ratio, 0, scale,
                                out, lse, ws, ws_bytes, ds->err, ds->num_sms, ds->num_sms);
     const size_t need = attend_workspace_bytes(a);
     if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return CSA_ERR_WORKSPACE;
@@ -531,7 +533,7 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
     const bool c1 = cudaStreamWaitEvent(ds->aux, ds->sdone, 0) == cudaSuccess;
     csa_status_t s_h = s_c;
     if (s_h == CSA_OK) {
-        AttendArgs ha = attend_args(L, L->cu_hca, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d,
+        AttendArgs ha = attend_args(L, false, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d,
                                     p->ratio_hca, 0, p->scale, p->o_hca, p->lse_hca,
                                     w_hc ? ws + w_idx + w_sp : nullptr, w_hc, ds->err, ds->num_sms, sh_d);
         s_h = from_cuda(launch_attend(ha, ds->aux));
@@ -539,7 +541,7 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
 
     // a4, launched behind the selection
     if (s_c == CSA_OK) {
-        AttendArgs sa = attend_args(L, L->cu_csa, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d,
+        AttendArgs sa = attend_args(L, true, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d,
                                     p->ratio_csa, p->top_k, p->scale, p->o_csa, p->lse_csa,
                                     w_sp ? ws + w_idx : nullptr, w_sp, ds->err, ds->num_sms, sh_s);
         sa.pdl = true;

@@ -17,14 +17,19 @@
 // 128-byte row of 64 heads per key) as the MN-major B operand.  With M = 64
 // the accumulator row r sits in tensor-memory lane 32 (r / 16) + r % 16.
 // Two key stages, two S^T buffers and two P stages let the tensor core run
-// S^T of tile t+1 while the softmax of tile t proceeds, and the gather of a
-// stage overlap the other stage's products.  Tensor memory: S^T x 2 (64
-// columns each) and O^T (4 x 64 columns).
+// S^T of tile t+1 and P V of tile t-1 while the softmax of tile t proceeds,
+// and the gather of a stage overlap the other stage's products.  Tensor
+// memory: S^T x 2 (64 columns each) and O^T (4 x 64 columns).
 //
-// Warp roles (352 threads): warps 0-3 softmax (thread (w, l) takes key
+// Warp roles (384 threads): warps 0-3 softmax (thread (w, l) takes key
 // 16 w + l % 16 of the tile, heads 32 (l / 16) .. +31; afterwards row
-// d = 128 m + 32 w + l of the output), warp 4 lane 0 issues the MMAs, warps
-// 5-7 gather even tiles and warps 8-10 odd tiles with cp.async.  The
+// d = 128 m + 32 w + l of the output), warp 4 lane 0 issues the MMAs, warp 5
+// lane 0 issues the tensor-memory-access (TMA) loads: visible entries, raw
+// tail rows and the query tile as 64-row tiles, all in the 128-byte swizzled
+// layout the MMAs read.  Selected entries are gathered by warps 6-11 with
+// 16-byte cp.async (measured faster than four-row TMA gathers of 128-byte
+// rows, whose issue rate bounds a tile at about 4 us).  A tile holds either
+// entries or raw tail rows, never both, so each comes from one tensor.  The
 // running maximum of a head is raised only when a tile exceeds it by more
 // than 2^8 (the accumulated O^T column and sum are then rescaled); the
 // result is exact either way because the sum uses the same maximum.
@@ -33,6 +38,11 @@
 // and each head's (max, sum); attend_tc_merge_kernel, launched behind it,
 // combines the splits: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 // Every wait is bounded: one that runs out reports CSA_ERR_TIMEOUT.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
@@ -41,13 +51,13 @@ namespace csa {
 
 namespace {
 
-constexpr int kTcThreads = 352;
+constexpr int kTcThreads = 384;
+constexpr int kGatherBase = 192;             // first cp.async gather thread (warp 6)
+constexpr int kGatherThreads = 192;          // warps 6-11
 constexpr int kTcKeys = 64;                  // keys per tile (M of S^T)
 constexpr int kTcHeads = 64;                 // heads per CTA (N)
 constexpr int kTcD = 512;
 constexpr int kRegions = kTcD / 64;          // 64-column regions of a 128-byte swizzled row
-constexpr int kProd = 96;                    // producer threads per group (3 warps)
-constexpr int kProdBase = 160;               // first producer thread (warp 5)
 constexpr uint32_t kReg = 64 * 128;          // 8 KiB: 64 rows x 128 bytes
 constexpr uint32_t kStage = kRegions * kReg; // 64 KiB key stage
 constexpr int kTcIdxCap = 2048;
@@ -58,8 +68,9 @@ constexpr uint32_t OFF_Q = 0;                              // 8 regions x (64 he
 constexpr uint32_t OFF_K = OFF_Q + kStage;                 // 2 stages x 8 regions x (64 keys x 128 B)
 constexpr uint32_t OFF_P = OFF_K + 2 * kStage;             // 2 stages x (64 keys x 128 B)
 constexpr uint32_t OFF_BAR = OFF_P + 2 * kReg;
-// barriers: kfull[2], kfree[2] (P V of the stage's tile done), sfull[2], sfree[2], pfull[2], ofull
-constexpr int BAR_KFULL = 0, BAR_KFREE = 2, BAR_SFULL = 4, BAR_SFREE = 6, BAR_PFULL = 8, BAR_OFULL = 10;
+// barriers: kfull[2], kfree[2] (P V of the stage's tile done), sfull[2], sfree[2], pfull[2], ofull, qfull
+constexpr int BAR_KFULL = 0, BAR_KFREE = 2, BAR_SFULL = 4, BAR_SFREE = 6, BAR_PFULL = 8, BAR_OFULL = 10,
+              BAR_QFULL = 11;
 constexpr uint32_t OFF_MISC = OFF_BAR + 16 * 8;
 constexpr uint32_t MISC_TMEM = 0, MISC_FLAG = 4, MISC_M = 32, MISC_L = MISC_M + 256, MISC_MN = MISC_L + 256,
                    MISC_AL = MISC_MN + 256, MISC_RMAX = MISC_AL + 256, MISC_RSUM = MISC_RMAX + 1024,
@@ -102,54 +113,67 @@ __device__ __forceinline__ void halfwarp_reduce32(const float *v, float &r0, flo
     r1 = a[1];
 }
 
-struct TcKeys {
-    const uint16_t *entries;   // the sequence's first entry row
-    const uint16_t *tail;      // first raw tail row
-    const int32_t *idx;        // sparse: the query's selection (shared or global memory)
-    int64_t n_vis;
-    int n_main, n_keys;
-};
-
-template <bool GATHER>
-__device__ __forceinline__ const uint16_t *tc_key_row(const TcKeys &ks, int slot)
+// L2 eviction policies: the compressed entries are read by many queries and
+// should stay in L2; each query's own rows (its query tile, its raw tail, its
+// output) are touched once and should leave first.
+__device__ __forceinline__ uint64_t policy_evict_last()
 {
-    if (slot < ks.n_main) {
-        if (GATHER) {
-            const int e = ks.idx[slot];
-            if (e < 0 || (int64_t)e >= ks.n_vis) return nullptr;
-            return ks.entries + (int64_t)e * kTcD;
-        }
-        return ks.entries + (int64_t)slot * kTcD;
-    }
-    if (slot < ks.n_keys) return ks.tail + (int64_t)(slot - ks.n_main) * kTcD;
-    return nullptr;
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
 }
 
-// Keys of the query at `p` (selected or visible entries, then the raw tail).
+// TMA loads into 128-byte swizzled shared memory, completing on `bar`, with
+// an L2 policy.  64 x box-rows tile at (column x, row y):
+__device__ __forceinline__ void tma_tile2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar,
+                                           uint64_t pol)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%2, %3}], [%4], %5;\n"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+                 : "memory");
+}
+// 16-byte cp.async (src_bytes < 16 zero-fills the rest) with an L2 policy.
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, int src_bytes, uint64_t pol)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes), "l"(pol)
+                 : "memory");
+}
+
+// Key tiles of the query at `p`: the main keys (selected or visible entries)
+// fill ceil(n_main / 64) tiles, the raw tail its own ceil(r / 64) tiles.
 template <bool GATHER>
-__device__ __forceinline__ int tc_key_count(const QueryPos &p, int ratio, int top_k)
+__device__ __forceinline__ int tc_tiles(const QueryPos &p, int ratio, int top_k, int *t_main)
 {
     const int64_t n_vis = (p.t + 1) / ratio;
     const int n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
-    return n_main + (int)((p.t + 1) % ratio);
+    const int r_tail = (int)((p.t + 1) % ratio);
+    const int tm = (n_main + kTcKeys - 1) / kTcKeys;
+    if (t_main) *t_main = tm;
+    return tm + (r_tail + kTcKeys - 1) / kTcKeys;
 }
 
 // A query with T key tiles runs in min(nsplit_max, T) splits; split s takes
 // tiles [s T / ns, (s + 1) T / ns).
-__device__ __forceinline__ int tc_nsplit(int n_keys, int nsplit_max)
-{
-    const int T = (n_keys + kTcKeys - 1) / kTcKeys;
-    return T < nsplit_max ? T : nsplit_max;
-}
+__device__ __forceinline__ int tc_nsplit(int T, int nsplit_max) { return T < nsplit_max ? T : nsplit_max; }
 
 template <bool GATHER>
 __global__ void __launch_bounds__(kTcThreads, 1)
-attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
-                 const int64_t *__restrict__ cu_ent, const uint16_t *__restrict__ q,
-                 const uint16_t *__restrict__ entries, const uint16_t *__restrict__ kv,
-                 const int32_t *__restrict__ idx, int H, int ratio, int top_k, float scale_log2, int max_kv_len,
-                 int nsplit_max, uint16_t *__restrict__ out, float *__restrict__ lse,
-                 float *__restrict__ part_o, float2 *__restrict__ part_ml, int *err)
+attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_ent_rows,
+                 const __grid_constant__ CUtensorMap map_kv,
+                 int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                 const int64_t *__restrict__ cu_ent, const uint16_t *__restrict__ entries,
+                 const int32_t *__restrict__ idx, int H,
+                 int ratio, int top_k, float scale_log2, int max_kv_len, int nsplit_max,
+                 uint16_t *__restrict__ out, float *__restrict__ lse, float *__restrict__ part_o,
+                 float2 *__restrict__ part_ml, int *err)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -169,20 +193,17 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
         if (tid == 0) set_error(err, CSA_ERR_DEVICE);
         return;
     }
-    TcKeys ks;
-    ks.entries = entries + p.e0 * kTcD;
-    ks.tail = kv + (p.kv0 + p.t - r_tail + 1) * kTcD;
-    ks.idx = GATHER ? idx + qi * top_k : nullptr;
-    ks.n_vis = n_vis;
-    ks.n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
-    ks.n_keys = ks.n_main + r_tail;
-    const int nsplit = tc_nsplit(ks.n_keys, nsplit_max);
+    const int n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
+    int T_main = 0;
+    const int T_all = tc_tiles<GATHER>(p, ratio, top_k, &T_main);
+    const int nsplit = tc_nsplit(T_all, nsplit_max);
     if (split >= nsplit) return;   // this query has fewer key tiles than splits
-    const int T_all = (ks.n_keys + kTcKeys - 1) / kTcKeys;
     const int t0 = (int)((int64_t)split * T_all / nsplit), t1 = (int)((int64_t)(split + 1) * T_all / nsplit);
-    const int key0 = t0 * kTcKeys;
-    const int key1 = min(ks.n_keys, t1 * kTcKeys);
     const int T = t1 - t0;
+    // main-key slots of this split (selection entries read here)
+    const int slot0 = min(t0, T_main) * kTcKeys;
+    const int slot1 = min(min(t1, T_main) * kTcKeys, n_main);
+    const int64_t tail_row0 = p.kv0 + p.t - r_tail + 1;
 
     const uint32_t bar0 = sb + OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -196,8 +217,9 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
     volatile int *s_flag = reinterpret_cast<volatile int *>(misc + MISC_FLAG);
 
     if (tid == 0) {
+        mbar_init(bar(BAR_QFULL), 1);
         for (int s = 0; s < 2; s++) {
-            mbar_init(bar(BAR_KFULL + s), kProd);
+            mbar_init(bar(BAR_KFULL + s), 1 + kGatherThreads);   // TMA issuer + cp.async gatherers
             mbar_init(bar(BAR_KFREE + s), 1);
             mbar_init(bar(BAR_SFULL + s), 1);
             mbar_init(bar(BAR_SFREE + s), 128);
@@ -216,63 +238,99 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + MISC_TMEM);
 
+    // the query tile is an input of the call: it loads while the kernels
+    // before this one finish
+    if (warp == 5 && lane == 0) {
+        mbar_expect_tx(bar(BAR_QFULL), kStage);
+        const int qrow = (int)(qi * H + (int64_t)hg * kTcHeads);
+        const uint64_t once = policy_evict_first();
+#pragma unroll
+        for (int r = 0; r < kRegions; r++)
+            tma_tile2d(sb + OFF_Q + r * kReg, &map_q, r * 64, qrow, bar(BAR_QFULL), once);
+    }
     // the selection and the entries come from earlier kernels
     griddep_wait();
-    if (GATHER) {   // this split's part of the selection
-        const int i1 = min(key1, ks.n_main);
-        if (i1 - key0 <= kTcIdxCap) {
-            int32_t *s_idx = reinterpret_cast<int32_t *>(sm + OFF_IDX);
-            for (int i = key0 + tid; i < i1; i += kTcThreads) s_idx[i - key0] = __ldg(ks.idx + i);
-            ks.idx = s_idx - key0;
-        }
-    }
+    // this split's part of the selection (slot1 - slot0 <= top_k <= kTcIdxCap)
+    int32_t *s_idx = reinterpret_cast<int32_t *>(sm + OFF_IDX);
+    if (GATHER)
+        for (int i = slot0 + tid; i < slot1; i += kTcThreads) s_idx[i - slot0] = __ldg(idx + qi * top_k + i);
     __syncthreads();
 
-    if (warp >= 5) {
-        // ------------------------------------------------------------ producers
-        // Group g (warps 5-7: g = 0, warps 8-10: g = 1) fills stage g with tiles
-        // g, g + 2, ...  Thread pt copies chunk pc (16 bytes) of rows pk0,
-        // pk0 + 12, ...: a warp moves four whole 128-byte row segments per
-        // instruction.
-        const int g = warp >= 8 ? 1 : 0;
-        const int pt = tid - kProdBase - g * kProd;
-        const int pc = pt & 7, pk0 = pt >> 3;
-        constexpr int RSTEP = kProd / 8;                          // 12 rows per pass
-        constexpr int KPP = (kTcKeys + RSTEP - 1) / RSTEP;        // 6 rows per thread
-        const uint32_t stage = sb + OFF_K + g * kStage;
-        bool ok = true;
-        for (int t = g; t < T && ok; t += 2) {
-            if (t >= 2 && !mbar_wait(bar(BAR_KFREE + g), (uint32_t)(((t - 2) >> 1) & 1))) {
-                set_error(err, CSA_ERR_TIMEOUT);
-                ok = false;
-                break;
-            }
-            if (t == 0) {   // the Q tile travels with the first key tile
-                const uint16_t *qrow = q + (qi * H + (int64_t)hg * kTcHeads) * kTcD;
-#pragma unroll
-                for (int i = 0; i < KPP; i++) {
-                    const int h = pk0 + RSTEP * i;
-                    if (h < kTcHeads)
+    if (warp == 5) {
+        // ------------------------------------------------------------ producer
+        // Tile tt of the split goes to stage tt & 1, once P V of tile tt - 2
+        // has released it.  Invalid selections read entry row 0 (the softmax
+        // masks them).
+        if (lane == 0) {
+            const uint64_t keep = policy_evict_last(), once = policy_evict_first();
+            int tt = 0;
+            for (; tt < T; tt++) {
+                const int g = tt & 1;
+                if (tt >= 2 && !mbar_wait(bar(BAR_KFREE + g), (uint32_t)(((tt - 2) >> 1) & 1))) {
+                    set_error(err, CSA_ERR_TIMEOUT);
+                    break;
+                }
+                const uint32_t stage = sb + OFF_K + g * kStage;
+                const uint32_t fb = bar(BAR_KFULL + g);
+                const int tile = t0 + tt;
+                mbar_expect_tx(fb, (GATHER && tile < T_main) ? 0u : kStage);   // selected entries: cp.async
+                if (tile < T_main) {
+                    if (!GATHER) {
+                        const int row = (int)(p.e0 + (int64_t)tile * kTcKeys);
 #pragma unroll
                         for (int r = 0; r < kRegions; r++)
-                            cp_async_16(sb + OFF_Q + r * kReg + h * 128 + ((pc ^ (h & 7)) << 4),
-                                        qrow + (int64_t)h * kTcD + r * 64 + pc * 8, 16);
+                            tma_tile2d(stage + r * kReg, &map_ent_rows, r * 64, row, fb, keep);
+                    }
+                } else {
+                    const int row = (int)(tail_row0 + (int64_t)(tile - T_main) * kTcKeys);
+#pragma unroll
+                    for (int r = 0; r < kRegions; r++) tma_tile2d(stage + r * kReg, &map_kv, r * 64, row, fb, once);
                 }
             }
-#pragma unroll
-            for (int i = 0; i < KPP; i++) {
-                const int k = pk0 + RSTEP * i;
-                if (k < kTcKeys) {
-                    const uint16_t *src = tc_key_row<GATHER>(ks, key0 + t * kTcKeys + k);
-#pragma unroll
-                    for (int r = 0; r < kRegions; r++)
-                        cp_async_16(stage + r * kReg + k * 128 + ((pc ^ (k & 7)) << 4),
-                                    src ? (const void *)(src + r * 64 + pc * 8) : (const void *)kv, src ? 16 : 0);
-                }
+            // no load may still be writing when the CTA ends (normally they
+            // have all been consumed): the last phase of each stage
+            for (int u = tt - 1; u >= 0 && u >= tt - 2; u--)
+                if (!mbar_wait(bar(BAR_KFULL + (u & 1)), (uint32_t)((u >> 1) & 1))) set_error(err, CSA_ERR_TIMEOUT);
+            if (!mbar_wait(bar(BAR_QFULL), 0)) set_error(err, CSA_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------ cp.async gatherers
+        // Thread pt copies 16-byte chunk pt % 8 of rows pt / 8, + 24, ... in
+        // every region of selected-entry tiles; every thread arrives on each
+        // tile's KFULL (after its own copies landed), whatever the tile.
+        const int pt = tid - kGatherBase;
+        const int pc = pt & 7, pk0 = pt >> 3;
+        constexpr int RSTEP = kGatherThreads / 8;                 // 24 rows per pass
+        constexpr int KPP = (kTcKeys + RSTEP - 1) / RSTEP;        // 3 rows per thread
+        const uint64_t keep = policy_evict_last();
+        for (int tt = 0; tt < T; tt++) {
+            const int g = tt & 1;
+            if (tt >= 2 && !mbar_wait(bar(BAR_KFREE + g), (uint32_t)(((tt - 2) >> 1) & 1))) {
+                set_error(err, CSA_ERR_TIMEOUT);
+                break;
             }
-            cp_async_commit();
-            cp_async_wait<0>();
-            tc::fence_proxy_async();
+            const int tile = t0 + tt;
+            if (GATHER && tile < T_main) {
+                const uint32_t stage = sb + OFF_K + g * kStage;
+#pragma unroll
+                for (int i = 0; i < KPP; i++) {
+                    const int k = pk0 + RSTEP * i;
+                    if (k < kTcKeys) {
+                        const int slot = tile * kTcKeys + k;
+                        const int e = slot < slot1 ? s_idx[slot - slot0] : -1;
+                        const bool v = e >= 0 && (int64_t)e < n_vis;
+                        const uint16_t *src = entries + (p.e0 + (v ? e : 0)) * kTcD;
+#pragma unroll
+                        for (int r = 0; r < kRegions; r++)
+                            cp_async_16_hint(stage + r * kReg + k * 128 + ((pc ^ (k & 7)) << 4), src + r * 64 + pc * 8,
+                                             v ? 16 : 0, keep);
+                    }
+                }
+                cp_async_commit();
+                cp_async_wait<0>();
+                tc::fence_proxy_async();
+            }
             mbar_arrive(bar(BAR_KFULL + g));
         }
         cp_async_wait<0>();
@@ -289,10 +347,10 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
             const uint64_t qb0 = tc::sdesc_sw128(sb + OFF_Q, 16, 1024);
             const uint64_t pa0 = tc::sdesc_sw128(sb + OFF_K, kReg, 1024);
             const uint64_t pb0 = tc::sdesc_sw128(sb + OFF_P, kReg, 1024);
-            bool ok = true;
+            bool ok = mbar_wait(bar(BAR_QFULL), 0);   // the query tile
             int nq = 0, np = 0;                       // next S tile, next PV tile
             uint64_t idle0 = global_ns();
-            while (np < T) {
+            while (ok && np < T) {
                 bool did = false;
                 if (nq < T && nq <= np + 1) {
                     const int sidx = nq & 1;
@@ -376,11 +434,18 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
                 const float other = __shfl_xor_sync(0xffffffffu, v[32 + j], 16);
                 s[j] = hh ? other : v[j];
             }
-            const int slot = key0 + t * kTcKeys + key;
-            bool valid = slot < ks.n_keys;
-            if (GATHER && valid && slot < ks.n_main) {
-                const int e = ks.idx[slot];
-                valid = e >= 0 && (int64_t)e < ks.n_vis;
+            const int tile = t0 + t;
+            bool valid;
+            if (tile < T_main) {
+                const int slot = tile * kTcKeys + key;
+                valid = slot < n_main;
+                if (GATHER && valid) {
+                    const int e = s_idx[slot - slot0];
+                    valid = e >= 0 && (int64_t)e < n_vis;
+                    if (e >= 0 && !valid) set_error(err, CSA_ERR_DEVICE);   // an index that is not visible
+                }
+            } else {
+                valid = (tile - T_main) * kTcKeys + key < r_tail;
             }
 #pragma unroll
             for (int j = 0; j < 32; j++) s[j] = valid ? s[j] * scale_log2 : -INFINITY;
@@ -410,9 +475,12 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
                 const float mn = s_mn[32 * hh + j];
                 s[j] = (mn == -INFINITY) ? 0.f : fast_exp2(s[j] - mn);
             }
-            // P V of the previous tile must be done: it read this P stage two
-            // tiles ago and the O^T columns are rescaled below
-            if (t >= 1 && !wait_all(BAR_KFREE + ((t - 1) & 1), (uint32_t)(((t - 1) >> 1) & 1))) {
+            // This P stage was last read by P V of tile t - 2, which must be done.
+            // A rescale of the O^T columns also needs P V of tile t - 1 done; the
+            // lazy maximum makes that rare, so P V of the previous tile usually
+            // still runs while this tile's probabilities are written.
+            if (rescale ? (t >= 1 && !wait_all(BAR_KFREE + ((t - 1) & 1), (uint32_t)(((t - 1) >> 1) & 1)))
+                        : (t >= 2 && !wait_all(BAR_KFREE + (t & 1), (uint32_t)(((t - 2) >> 1) & 1)))) {
                 ok = false;
                 break;
             }
@@ -497,7 +565,7 @@ attend_tc_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__
                 for (int j = 0; j < 32; j++) {
                     const float l = s_l[h0 + j];
                     const float inv = l > 0.f ? 1.f / l : 0.f;
-                    orow[(int64_t)(h0 + j) * kTcD + d] = (uint16_t)f32_to_bf16_bits(o[j] * inv);
+                    __stcs(orow + (int64_t)(h0 + j) * kTcD + d, (uint16_t)f32_to_bf16_bits(o[j] * inv));   // streaming
                 }
             }
             if (lse && tid < kTcHeads)
@@ -538,7 +606,7 @@ attend_tc_merge_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64
     const int head = blockIdx.y;
     const QueryPos p = query_pos(cu_kv, cu_q, cu_ent, batch, qi);
     if (p.t < 0 || p.t >= p.L || p.ne != p.L / ratio) return;   // reported by the attention kernel
-    const int nsplit = tc_nsplit(tc_key_count<GATHER>(p, ratio, top_k), nsplit_max);
+    const int nsplit = tc_nsplit(tc_tiles<GATHER>(p, ratio, top_k, nullptr), nsplit_max);
     if (nsplit <= 1) return;   // written by the attention kernel itself
     griddep_wait();            // the partial results are complete
     const int64_t base = (qi * (H / kTcHeads) + head / kTcHeads) * nsplit_max * kTcHeads + head % kTcHeads;
@@ -615,6 +683,38 @@ size_t tc_ws_bytes(const AttendArgs &a, const TcPlan &pl, float **part_o, float2
     return ml + slots * kTcD * sizeof(float);
 }
 
+// cuTensorMapEncodeTiled from the driver (looked up once).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// A [rows, 512] bf16 row-major matrix as a TMA source: boxes of 64 columns
+// (128 bytes, swizzled) by box_rows rows.
+cudaError_t rows_map(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 f = encode_fn();
+    if (!f) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)kTcD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kTcD * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <bool GATHER>
 cudaError_t launch_tc(const AttendArgs &a, cudaStream_t st)
 {
@@ -626,10 +726,21 @@ cudaError_t launch_tc(const AttendArgs &a, cudaStream_t st)
     if ((int64_t)HG * pl.nsplit_max > 65535) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)a.total_q, (unsigned)(HG * pl.nsplit_max));
     const float scale_log2 = a.scale * 1.4426950408889634f;
-    cudaError_t e = launch_kernel(GATHER ? "sparse_attend" : "dense_attend", attend_tc_kernel<GATHER>, grid,
-                                  dim3(kTcThreads), kTcSmem, st, a.pdl, a.batch, a.cu_kv, a.cu_q, a.cu_ent, a.q,
-                                  a.entries, a.kv, a.idx, a.n_heads, a.ratio, a.top_k, scale_log2, a.max_kv_len,
-                                  pl.nsplit_max, a.out, a.lse, part_o, part_ml, a.err);
+    // Tensor maps: the query rows [total_q * H, 512], the entries and the raw
+    // KV rows, each in 64-row tiles.  With no entries at all the entry map
+    // points at the KV rows; no tile reads it then.
+    CUtensorMap m_q, m_ent_rows, m_kv;
+    const bool have_ent = a.entries != nullptr && a.n_ent_rows > 0;
+    const void *ent = have_ent ? (const void *)a.entries : (const void *)a.kv;
+    const int64_t ent_rows = have_ent ? a.n_ent_rows : a.n_kv_rows;
+    cudaError_t e = rows_map(&m_q, a.q, a.total_q * a.n_heads, 64);
+    if (e == cudaSuccess) e = rows_map(&m_ent_rows, ent, ent_rows, 64);
+    if (e == cudaSuccess) e = rows_map(&m_kv, a.kv, a.n_kv_rows, 64);
+    if (e != cudaSuccess) return e;
+    e = launch_kernel(GATHER ? "sparse_attend" : "dense_attend", attend_tc_kernel<GATHER>, grid, dim3(kTcThreads),
+                      kTcSmem, st, a.pdl, m_q, m_ent_rows, m_kv, a.batch, a.cu_kv, a.cu_q, a.cu_ent,
+                      static_cast<const uint16_t *>(ent), a.idx, a.n_heads, a.ratio, a.top_k, scale_log2, a.max_kv_len, pl.nsplit_max, a.out, a.lse,
+                      part_o, part_ml, a.err);
     if (e != cudaSuccess || pl.nsplit_max <= 1) return e;
     // The merge overlaps the attention's tail only on a dependent-launch chain
     // (a.pdl); otherwise its many small CTAs, launched early, would wait on
@@ -645,8 +756,10 @@ cudaError_t launch_tc(const AttendArgs &a, cudaStream_t st)
 
 bool attend_tc_applicable(const AttendArgs &a)
 {
+    // row coordinates of the TMA loads are 32-bit
     return a.d == kTcD && a.n_heads % kTcHeads == 0 && (a.idx == nullptr || a.top_k <= kTcIdxCap) &&
-           a.total_q <= 0x7fffffffLL;
+           a.total_q * a.n_heads < 0x7fffffffLL && a.n_kv_rows < 0x7fffffffLL && a.n_ent_rows < 0x7fffffffLL &&
+           encode_fn() != nullptr;
 }
 
 size_t attend_tc_workspace_bytes(const AttendArgs &a) { return tc_ws_bytes(a, tc_plan(a), nullptr, nullptr); }

@@ -138,6 +138,8 @@ struct AttendArgs {
     const int64_t *cu_kv, *cu_q, *cu_ent;
     const uint16_t *q, *entries, *kv;
     const int32_t *idx;   // sparse: [total_q, top_k]; dense: nullptr
+    int64_t n_ent_rows;   // rows of `entries` (all sequences)
+    int64_t n_kv_rows;    // rows of `kv` (all sequences)
     int n_heads, d, ratio, top_k;
     float scale;
     uint16_t *out;
