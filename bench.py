@@ -30,11 +30,19 @@ sys.path.insert(0, ROOT)
 METRIC = "CSA+HCA attention tokens/s at 64K–1M ctx; % of HBM / tensor-core roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM traffic per launch of the dominant kernel from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel name, with
-# the sha256 of the kernel's source file at capture time; a changed source
-# makes the figure stale and it is reported as null.
-NCU_TRAFFIC = {}
+# DRAM traffic per call of the dominant call from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum over the call's kernels),
+# keyed by (workload, call), with the sha256 of the sources at capture time;
+# a changed source makes the figure stale and it is reported as null.
+NCU_TRAFFIC = {
+    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,598,464 B read +
+    # index_select_kernel 1,353,216 B read, 0 B written (both captured calls alike)
+    ("decode_64k", "index_topk"): {
+        "bytes_per_launch": 34951680,
+        "sources": {"indexer.cu": "41b107f51effef0b23de6600aa151e8ce35c6609dfd9a6dbe27138e56637822c",
+                    "common.cuh": "c163a7f706451d39f03aab7a1b3d9ca5dd901eb0067e2031b1f8ae5268757c9d"},
+    },
+}
 
 
 def parse():
@@ -66,7 +74,7 @@ def load_peaks():
 def step_work(p):
     """Algorithmic bytes/flops of one hybrid step on problem p (dict from workloads)."""
     H, d, HI, dI, k, mC, mH = p["H"], p["d"], p["HI"], p["dI"], p["top_k"], p["mC"], p["mH"]
-    w = {"compress": 0, "index_scan": 0, "sparse_attend": 0, "dense_attend": 0}
+    w = {"compress": 0, "index_topk": 0, "sparse_attend": 0, "dense_attend": 0}
     flops = {"index": 0, "sparse": 0, "dense": 0}
     for L, nq in zip(p["lengths"], p["n_q"]):
         lo = L - nq
@@ -79,7 +87,7 @@ def step_work(p):
             nC, rC = (t + 1) // mC, (t + 1) % mC
             nH, rH = (t + 1) // mH, (t + 1) % mH
             sel = min(k, nC)
-            w["index_scan"] += 2 * (HI * dI + nC * dI) + 4 * k
+            w["index_topk"] += 2 * (HI * dI + nC * dI) + 4 * k
             w["sparse_attend"] += 2 * ((sel + rC) * d + 2 * H * d) + 4 * k + 4 * H
             w["dense_attend"] += 2 * ((nH + rH) * d + 2 * H * d) + 4 * H
             flops["index"] += 2 * dI * nC
@@ -94,7 +102,7 @@ def step_work_fast(p):
         return step_work(p)
     H, d, HI, dI, k, mC, mH = p["H"], p["d"], p["HI"], p["dI"], p["top_k"], p["mC"], p["mH"]
     import numpy as np
-    w = {"compress": 0, "index_scan": 0, "sparse_attend": 0, "dense_attend": 0}
+    w = {"compress": 0, "index_topk": 0, "sparse_attend": 0, "dense_attend": 0}
     flops = {"index": 0, "sparse": 0, "dense": 0}
     for L, nq in zip(p["lengths"], p["n_q"]):
         lo = L - nq
@@ -105,7 +113,7 @@ def step_work_fast(p):
         n_blk_c, n_blk_h = L // mC - lo // mC, L // mH - lo // mH
         tok = max(n_blk_c * mC, n_blk_h * mH)
         w["compress"] += 2 * d * tok + 4 * tok + 2 * d * (n_blk_c + n_blk_h)
-        w["index_scan"] += int((2 * (HI * dI + nC * dI) + 4 * k).sum())
+        w["index_topk"] += int((2 * (HI * dI + nC * dI) + 4 * k).sum())
         w["sparse_attend"] += int((2 * ((sel + rC) * d + 2 * H * d) + 4 * k + 4 * H).sum())
         w["dense_attend"] += int((2 * ((nH + rH) * d + 2 * H * d) + 4 * H).sum())
         flops["index"] += int((2 * dI * nC).sum())
@@ -373,7 +381,7 @@ def main():
     tokens_per_step = sum(p["n_q"])
     value = tokens_per_step * world / (ms_step * 1e-3)
 
-    # per-kernel durations: an instrumented eager pass (events on each launch's stream)
+    # launches inside the step: an instrumented eager pass counts them per kernel
     csa.timing_reset()
     csa.timing_enable(True)
     for i in range(args.steps):
@@ -384,49 +392,95 @@ def main():
     csa.timing_reset()
     launches_per_step = sum(n for n, _ in kt.values()) / args.steps
 
+    # per-call durations: each C-ABI call of the step alone, back to back over
+    # the rotating copies in one CUDA graph (no host gaps), CUDA events around
+    # the replays on the capturing stream
+    calls = {
+        "compress": lambda h: (csa.csa_compress(layout, h.kv, h.gate, h.csa_cache),
+                               csa.hca_compress(layout, h.kv, h.gate, h.hca_cache)),
+        "index_topk": lambda h: csa.lightning_index_topk(layout, h.q_idx, h.k_idx, w.top_k, idx_out=h.idx,
+                                                         with_scores=False, ws=ws_idx[id(h)]),
+        "sparse_attend": lambda h: csa.sparse_mqa_attend(layout, h.q, h.csa_cache, h.kv, h.idx, w.top_k, w.scale,
+                                                         out=h.o_csa, lse=h.lse_csa, ws=ws_sp[id(h)]),
+        "dense_attend": lambda h: csa.hca_dense_attend(layout, h.q, h.hca_cache, h.kv, w.scale, out=h.o_hca,
+                                                       lse=h.lse_hca, ws=ws_de[id(h)]),
+    }
+    ws_idx, ws_sp, ws_de = {}, {}, {}
+    for h in copies:
+        ws_idx[id(h)] = torch.zeros(max(1, csa.index_workspace_size(layout, w.HI, w.dI, w.top_k)), dtype=torch.uint8,
+                                    device=dev)
+        ws_sp[id(h)] = torch.zeros(max(1, csa.attend_workspace_size(layout, w.H, w.d, w.mC, w.top_k)),
+                                   dtype=torch.uint8, device=dev)
+        ws_de[id(h)] = torch.zeros(max(1, csa.attend_workspace_size(layout, w.H, w.d, w.mH, 0)), dtype=torch.uint8,
+                                   device=dev)
+    call_us = {}
+    for name, fn in calls.items():
+        for h in copies:   # warm
+            fn(h)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for h in copies:
+                fn(h)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps_c = 1
+        while True:
+            e0.record()
+            for _ in range(reps_c):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            if ms >= 20.0 or reps_c >= 4096:
+                break
+            reps_c *= 4
+        call_us[name] = ms * 1e3 / (reps_c * ncopies)
+    assert csa.check_device_error() == 0
+
     work, flops = step_work_fast(p)
-    kernel_bytes = {"compress": work["compress"], "index_scan": work["index_scan"],
-                    "sparse_attend": work["sparse_attend"], "dense_attend": work["dense_attend"]}
     kernels = {}
-    for name, (n, ms) in kt.items():
-        per_launch = ms / n
-        per_step_launches = n / args.steps
-        entry = {"launches_per_step": per_step_launches, "avg_us": per_launch * 1e3}
-        if name in kernel_bytes and per_step_launches > 0:
-            b = kernel_bytes[name] / per_step_launches
-            entry["alg_bytes_per_launch"] = b
-            entry["alg_GBps"] = b / (per_launch * 1e-3) / 1e9
+    for name, us in call_us.items():
+        entry = {"avg_us": us, "kernels": sorted(k for k in kt if k.split("_")[0] in name.split("_")[0] or
+                                                  (name == "index_topk" and k.startswith("index")))}
+        entry["alg_bytes"] = work[name]
+        entry["alg_GBps"] = work[name] / (us * 1e-6) / 1e9
+        fl = {"sparse_attend": flops["sparse"], "dense_attend": flops["dense"], "index_topk": flops["index"]}.get(name)
+        if fl:
+            entry["alg_TFLOPs"] = fl / (us * 1e-6) / 1e12
         kernels[name] = entry
+    kernels["launches_per_step"] = {k: n / args.steps for k, (n, _) in kt.items()}
     step_bytes = sum(work.values())
     step_flops = sum(flops.values())
 
-    # dominant kernel and its roofline
-    dom = max(kt.items(), key=lambda kv: kv[1][1])[0]
-    n_dom, ms_dom = kt[dom]
-    avg_dom_s = ms_dom / n_dom * 1e-3
+    # dominant call and its roofline: HBM-bound for decode (bytes), tensor-bound
+    # for prefill attention (flops)
+    dom = max(call_us, key=lambda k: call_us[k])
+    avg_dom_s = call_us[dom] * 1e-6
     if w.decode or dom not in ("sparse_attend", "dense_attend"):
-        if dom in kernel_bytes:
-            alg = kernel_bytes[dom] / (n_dom / args.steps)
-        else:
-            alg = 0.0
+        alg = work[dom]
         achieved = alg / avg_dom_s / 1e9
         peak = float(peaks["hbm_gbs"])
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": f"hbm_gbs ({peak_src})",
-                "alg_bytes_per_launch": alg}
+                "frac": achieved / peak, "peak_source": f"hbm_gbs ({peak_src})", "alg_bytes_per_launch": alg,
+                "avg_us": call_us[dom]}
     else:
-        fl = flops["sparse" if dom == "sparse_attend" else "dense"] / (n_dom / args.steps)
+        fl = flops["sparse" if dom == "sparse_attend" else "dense"]
         achieved = fl / avg_dom_s / 1e12
         peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_source": f"bf16_tflops_sustained ({peak_src})",
-                "alg_flops_per_launch": fl}
+                "alg_flops_per_launch": fl, "avg_us": call_us[dom]}
     traffic = None
-    t_rec = NCU_TRAFFIC.get(dom)
+    t_rec = NCU_TRAFFIC.get((w.name, dom))
     if t_rec:
-        src = os.path.join(ROOT, "compressed_sparse_attention_21_b300", "csrc", t_rec["source"])
-        if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest() == t_rec["sha256"]:
-            traffic = t_rec["bytes_per_launch"] * t_rec.get("scale", 1.0)
+        ok = all(os.path.exists(os.path.join(ROOT, "compressed_sparse_attention_21_b300", "csrc", f)) and
+                 hashlib.sha256(open(os.path.join(ROOT, "compressed_sparse_attention_21_b300", "csrc", f),
+                                     "rb").read()).hexdigest() == sha
+                 for f, sha in t_rec["sources"].items())
+        if ok:
+            traffic = t_rec["bytes_per_launch"]
     roof["traffic"] = traffic
 
     # whole-step roofline (context)
