@@ -656,6 +656,230 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
     griddep_wait();
 }
 
+// Shared memory of one select CTA.
+template <int NT>
+struct SelSmem {
+    uint32_t cand[kSelCandCta];   // this CTA's keys in the boundary bin
+    uint32_t ncand;               // read by the peers
+    uint32_t hist[2][256];        // fallback refinement histograms (read by the peers)
+    uint32_t tot[256];
+    uint32_t cnt[2];              // this CTA's (greater, equal) counts (read by the peers)
+    uint32_t off[2];
+    uint32_t coff[kSelCluster + 1];
+    uint32_t w[2 * (NT / 32) + 1];
+    uint32_t digit, above, bin;
+};
+
+// The select of one query by a cluster of kSelCluster CTAs (see the kernels
+// below).  On entry: big (4096 words of shared memory) holds the query's
+// summed histogram (it later holds the cluster's candidates),
+// ss.ncand is zero and a __syncthreads() has passed; thread t of cluster rank
+// r holds the keys seg0 .. seg0 + m - 1 of the row in key[0 .. m).  A
+// non-null ghist (the global histogram) is returned to zero.
+template <int NT, int KPT>
+__device__ __forceinline__ void select_core(SelSmem<NT> &ss, uint32_t *big, const uint32_t (&key)[KPT], int m, int64_t seg0,
+                                            uint32_t rank, int64_t n, int top_k, bool bad, uint32_t *ghist,
+                                            int32_t *idx_row, float *sc_row, int *err)
+{
+    constexpr int CL = kSelCluster;
+    constexpr int BPT = kHistBins / NT;                 // top-level bins per thread
+    static_assert(KPT % 4 == 0 && BPT % 4 == 0 && NT >= 256 && kHistBins % CL == 0, "select tiling");
+    static_assert(kSelCandTotal <= kHistBins, "the candidate list reuses the histogram stage");
+    static_assert(NT * KPT < 65536, "per-CTA counts are packed in 16 bits");
+    const int tid = threadIdx.x;
+    // thread t takes bins 4095 - BPT t - i, i < BPT (walked from the top bin down)
+    uint32_t hc[BPT], hsum = 0;
+#pragma unroll
+    for (int j = 0; j < BPT / 4; j++) {
+        const uint4 v = reinterpret_cast<const uint4 *>(big)[(kHistBins - BPT * (tid + 1)) / 4 + j];
+        hc[BPT - 1 - 4 * j] = v.x;
+        hc[BPT - 2 - 4 * j] = v.y;
+        hc[BPT - 3 - 4 * j] = v.z;
+        hc[BPT - 4 - 4 * j] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < BPT; i++) hsum += hc[i];
+    const uint32_t k_eff = (uint32_t)(n < top_k ? n : top_k);
+    // level 1: the 12-bit bin that holds the k-th largest key
+    uint32_t tot;
+    const uint32_t excl = block_scan<NT>(hsum, ss.w, tot);
+    if (k_eff > 0 && excl < k_eff && k_eff <= excl + hsum) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int i = 0; i < BPT; i++) {
+            if (acc + hc[i] >= k_eff) {
+                ss.digit = (uint32_t)(kHistBins - 1 - BPT * tid - i);
+                ss.above = acc;
+                ss.bin = hc[i];
+                break;
+            }
+            acc += hc[i];
+        }
+    }
+    __syncthreads();
+    const bool partial = !bad && tot == (uint32_t)n && k_eff < (uint32_t)n;   // the boundary bin is split
+    const uint32_t b1 = ss.digit;
+    // this CTA's members of the boundary bin
+    if (partial) {
+#pragma unroll
+        for (int i = 0; i < KPT; i++) {
+            if (i < m && (key[i] >> 20) == b1) {
+                const uint32_t slot = atomicAdd(&ss.ncand, 1u);
+                if (slot < (uint32_t)kSelCandCta) ss.cand[slot] = key[i];
+            }
+        }
+    }
+    cluster_sync();   // the histogram has been read everywhere; candidate counts are published
+    if (ghist)
+        for (int i = (int)rank * (kHistBins / CL) + tid; i < (int)(rank + 1) * (kHistBins / CL); i += NT) ghist[i] = 0;
+    if (bad || tot != (uint32_t)n) {   // a layout error, or a chunk that did not land (reported by the scan)
+        if (bad && rank == 0 && tid == 0) set_error(err, CSA_ERR_DEVICE);
+        if (rank == 0) write_row_padding(idx_row, sc_row, 0, top_k);
+        cluster_sync();   // no CTA leaves while a peer may still read its counts
+        return;
+    }
+    // the k-th key kstar: keys above it are taken, keys equal to it lowest index first
+    uint32_t kstar = 0, need_eq = 0xffffffffu;   // default: every key (kstar = 0 is at or below all of them)
+    if (partial) {
+        uint32_t remaining = k_eff - ss.above;
+        if (tid < 32) {   // lane r reads rank r's count; a warp scan gives the offsets
+            const uint32_t c = tid < CL ? ld_cluster_u32(cluster_map(smem_u32(&ss.ncand), (uint32_t)tid)) : 0u;
+            uint32_t incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += v;
+            }
+            if (tid <= CL) ss.coff[tid] = incl - c;
+        }
+        __syncthreads();
+        bool fits = ss.coff[CL] <= (uint32_t)kSelCandTotal;
+        for (int r = 0; r < CL; r++) fits = fits && ss.coff[r + 1] - ss.coff[r] <= (uint32_t)kSelCandCta;
+        uint32_t prefix = b1 << 20, pmask = 0xfff00000u;
+        bool whole = ss.bin == remaining;   // the boundary bin is taken whole
+        if (!whole && fits) {
+            // gather the cluster's boundary-bin keys, then refine them here
+            // 8 + 8 + 4 bits at a time (every CTA reaches the same answer)
+            const uint32_t total = ss.coff[CL];
+            uint32_t *all = big;
+            for (uint32_t i = tid; i < total; i += NT) {
+                int r = 0;
+                while (i >= ss.coff[r + 1]) r++;
+                all[i] = ld_cluster_u32(cluster_map(smem_u32(ss.cand + (i - ss.coff[r])), (uint32_t)r));
+            }
+#pragma unroll 1
+            for (int level = 0; level < 3 && !whole; level++) {
+                const int sh = level == 0 ? 12 : (level == 1 ? 4 : 0);
+                const uint32_t dm = level == 2 ? 0xfu : 0xffu;
+                for (int i = tid; i < 256; i += NT) ss.tot[i] = 0;
+                __syncthreads();
+                for (uint32_t i = tid; i < total; i += NT) {
+                    const uint32_t k = all[i];
+                    if ((k & pmask) == prefix) atomicAdd(&ss.tot[(k >> sh) & dm], 1u);
+                }
+                __syncthreads();
+                if (tid < 32) find_digit_256(ss.tot, remaining, &ss.digit, &ss.above);
+                __syncthreads();
+                remaining -= ss.above;
+                prefix |= ss.digit << sh;
+                pmask |= dm << sh;
+                whole = ss.tot[ss.digit] == remaining;
+                __syncthreads();   // ss.digit, ss.above and ss.tot are rewritten by the next level
+            }
+        } else if (!whole) {
+            // many members (heavy ties): the same refinement over the keys in
+            // registers, the CTAs' histograms summed through distributed shared memory
+#pragma unroll 1
+            for (int level = 0; level < 3 && !whole; level++) {
+                const int sh = level == 0 ? 12 : (level == 1 ? 4 : 0);
+                const uint32_t dm = level == 2 ? 0xfu : 0xffu;
+                uint32_t *h = ss.hist[level & 1];
+                for (int i = tid; i < 256; i += NT) h[i] = 0;
+                __syncthreads();
+#pragma unroll
+                for (int i = 0; i < KPT; i++)
+                    if (i < m && (key[i] & pmask) == prefix) atomicAdd(&h[(key[i] >> sh) & dm], 1u);
+                cluster_sync();
+                if (tid < 256) {
+                    const uint32_t a = smem_u32(h + tid);
+                    uint32_t t = 0;
+#pragma unroll
+                    for (int r = 0; r < CL; r++) t += ld_cluster_u32(cluster_map(a, (uint32_t)r));
+                    ss.tot[tid] = t;
+                }
+                __syncthreads();
+                if (tid < 32) find_digit_256(ss.tot, remaining, &ss.digit, &ss.above);
+                __syncthreads();
+                remaining -= ss.above;
+                prefix |= ss.digit << sh;
+                pmask |= dm << sh;
+                whole = ss.tot[ss.digit] == remaining;
+                __syncthreads();   // ss.digit, ss.above and ss.tot are rewritten by the next level
+            }
+        }
+        // whole: every key at or above `prefix` (its lower bits zero) is taken
+        kstar = prefix;
+        need_eq = whole ? 0xffffffffu : remaining;
+    }
+    // ordered emission: a thread's keys are contiguous in index order, and the
+    // CTAs of the cluster hold consecutive segments
+    uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int i = 0; i < KPT; i++) {
+        n_gt += (i < m && key[i] > kstar) ? 1u : 0u;
+        n_eq += (i < m && key[i] == kstar) ? 1u : 0u;
+    }
+    uint32_t t_both;   // (greater, equal) counts packed 16 + 16 bits: at most NT * KPT <= 65536 keys per CTA
+    const uint32_t both_before = block_scan<NT>((n_eq << 16) | n_gt, ss.w, t_both);
+    const uint32_t gt_before = both_before & 0xffffu, eq_before = both_before >> 16;
+    if (tid == 0) {
+        ss.cnt[0] = t_both & 0xffffu;
+        ss.cnt[1] = t_both >> 16;
+    }
+    cluster_sync();
+    if (tid < 32) {   // lane r < rank reads rank r's counts
+        uint32_t g = 0, e = 0;
+        if ((uint32_t)tid < rank) {
+            g = ld_cluster_u32(cluster_map(smem_u32(ss.cnt), (uint32_t)tid));
+            e = ld_cluster_u32(cluster_map(smem_u32(ss.cnt + 1), (uint32_t)tid));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            e += __shfl_xor_sync(0xffffffffu, e, o);
+        }
+        if (tid == 0) {
+            ss.off[0] = g;
+            ss.off[1] = e;
+        }
+    }
+    cluster_arrive();   // this CTA reads no peer from here on (waited for at the end)
+    // The attention after this kernel may launch now (it waits for this grid
+    // on the device).  Triggered this late so that its CTAs do not sit on SMs
+    // the concurrent dense branch could use.
+    griddep_launch();
+    __syncthreads();
+    const uint32_t eq0 = ss.off[1] + eq_before;
+    uint32_t pos = ss.off[0] + gt_before + (eq0 < need_eq ? eq0 : need_eq);
+    uint32_t eq_rank = eq0;
+#pragma unroll
+    for (int i = 0; i < KPT; i++) {
+        if (i >= m) continue;
+        bool take = key[i] > kstar;
+        if (key[i] == kstar) take = eq_rank++ < need_eq;
+        if (take) {
+            if (pos < (uint32_t)top_k) {
+                idx_row[pos] = (int32_t)(seg0 + i);
+                if (sc_row) sc_row[pos] = key_score(key[i]);
+            }
+            pos++;
+        }
+    }
+    if (rank == 0) write_row_padding(idx_row, sc_row, (int)k_eff, top_k);
+    if (rank == CL - 1 && tid == NT - 1 && pos != k_eff) set_error(err, CSA_ERR_DEVICE);
+    cluster_wait();   // the peers have read this CTA's counts and candidates
+}
+
 template <int NT, int KPT>
 __global__ void __launch_bounds__(NT, 1)
 index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
@@ -663,27 +887,15 @@ index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
                     int32_t *__restrict__ idx_out, float *__restrict__ score_out, int *err)
 {
     constexpr int CL = kSelCluster;
-    constexpr int BPT = kHistBins / NT;                 // top-level bins per thread
-    static_assert(KPT % 4 == 0 && BPT % 4 == 0 && NT >= 256 && kHistBins % CL == 0, "select tiling");
-    static_assert(kSelCandTotal * 8 <= kHistBins * 4, "the candidate list reuses the histogram stage");
-    __shared__ __align__(16) uint32_t s_big[kHistBins];   // the histogram, then the cluster's candidates
-    __shared__ uint32_t s_cand[kSelCandCta];              // this CTA's keys in the boundary bin
-    __shared__ uint32_t s_ncand;                          // read by the peers
-    __shared__ uint32_t s_hist[2][256];                   // fallback refinement histograms (read by the peers)
-    __shared__ uint32_t s_tot[256];
-    __shared__ uint32_t s_cnt[2];                         // this CTA's (greater, equal) counts (read by the peers)
-    __shared__ uint32_t s_off[2];
-    __shared__ uint32_t s_coff[CL + 1];
-    __shared__ uint32_t s_w[2 * (NT / 32) + 1];
-    __shared__ uint32_t s_digit, s_above, s_bin;
+    __shared__ __align__(16) SelSmem<NT> ss;
+    __shared__ __align__(16) uint32_t s_big[kHistBins];
 
     const int tid = threadIdx.x;
     const uint32_t rank = cluster_rank();
     const int64_t qg = blockIdx.y;
     const int64_t qi = q_begin + qg;
     const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);   // layout arrays: inputs of the call
-    if (tid == 0) s_ncand = 0;
-    static_assert(NT * KPT < 65536, "per-CTA counts are packed in 16 bits");
+    if (tid == 0) ss.ncand = 0;
     griddep_wait();   // every chunk's keys and histogram counts are in place
     const int64_t n = (p.t + 1) / ratio;
     int32_t *idx_row = idx_out + qi * top_k;
@@ -709,196 +921,7 @@ index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
     for (int i = tid; i < kHistBins / 4; i += NT)
         reinterpret_cast<uint4 *>(s_big)[i] = bad ? make_uint4(0, 0, 0, 0) : __ldcg(reinterpret_cast<const uint4 *>(ghist) + i);
     __syncthreads();
-    // thread t takes bins 4095 - BPT t - i, i < BPT (walked from the top bin down)
-    uint32_t hc[BPT], hsum = 0;
-#pragma unroll
-    for (int j = 0; j < BPT / 4; j++) {
-        const uint4 v = reinterpret_cast<const uint4 *>(s_big)[(kHistBins - BPT * (tid + 1)) / 4 + j];
-        hc[BPT - 1 - 4 * j] = v.x;
-        hc[BPT - 2 - 4 * j] = v.y;
-        hc[BPT - 3 - 4 * j] = v.z;
-        hc[BPT - 4 - 4 * j] = v.w;
-    }
-#pragma unroll
-    for (int i = 0; i < BPT; i++) hsum += hc[i];
-    const uint32_t k_eff = (uint32_t)(n < top_k ? n : top_k);
-    // level 1: the 12-bit bin that holds the k-th largest key
-    uint32_t tot;
-    const uint32_t excl = block_scan<NT>(hsum, s_w, tot);
-    if (k_eff > 0 && excl < k_eff && k_eff <= excl + hsum) {
-        uint32_t acc = excl;
-#pragma unroll
-        for (int i = 0; i < BPT; i++) {
-            if (acc + hc[i] >= k_eff) {
-                s_digit = (uint32_t)(kHistBins - 1 - BPT * tid - i);
-                s_above = acc;
-                s_bin = hc[i];
-                break;
-            }
-            acc += hc[i];
-        }
-    }
-    __syncthreads();
-    const bool partial = !bad && tot == (uint32_t)n && k_eff < (uint32_t)n;   // the boundary bin is split
-    const uint32_t b1 = s_digit;
-    // this CTA's members of the boundary bin
-    if (partial) {
-#pragma unroll
-        for (int i = 0; i < KPT; i++) {
-            if (i < m && (key[i] >> 20) == b1) {
-                const uint32_t slot = atomicAdd(&s_ncand, 1u);
-                if (slot < (uint32_t)kSelCandCta) s_cand[slot] = key[i];
-            }
-        }
-    }
-    cluster_sync();   // the histogram has been read everywhere; candidate counts are published
-    for (int i = (int)rank * (kHistBins / CL) + tid; i < (int)(rank + 1) * (kHistBins / CL); i += NT) ghist[i] = 0;
-    if (bad || tot != (uint32_t)n) {   // a layout error, or a chunk that did not land (reported by the scan)
-        if (bad && rank == 0 && tid == 0) set_error(err, CSA_ERR_DEVICE);
-        if (rank == 0) write_row_padding(idx_row, sc_row, 0, top_k);
-        cluster_sync();   // no CTA leaves while a peer may still read its counts
-        return;
-    }
-    // the k-th key kstar: keys above it are taken, keys equal to it lowest index first
-    uint32_t kstar = 0, need_eq = 0xffffffffu;   // default: every key (kstar = 0 is at or below all of them)
-    if (partial) {
-        uint32_t remaining = k_eff - s_above;
-        if (tid < 32) {   // lane r reads rank r's count; a warp scan gives the offsets
-            const uint32_t c = tid < CL ? ld_cluster_u32(cluster_map(smem_u32(&s_ncand), (uint32_t)tid)) : 0u;
-            uint32_t incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (tid >= o) incl += v;
-            }
-            if (tid <= CL) s_coff[tid] = incl - c;
-        }
-        __syncthreads();
-        bool fits = s_coff[CL] <= (uint32_t)kSelCandTotal;
-        for (int r = 0; r < CL; r++) fits = fits && s_coff[r + 1] - s_coff[r] <= (uint32_t)kSelCandCta;
-        uint32_t prefix = b1 << 20, pmask = 0xfff00000u;
-        bool whole = s_bin == remaining;   // the boundary bin is taken whole
-        if (!whole && fits) {
-            // gather the cluster's boundary-bin keys, then refine them here
-            // 8 + 8 + 4 bits at a time (every CTA reaches the same answer)
-            const uint32_t total = s_coff[CL];
-            uint32_t *all = s_big;
-            for (uint32_t i = tid; i < total; i += NT) {
-                int r = 0;
-                while (i >= s_coff[r + 1]) r++;
-                all[i] = ld_cluster_u32(cluster_map(smem_u32(s_cand + (i - s_coff[r])), (uint32_t)r));
-            }
-#pragma unroll 1
-            for (int level = 0; level < 3 && !whole; level++) {
-                const int sh = level == 0 ? 12 : (level == 1 ? 4 : 0);
-                const uint32_t dm = level == 2 ? 0xfu : 0xffu;
-                for (int i = tid; i < 256; i += NT) s_tot[i] = 0;
-                __syncthreads();
-                for (uint32_t i = tid; i < total; i += NT) {
-                    const uint32_t k = all[i];
-                    if ((k & pmask) == prefix) atomicAdd(&s_tot[(k >> sh) & dm], 1u);
-                }
-                __syncthreads();
-                if (tid < 32) find_digit_256(s_tot, remaining, &s_digit, &s_above);
-                __syncthreads();
-                remaining -= s_above;
-                prefix |= s_digit << sh;
-                pmask |= dm << sh;
-                whole = s_tot[s_digit] == remaining;
-                __syncthreads();   // s_digit, s_above and s_tot are rewritten by the next level
-            }
-        } else if (!whole) {
-            // many members (heavy ties): the same refinement over the keys in
-            // registers, the CTAs' histograms summed through distributed shared memory
-#pragma unroll 1
-            for (int level = 0; level < 3 && !whole; level++) {
-                const int sh = level == 0 ? 12 : (level == 1 ? 4 : 0);
-                const uint32_t dm = level == 2 ? 0xfu : 0xffu;
-                uint32_t *h = s_hist[level & 1];
-                for (int i = tid; i < 256; i += NT) h[i] = 0;
-                __syncthreads();
-#pragma unroll
-                for (int i = 0; i < KPT; i++)
-                    if (i < m && (key[i] & pmask) == prefix) atomicAdd(&h[(key[i] >> sh) & dm], 1u);
-                cluster_sync();
-                if (tid < 256) {
-                    const uint32_t a = smem_u32(h + tid);
-                    uint32_t t = 0;
-#pragma unroll
-                    for (int r = 0; r < CL; r++) t += ld_cluster_u32(cluster_map(a, (uint32_t)r));
-                    s_tot[tid] = t;
-                }
-                __syncthreads();
-                if (tid < 32) find_digit_256(s_tot, remaining, &s_digit, &s_above);
-                __syncthreads();
-                remaining -= s_above;
-                prefix |= s_digit << sh;
-                pmask |= dm << sh;
-                whole = s_tot[s_digit] == remaining;
-                __syncthreads();   // s_digit, s_above and s_tot are rewritten by the next level
-            }
-        }
-        // whole: every key at or above `prefix` (its lower bits zero) is taken
-        kstar = prefix;
-        need_eq = whole ? 0xffffffffu : remaining;
-    }
-    // ordered emission: a thread's keys are contiguous in index order, and the
-    // CTAs of the cluster hold consecutive segments
-    uint32_t n_gt = 0, n_eq = 0;
-#pragma unroll
-    for (int i = 0; i < KPT; i++) {
-        n_gt += (i < m && key[i] > kstar) ? 1u : 0u;
-        n_eq += (i < m && key[i] == kstar) ? 1u : 0u;
-    }
-    uint32_t t_both;   // (greater, equal) counts packed 16 + 16 bits: at most NT * KPT <= 65536 keys per CTA
-    const uint32_t both_before = block_scan<NT>((n_eq << 16) | n_gt, s_w, t_both);
-    const uint32_t gt_before = both_before & 0xffffu, eq_before = both_before >> 16;
-    if (tid == 0) {
-        s_cnt[0] = t_both & 0xffffu;
-        s_cnt[1] = t_both >> 16;
-    }
-    cluster_sync();
-    if (tid < 32) {   // lane r < rank reads rank r's counts
-        uint32_t g = 0, e = 0;
-        if ((uint32_t)tid < rank) {
-            g = ld_cluster_u32(cluster_map(smem_u32(s_cnt), (uint32_t)tid));
-            e = ld_cluster_u32(cluster_map(smem_u32(s_cnt + 1), (uint32_t)tid));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            g += __shfl_xor_sync(0xffffffffu, g, o);
-            e += __shfl_xor_sync(0xffffffffu, e, o);
-        }
-        if (tid == 0) {
-            s_off[0] = g;
-            s_off[1] = e;
-        }
-    }
-    cluster_arrive();   // this CTA reads no peer from here on (waited for at the end)
-    // The attention after this kernel may launch now (it waits for this grid
-    // on the device).  Triggered this late so that its CTAs do not sit on SMs
-    // the concurrent dense branch could use.
-    griddep_launch();
-    __syncthreads();
-    const uint32_t eq0 = s_off[1] + eq_before;
-    uint32_t pos = s_off[0] + gt_before + (eq0 < need_eq ? eq0 : need_eq);
-    uint32_t eq_rank = eq0;
-#pragma unroll
-    for (int i = 0; i < KPT; i++) {
-        if (i >= m) continue;
-        bool take = key[i] > kstar;
-        if (key[i] == kstar) take = eq_rank++ < need_eq;
-        if (take) {
-            if (pos < (uint32_t)top_k) {
-                idx_row[pos] = (int32_t)(seg0 + i);
-                if (sc_row) sc_row[pos] = key_score(key[i]);
-            }
-            pos++;
-        }
-    }
-    if (rank == 0) write_row_padding(idx_row, sc_row, (int)k_eff, top_k);
-    if (rank == CL - 1 && tid == NT - 1 && pos != k_eff) set_error(err, CSA_ERR_DEVICE);
-    cluster_wait();   // the peers have read this CTA's counts and candidates
+    select_core<NT, KPT>(ss, s_big, key, m, seg0, rank, n, top_k, bad, ghist, idx_row, sc_row, err);
 }
 
 constexpr int64_t kSelMaxN = (int64_t)kSelCluster * 1024 * 32;   // longest row the select cluster holds (entries)
