@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--min-seconds", type=float, default=2.0, help="repeat the K-step region this long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="every sequence this long instead of the workload's lengths (smaller cases of the same "
+                         "shape, e.g. for a profiler capture); the JSON line then names the override")
     return ap.parse_args()
 
 
@@ -288,7 +291,7 @@ def main():
     csa.load()
 
     w = wl.WORKLOADS[args.workload]
-    p = wl.make_problem(w)                 # each rank serves its own batch of the same shape
+    p = wl.make_problem(w, lengths=[args.ctx] * w.batch if args.ctx > 0 else None)   # each rank: its own batch
     peaks, peak_src = load_peaks()
 
     # CPU baseline first (oracle threads run before heavy GPU work; rank 0 only, N=1 only)
@@ -553,6 +556,8 @@ def main():
 
     touched = step_bytes
     cfg = workload_config(w, p)
+    if args.ctx > 0:
+        cfg["ctx_override"] = args.ctx
     cfg["l2"] = (f"{ncopies} rotating copies of the step state; {touched / 2**20:.1f} MiB algorithmic per step, "
                  f"{ncopies * touched / 2**20:.0f} MiB per rotation vs 126 MB L2") if ncopies > 1 else \
         "inputs larger than L2"
