@@ -36,10 +36,10 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # a changed source makes the figure stale and it is reported as null.
 NCU_TRAFFIC = {
     # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,598,464 B read +
-    # index_select_kernel 1,353,216 B read, 0 B written (both captured calls alike)
+    # index_select_kernel 1,353,216 B read, 0 B written (means of two captured calls)
     ("decode_64k", "index_topk"): {
         "bytes_per_launch": 34951680,
-        "sources": {"indexer.cu": "41b107f51effef0b23de6600aa151e8ce35c6609dfd9a6dbe27138e56637822c",
+        "sources": {"indexer.cu": "097e045c8ea32cd43656e1c4dd5d2283f27fba368fbf9f390b1bd016040a7b0f",
                     "common.cuh": "c163a7f706451d39f03aab7a1b3d9ca5dd901eb0067e2031b1f8ae5268757c9d"},
     },
 }
