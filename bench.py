@@ -126,6 +126,25 @@ def step_work_fast(p):
 
 
 # ---------------------------------------------------------------------------
+# ranks: each serves its own batch (weak scaling, no collective on the data path)
+# ---------------------------------------------------------------------------
+def max_over_ranks(ms, device=None):
+    """The slowest rank's time (the job's time); the value itself on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(tokens_per_rank_step, world, ms_per_step):
+    """Whole-job tokens/s: every rank's tokens over the job's (max-over-ranks) step time."""
+    return tokens_per_rank_step * world / (ms_per_step * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
@@ -362,12 +381,7 @@ def main():
             copies[i]()
         e1.record()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms = float(tt.item())
-        return ms
+        return max_over_ranks(e0.elapsed_time(e1), dev)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -382,7 +396,7 @@ def main():
     ms_region = statistics.median(reps)
     ms_step = ms_region / args.steps
     tokens_per_step = sum(p["n_q"])
-    value = tokens_per_step * world / (ms_step * 1e-3)
+    value = job_value(tokens_per_step, world, ms_step)
 
     # launches inside the step: an instrumented eager pass counts them per kernel
     csa.timing_reset()
@@ -524,12 +538,7 @@ def main():
             run()
             e1.record()
             torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1)
-            if world > 1:
-                tt = torch.tensor([ms], device=dev)
-                dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-                ms = float(tt.item())
-            return ms
+            return max_over_ranks(e0.elapsed_time(e1), dev)
 
         # eager: one hybrid_attend call per step, host copies around it
         for i in range(3):
@@ -545,12 +554,12 @@ def main():
         torch.cuda.synchronize()
         full, rem = divmod(args.steps, ncopies)
         ms_graph = timed_e2e(lambda: ([g_e2e.replay() for _ in range(full)], [e2e_step(copies[i]) for i in range(rem)]))
-        e2e = {"value": tokens_per_step * world / (ms_graph / args.steps * 1e-3), "unit": "tokens/s",
+        e2e = {"value": job_value(tokens_per_step, world, ms_graph / args.steps), "unit": "tokens/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": ms_graph / args.steps,
                "path": "per step: pinned host q/q_idx copied in, hybrid_attend through the C ABI, both outputs "
                        "and LSEs copied out to pinned host memory; the step sequence captured once in a CUDA "
                        "graph and replayed",
-               "eager": {"value": tokens_per_step * world / (ms_eager / args.steps * 1e-3),
+               "eager": {"value": job_value(tokens_per_step, world, ms_eager / args.steps),
                          "ms_per_step": ms_eager / args.steps,
                          "path": "the same sequence issued eagerly from Python each step"}}
 
