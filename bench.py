@@ -32,14 +32,20 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 
 # DRAM traffic per call of the dominant call from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum over the call's kernels),
-# keyed by (workload, call), with the sha256 of the sources at capture time;
+# keyed by (workload, call, indexer key format), with the sha256 of the sources at capture time;
 # a changed source makes the figure stale and it is reported as null.
 NCU_TRAFFIC = {
-    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,598,464 B read +
-    # index_select_kernel 1,353,216 B read, 0 B written (means of two captured calls)
-    ("decode_64k", "index_topk"): {
-        "bytes_per_launch": 34951680,
-        "sources": {"indexer.cu": "097e045c8ea32cd43656e1c4dd5d2283f27fba368fbf9f390b1bd016040a7b0f",
+    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,598,080 B read +
+    # index_select_kernel 1,358,080 B read, 0 B written (means of two captured calls)
+    ("decode_64k", "index_topk", "bf16"): {
+        "bytes_per_launch": 34956160,
+        "sources": {"indexer.cu": "563ed062291771308c91427e0dc17ba4cb5e5736ed7159ffc026d3e048caddfa",
+                    "common.cuh": "c163a7f706451d39f03aab7a1b3d9ca5dd901eb0067e2031b1f8ae5268757c9d"},
+    },
+    # the same call on FP8 E4M3 keys: scan 17,879,296 B read + select 1,352,192 B read, 0 B written
+    ("decode_64k", "index_topk", "fp8"): {
+        "bytes_per_launch": 19231488,
+        "sources": {"indexer.cu": "563ed062291771308c91427e0dc17ba4cb5e5736ed7159ffc026d3e048caddfa",
                     "common.cuh": "c163a7f706451d39f03aab7a1b3d9ca5dd901eb0067e2031b1f8ae5268757c9d"},
     },
 }
@@ -56,6 +62,8 @@ def parse():
     ap.add_argument("--min-seconds", type=float, default=2.0, help="repeat the K-step region this long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--index-fp8", action="store_true",
+                    help="the indexer reads FP8 E4M3 keys with per-row scales (quantised once with the caches)")
     ap.add_argument("--ctx", type=int, default=0,
                     help="every sequence this long instead of the workload's lengths (smaller cases of the same "
                          "shape, e.g. for a profiler capture); the JSON line then names the override")
@@ -74,9 +82,15 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 # algorithmic work (bytes and flops) of one step, per kernel
 # ---------------------------------------------------------------------------
-def step_work(p):
+def index_key_bytes(p, fp8=False):
+    """Bytes of one indexer key: dI bf16 values, or dI E4M3 codes and an fp32 scale."""
+    return p["dI"] + 4 if fp8 else 2 * p["dI"]
+
+
+def step_work(p, fp8=False):
     """Algorithmic bytes/flops of one hybrid step on problem p (dict from workloads)."""
     H, d, HI, dI, k, mC, mH = p["H"], p["d"], p["HI"], p["dI"], p["top_k"], p["mC"], p["mH"]
+    kb = index_key_bytes(p, fp8)
     w = {"compress": 0, "index_topk": 0, "sparse_attend": 0, "dense_attend": 0}
     flops = {"index": 0, "sparse": 0, "dense": 0}
     for L, nq in zip(p["lengths"], p["n_q"]):
@@ -90,7 +104,7 @@ def step_work(p):
             nC, rC = (t + 1) // mC, (t + 1) % mC
             nH, rH = (t + 1) // mH, (t + 1) % mH
             sel = min(k, nC)
-            w["index_topk"] += 2 * (HI * dI + nC * dI) + 4 * k
+            w["index_topk"] += 2 * HI * dI + nC * kb + 4 * k
             w["sparse_attend"] += 2 * ((sel + rC) * d + 2 * H * d) + 4 * k + 4 * H
             w["dense_attend"] += 2 * ((nH + rH) * d + 2 * H * d) + 4 * H
             flops["index"] += 2 * dI * nC
@@ -99,11 +113,12 @@ def step_work(p):
     return w, flops
 
 
-def step_work_fast(p):
+def step_work_fast(p, fp8=False):
     """Closed-form version of step_work for prefill-sized problems (same counts)."""
     if sum(p["n_q"]) <= 4096:
-        return step_work(p)
+        return step_work(p, fp8)
     H, d, HI, dI, k, mC, mH = p["H"], p["d"], p["HI"], p["dI"], p["top_k"], p["mC"], p["mH"]
+    kb = index_key_bytes(p, fp8)
     import numpy as np
     w = {"compress": 0, "index_topk": 0, "sparse_attend": 0, "dense_attend": 0}
     flops = {"index": 0, "sparse": 0, "dense": 0}
@@ -116,7 +131,7 @@ def step_work_fast(p):
         n_blk_c, n_blk_h = L // mC - lo // mC, L // mH - lo // mH
         tok = max(n_blk_c * mC, n_blk_h * mH)
         w["compress"] += 2 * d * tok + 4 * tok + 2 * d * (n_blk_c + n_blk_h)
-        w["index_topk"] += int((2 * (HI * dI + nC * dI) + 4 * k).sum())
+        w["index_topk"] += int((2 * HI * dI + nC * kb + 4 * k).sum())
         w["sparse_attend"] += int((2 * ((sel + rC) * d + 2 * H * d) + 4 * k + 4 * H).sum())
         w["dense_attend"] += int((2 * ((nH + rH) * d + 2 * H * d) + 4 * H).sum())
         flops["index"] += int((2 * dI * nC).sum())
@@ -330,8 +345,10 @@ def main():
         if w.decode:   # caches hold every entry before the step (built by a prefill-shaped call)
             csa.csa_compress(full, t["kv"], t["gate"], csa_cache)
             csa.hca_compress(full, t["kv"], t["gate"], hca_cache)
+        # FP8 indexer keys live beside the caches, quantised when the entries are made
+        fp8 = csa.quantize_index_keys(full, t["kI"]) if args.index_fp8 else None
         h = csa.Hybrid(layout, t["kv"], t["gate"], t["qI"], t["kI"], t["q"], w.top_k, w.scale,
-                       csa_cache=csa_cache, hca_cache=hca_cache)
+                       csa_cache=csa_cache, hca_cache=hca_cache, k_idx_fp8=fp8)
         copies.append(h)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -415,8 +432,12 @@ def main():
     calls = {
         "compress": lambda h: (csa.csa_compress(layout, h.kv, h.gate, h.csa_cache),
                                csa.hca_compress(layout, h.kv, h.gate, h.hca_cache)),
-        "index_topk": lambda h: csa.lightning_index_topk(layout, h.q_idx, h.k_idx, w.top_k, idx_out=h.idx,
-                                                         with_scores=False, ws=ws_idx[id(h)]),
+        "index_topk": (lambda h: csa.lightning_index_topk_fp8(layout, h.q_idx, h.k_idx_fp8[0], h.k_idx_fp8[1],
+                                                              w.top_k, idx_out=h.idx, with_scores=False,
+                                                              ws=ws_idx[id(h)]))
+        if args.index_fp8 else
+        (lambda h: csa.lightning_index_topk(layout, h.q_idx, h.k_idx, w.top_k, idx_out=h.idx,
+                                            with_scores=False, ws=ws_idx[id(h)])),
         "sparse_attend": lambda h: csa.sparse_mqa_attend(layout, h.q, h.csa_cache, h.kv, h.idx, w.top_k, w.scale,
                                                          out=h.o_csa, lse=h.lse_csa, ws=ws_sp[id(h)]),
         "dense_attend": lambda h: csa.hca_dense_attend(layout, h.q, h.hca_cache, h.kv, w.scale, out=h.o_hca,
@@ -424,8 +445,9 @@ def main():
     }
     ws_idx, ws_sp, ws_de = {}, {}, {}
     for h in copies:
-        ws_idx[id(h)] = torch.zeros(max(1, csa.index_workspace_size(layout, w.HI, w.dI, w.top_k)), dtype=torch.uint8,
-                                    device=dev)
+        ws_n = (csa.index_fp8_workspace_size if args.index_fp8 else csa.index_workspace_size)(layout, w.HI, w.dI,
+                                                                                               w.top_k)
+        ws_idx[id(h)] = torch.zeros(max(1, ws_n), dtype=torch.uint8, device=dev)
         ws_sp[id(h)] = torch.zeros(max(1, csa.attend_workspace_size(layout, w.H, w.d, w.mC, w.top_k)),
                                    dtype=torch.uint8, device=dev)
         ws_de[id(h)] = torch.zeros(max(1, csa.attend_workspace_size(layout, w.H, w.d, w.mH, 0)), dtype=torch.uint8,
@@ -456,7 +478,7 @@ def main():
         call_us[name] = ms * 1e3 / (reps_c * ncopies)
     assert csa.check_device_error() == 0
 
-    work, flops = step_work_fast(p)
+    work, flops = step_work_fast(p, args.index_fp8)
     kernels = {}
     for name, us in call_us.items():
         entry = {"avg_us": us, "kernels": sorted(k for k in kt if k.split("_")[0] in name.split("_")[0] or
@@ -490,7 +512,7 @@ def main():
                 "frac": achieved / peak, "peak_source": f"bf16_tflops_sustained ({peak_src})",
                 "alg_flops_per_launch": fl, "avg_us": call_us[dom]}
     traffic = None
-    t_rec = NCU_TRAFFIC.get((w.name, dom))
+    t_rec = NCU_TRAFFIC.get((w.name, dom, "fp8" if args.index_fp8 else "bf16"))
     if t_rec:
         ok = all(os.path.exists(os.path.join(ROOT, "compressed_sparse_attention_21_b300", "csrc", f)) and
                  hashlib.sha256(open(os.path.join(ROOT, "compressed_sparse_attention_21_b300", "csrc", f),
@@ -567,13 +589,15 @@ def main():
     cfg = workload_config(w, p)
     if args.ctx > 0:
         cfg["ctx_override"] = args.ctx
+    cfg["index_keys"] = "fp8_e4m3 + fp32 row scale" if args.index_fp8 else "bf16"
     cfg["l2"] = (f"{ncopies} rotating copies of the step state; {touched / 2**20:.1f} MiB algorithmic per step, "
                  f"{ncopies * touched / 2**20:.0f} MiB per rotation vs 126 MB L2") if ncopies > 1 else \
         "inputs larger than L2"
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg, "roofline": roof,
+            "vs_baseline": None, "dtype": "bf16 (indexer keys fp8 e4m3)" if args.index_fp8 else "bf16",
+            "data": "synthetic", "config": cfg, "roofline": roof,
             "step_roofline": step_roof, "cpu_baseline": cpu_base, "e2e": e2e,
             "gpu_launches": int(round(launches_per_step * args.steps)), "launches_per_step": launches_per_step,
             "kernels": kernels, "clocks": clocks, "cache_build_ms": cache_build_ms,

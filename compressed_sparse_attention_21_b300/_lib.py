@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa.so")
 _lib = None
 
 CSA_SKIP_COMPRESS = 0x1
+CSA_INDEX_FP8 = 0x2
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size", 3: "workspace missing or too small",
           4: "CUDA error", 5: "device wait timed out", 6: "device-side layout or index error"}
 
@@ -43,12 +44,14 @@ class csa_hybrid_params(ctypes.Structure):
                 ("q", ctypes.c_void_p), ("csa_cache", ctypes.c_void_p), ("hca_cache", ctypes.c_void_p),
                 ("idx_out", ctypes.c_void_p), ("score_out", ctypes.c_void_p), ("o_csa", ctypes.c_void_p),
                 ("lse_csa", ctypes.c_void_p), ("o_hca", ctypes.c_void_p), ("lse_hca", ctypes.c_void_p),
-                ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+                ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t), ("k_idx_fp8", ctypes.c_void_p),
+                ("k_idx_scale", ctypes.c_void_p)]
 
 
 # Every symbol include/csa.h declares (checked by the CPU test suite).
 EXPORTS = ("csa_compress", "hca_compress", "lightning_index_topk", "csa_index_workspace_size",
-           "lightning_index_topk_static",
+           "lightning_index_topk_static", "csa_quantize_index_keys", "lightning_index_topk_fp8",
+           "csa_index_fp8_workspace_size",
            "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size", "hybrid_attend",
            "csa_workspace_size", "csa_workspace_init", "csa_status_string", "csa_check_device_error",
            "csa_version", "csa_timing_enable", "csa_timing_read", "csa_timing_reset")
@@ -70,6 +73,9 @@ def load():
     lib.lightning_index_topk.argtypes = [LP, P, P, I, I, I, I, P, P, P, Z, P]
     lib.csa_index_workspace_size.argtypes = [LP, I, I, I, I, ctypes.POINTER(Z)]
     lib.lightning_index_topk_static.argtypes = [LP, P, P, I, I, I, I, P, P, P]
+    lib.csa_quantize_index_keys.argtypes = [LP, P, I, P, P, P]
+    lib.lightning_index_topk_fp8.argtypes = [LP, P, P, P, I, I, I, I, P, P, P, Z, P]
+    lib.csa_index_fp8_workspace_size.argtypes = [LP, I, I, I, I, ctypes.POINTER(Z)]
     lib.sparse_mqa_attend.argtypes = [LP, P, P, P, P, I, I, I, I, F, P, P, P, Z, P]
     lib.hca_dense_attend.argtypes = [LP, P, P, P, I, I, I, F, P, P, P, Z, P]
     lib.csa_attend_workspace_size.argtypes = [LP, I, I, I, I, ctypes.POINTER(Z)]
@@ -86,7 +92,8 @@ def load():
     lib.csa_timing_read.restype = I
     lib.csa_timing_reset.restype = None
     for f in ("csa_compress", "hca_compress", "lightning_index_topk", "csa_index_workspace_size",
-              "lightning_index_topk_static", "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size",
+              "lightning_index_topk_static", "csa_quantize_index_keys", "lightning_index_topk_fp8",
+              "csa_index_fp8_workspace_size", "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size",
               "hybrid_attend",
               "csa_workspace_size", "csa_workspace_init", "csa_check_device_error", "csa_timing_enable"):
         getattr(lib, f).restype = I
@@ -208,6 +215,44 @@ def lightning_index_topk(layout, q_idx, k_idx, top_k, idx_out=None, score_out=No
     return idx_out, score_out
 
 
+def quantize_index_keys(layout, k_idx, k_fp8=None, k_scale=None, stream=None):
+    """E4M3 codes [total_csa, d_idx] (uint8) and per-row fp32 scales of the indexer keys."""
+    dev = k_idx.device
+    dI = k_idx.shape[-1]
+    if k_fp8 is None:
+        k_fp8 = torch.empty((layout.total_csa, dI), dtype=torch.uint8, device=dev)
+    if k_scale is None:
+        k_scale = torch.empty((layout.total_csa,), dtype=torch.float32, device=dev)
+    _check(load().csa_quantize_index_keys(ctypes.byref(layout.c), _ptr(k_idx), dI, _ptr(k_fp8), _ptr(k_scale),
+                                          _stream(stream)), "csa_quantize_index_keys")
+    return k_fp8, k_scale
+
+
+def index_fp8_workspace_size(layout, n_heads_idx, d_idx, top_k, ratio=None):
+    ratio = layout.ratio_csa if ratio is None else ratio
+    n = ctypes.c_size_t(0)
+    _check(load().csa_index_fp8_workspace_size(ctypes.byref(layout.c), n_heads_idx, d_idx, ratio, top_k,
+                                               ctypes.byref(n)), "csa_index_fp8_workspace_size")
+    return n.value
+
+
+def lightning_index_topk_fp8(layout, q_idx, k_fp8, k_scale, top_k, idx_out=None, score_out=None, ws=None,
+                             ratio=None, stream=None, with_scores=True):
+    """lightning_index_topk on E4M3 keys (see quantize_index_keys)."""
+    ratio = layout.ratio_csa if ratio is None else ratio
+    dev = q_idx.device
+    if idx_out is None:
+        idx_out = torch.empty((layout.total_q, top_k), dtype=torch.int32, device=dev)
+    if score_out is None and with_scores:
+        score_out = torch.empty((layout.total_q, top_k), dtype=torch.float32, device=dev)
+    HI, dI = q_idx.shape[-2], q_idx.shape[-1]
+    ws, nb = _ws(index_fp8_workspace_size(layout, HI, dI, top_k, ratio), dev, ws)
+    _check(load().lightning_index_topk_fp8(ctypes.byref(layout.c), _ptr(q_idx), _ptr(k_fp8), _ptr(k_scale), HI, dI,
+                                           ratio, top_k, _ptr(idx_out), _ptr(score_out), _ptr(ws), nb,
+                                           _stream(stream)), "lightning_index_topk_fp8")
+    return idx_out, score_out
+
+
 STATIC_SCRATCH_BYTES = 32 << 20   # CSA_INDEX_STATIC_SCRATCH_BYTES
 
 
@@ -272,7 +317,7 @@ class Hybrid:
     """One hybrid_attend problem: owns the parameter block and its buffers."""
 
     def __init__(self, layout, kv, gate, q_idx, k_idx, q, top_k, scale, csa_cache=None, hca_cache=None,
-                 skip_compress=False, with_scores=False, ws=None):
+                 skip_compress=False, with_scores=False, ws=None, k_idx_fp8=None):
         dev = q.device
         H, d = q.shape[-2], q.shape[-1]
         self.layout = layout
@@ -291,8 +336,14 @@ class Hybrid:
         p.layout = layout.c
         p.d, p.n_heads, p.n_heads_idx, p.d_idx = d, H, q_idx.shape[-2], q_idx.shape[-1]
         p.ratio_csa, p.ratio_hca, p.top_k = layout.ratio_csa, layout.ratio_hca, top_k
-        p.flags = CSA_SKIP_COMPRESS if skip_compress else 0
+        # k_idx_fp8: (codes, scales) from quantize_index_keys; the indexer then reads them
+        self.k_idx_fp8 = k_idx_fp8
+        self._fp8 = CSA_INDEX_FP8 if k_idx_fp8 is not None else 0
+        p.flags = (CSA_SKIP_COMPRESS if skip_compress else 0) | self._fp8
         p.scale = float(scale)
+        if k_idx_fp8 is not None:
+            p.k_idx_fp8 = _ptr(k_idx_fp8[0]).value
+            p.k_idx_scale = _ptr(k_idx_fp8[1]).value
         for name, t in (("kv", kv), ("gate", gate), ("q_idx", q_idx), ("k_idx", k_idx), ("q", q),
                         ("csa_cache", self.csa_cache), ("hca_cache", self.hca_cache), ("idx_out", self.idx),
                         ("score_out", self.score), ("o_csa", self.o_csa), ("lse_csa", self.lse_csa),
@@ -306,7 +357,7 @@ class Hybrid:
         self.params = p
 
     def set_flags(self, skip_compress):
-        self.params.flags = CSA_SKIP_COMPRESS if skip_compress else 0
+        self.params.flags = (CSA_SKIP_COMPRESS if skip_compress else 0) | self._fp8
 
     def __call__(self, stream=None):
         _check(load().hybrid_attend(ctypes.byref(self.params), _stream(stream)), "hybrid_attend")

@@ -144,6 +144,8 @@ IndexArgs index_args(const csa_layout *L, const csa_bf16 *q_idx, const csa_bf16 
     a.cu_csa = L->cu_csa;
     a.q_idx = q_idx;
     a.k_idx = k_idx;
+    a.k_fp8 = nullptr;
+    a.k_scale = nullptr;
     a.n_heads_idx = hi;
     a.d_idx = di;
     a.ratio = ratio;
@@ -201,6 +203,17 @@ csa_status_t check_index(const csa_layout *L, const csa_bf16 *q_idx, const csa_b
     if (L->total_q > 0 && !idx_out) return CSA_ERR_INVALID_ARG;
     if (score_out && (reinterpret_cast<uintptr_t>(score_out) & 3u)) return CSA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(idx_out) & 3u) return CSA_ERR_INVALID_ARG;
+    return CSA_OK;
+}
+
+// The FP8 indexer's key arrays (codes [total_csa, d_idx] bytes, scales
+// [total_csa] fp32) and its row-length limit.
+csa_status_t check_fp8_keys(const csa_layout *L, const uint8_t *k_fp8, const float *k_scale, int ratio)
+{
+    const bool any = L->total_csa > 0;
+    CSA_TRY(check_ptr(k_fp8, any));
+    if (any && (!k_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u))) return CSA_ERR_INVALID_ARG;
+    if (L->max_kv_len / ratio > index_fp8_max_n()) return CSA_ERR_UNSUPPORTED;
     return CSA_OK;
 }
 
@@ -293,7 +306,7 @@ size_t hybrid_ws_parts(const csa_hybrid_params *p, size_t *idx_ws, size_t *sp_ws
     sa.idx = reinterpret_cast<const int32_t *>(1);   // sparse plan
     AttendArgs ha = attend_args(L, false, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca,
                                 0, p->scale, nullptr, nullptr, nullptr, 0, nullptr, num_sms, sh_d);
-    *idx_ws = align_ws(index_workspace_bytes(ia));
+    *idx_ws = align_ws((p->flags & CSA_INDEX_FP8) ? index_fp8_workspace_bytes(ia) : index_workspace_bytes(ia));
     *sp_ws = align_ws(attend_workspace_bytes(sa));
     *hc_ws = align_ws(attend_workspace_bytes(ha));
     return *idx_ws + *sp_ws + *hc_ws;
@@ -339,6 +352,54 @@ csa_status_t hca_compress(const csa_layout *layout, const csa_bf16 *kv, const fl
                           csa_bf16 *out, csa_stream_t stream)
 {
     return compress_impl(layout, false, kv, gate, d, ratio, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+csa_status_t csa_quantize_index_keys(const csa_layout *layout, const csa_bf16 *k_idx, int d_idx, uint8_t *k_fp8,
+                                     float *k_scale, csa_stream_t stream)
+{
+    CSA_TRY(check_layout(layout, true, false));
+    if (d_idx != 32 && d_idx != 64 && d_idx != 128) return CSA_ERR_UNSUPPORTED;
+    const int64_t rows = layout->total_csa;
+    CSA_TRY(check_ptr(k_idx, rows > 0));
+    CSA_TRY(check_ptr(k_fp8, rows > 0));
+    if (rows > 0 && (!k_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u))) return CSA_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    return from_cuda(launch_quantize_index_keys(k_idx, rows, d_idx, k_fp8, k_scale,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status_t lightning_index_topk_fp8(const csa_layout *layout, const csa_bf16 *q_idx, const uint8_t *k_fp8,
+                                      const float *k_scale, int n_heads_idx, int d_idx, int ratio, int top_k,
+                                      int32_t *idx_out, float *score_out, void *ws, size_t ws_bytes,
+                                      csa_stream_t stream)
+{
+    CSA_TRY(check_index(layout, q_idx, reinterpret_cast<const csa_bf16 *>(k_fp8), n_heads_idx, d_idx, ratio, top_k,
+                        idx_out, score_out));
+    CSA_TRY(check_fp8_keys(layout, k_fp8, k_scale, ratio));
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    IndexArgs a = index_args(layout, q_idx, nullptr, n_heads_idx, d_idx, ratio, top_k, idx_out, score_out, ws,
+                             ws_bytes, ds->err);
+    a.k_fp8 = k_fp8;
+    a.k_scale = k_scale;
+    const size_t need = index_fp8_workspace_bytes(a);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return CSA_ERR_WORKSPACE;
+    return from_cuda(launch_index_topk(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status_t csa_index_fp8_workspace_size(const csa_layout *layout, int n_heads_idx, int d_idx, int ratio, int top_k,
+                                          size_t *bytes)
+{
+    if (!bytes) return CSA_ERR_INVALID_ARG;
+    CSA_TRY(check_layout(layout, true, false));
+    if (ratio <= 0 || top_k <= 0) return CSA_ERR_INVALID_ARG;
+    if (!index_supported(n_heads_idx, d_idx, top_k)) return CSA_ERR_UNSUPPORTED;
+    if (layout->max_kv_len / ratio > index_fp8_max_n()) return CSA_ERR_UNSUPPORTED;
+    IndexArgs a = index_args(layout, nullptr, nullptr, n_heads_idx, d_idx, ratio, top_k, nullptr, nullptr, nullptr,
+                             0, nullptr);
+    *bytes = align_ws(index_fp8_workspace_bytes(a));
+    return CSA_OK;
 }
 
 csa_status_t csa_index_workspace_size(const csa_layout *layout, int n_heads_idx, int d_idx, int ratio, int top_k,
@@ -454,8 +515,12 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
     if (!p || p->reserved != 0) return CSA_ERR_INVALID_ARG;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
     const csa_layout *L = &p->layout;
-    CSA_TRY(check_index(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k, p->idx_out,
-                        p->score_out));
+    const bool fp8 = (p->flags & CSA_INDEX_FP8) != 0;
+    if (p->flags & ~(CSA_SKIP_COMPRESS | CSA_INDEX_FP8)) return CSA_ERR_INVALID_ARG;
+    // with FP8 keys the bf16 keys are not read (a non-null placeholder passes the shared checks)
+    CSA_TRY(check_index(L, p->q_idx, fp8 ? reinterpret_cast<const csa_bf16 *>(p->k_idx_fp8) : p->k_idx,
+                        p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k, p->idx_out, p->score_out));
+    if (fp8) CSA_TRY(check_fp8_keys(L, p->k_idx_fp8, p->k_idx_scale, p->ratio_csa));
     CSA_TRY(check_attend(L, true, p->q, p->csa_cache, p->kv, p->idx_out, p->n_heads, p->d, p->ratio_csa, p->top_k,
                          p->o_csa, p->lse_csa));
     CSA_TRY(check_attend(L, false, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca, 0, p->o_hca,
@@ -521,6 +586,10 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
                                   p->idx_out, p->score_out, w_idx ? ws : nullptr, w_idx, ds->err);
         ia.scan_done = ds->sdone;
         ia.pdl = compress;
+        if (fp8) {
+            ia.k_fp8 = p->k_idx_fp8;
+            ia.k_scale = p->k_idx_scale;
+        }
         s_c = from_cuda(launch_index_topk(ia, st));
     } else {
         cudaEventRecord(ds->sdone, st);
@@ -591,7 +660,7 @@ csa_status_t csa_check_device_error(csa_stream_t stream, csa_status_t *device_st
     return CSA_OK;
 }
 
-int csa_version(void) { return 100; }
+int csa_version(void) { return 110; }   // 1.1: FP8 indexer keys
 
 csa_status_t csa_timing_enable(int enable)
 {

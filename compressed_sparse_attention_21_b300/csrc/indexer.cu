@@ -25,6 +25,8 @@
 //    winners by index.
 // The full score matrix is never stored; only one key row per query in the
 // multi-CTA path.
+#include <cuda_fp8.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -561,13 +563,17 @@ index_filter_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
 constexpr int kChunkBytes = 32 * 1024;
 constexpr int kScanStages = 3;   // chunks in flight per CTA (two CTAs per SM)
 
-template <int DI>
+template <int DI, bool FP8>
 __global__ void __launch_bounds__(kScanThreads, 2)
 index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
                         const int64_t *__restrict__ cu_csa, int64_t q_begin, const uint16_t *__restrict__ qI,
-                        const uint16_t *__restrict__ kI, int HI, int ratio, int cpc, WsD w, int *err)
+                        const void *__restrict__ kI_, const float *__restrict__ k_scale, int HI, int ratio, int cpc,
+                        WsD w, int *err)
 {
-    constexpr int ROWS = kChunkBytes / (2 * DI);
+    // bf16 keys: 2 DI bytes per row; FP8 keys: DI bytes per row and a scale
+    constexpr int RB = FP8 ? DI : 2 * DI;
+    constexpr int ROWS = kChunkBytes / RB;
+    const uint8_t *kI = static_cast<const uint8_t *>(kI_);
     constexpr int LPR = DI / 8;                         // lanes per key row
     constexpr int RPW = 32 / LPR;                       // rows per warp step
     constexpr int NWARP = kScanThreads / 32;
@@ -589,13 +595,14 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
     }
     const int64_t r_end = n - r_begin < (int64_t)cpc * ROWS ? n : r_begin + (int64_t)cpc * ROWS;
     const int nchunks = (int)((r_end - r_begin + ROWS - 1) / ROWS);
-    const uint16_t *kbase = kI + (p.e0 + r_begin) * DI;
+    const uint8_t *kbase = kI + (p.e0 + r_begin) * RB;
+    const float *sbase = FP8 ? k_scale + p.e0 + r_begin : nullptr;
     auto rows_of = [&](int c) { return (int)(r_end - r_begin - (int64_t)c * ROWS < ROWS ? r_end - r_begin - (int64_t)c * ROWS : ROWS); };
     auto issue = [&](int c) {
         const int s = c % kScanStages;
-        const uint32_t bytes = (uint32_t)rows_of(c) * DI * 2;
+        const uint32_t bytes = (uint32_t)rows_of(c) * RB;
         mbar_expect_tx(smem_u32(s_bar + s), bytes);
-        bulk_g2s(smem_u32(s_rows + s * kChunkBytes), kbase + (int64_t)c * ROWS * DI, bytes, smem_u32(s_bar + s));
+        bulk_g2s(smem_u32(s_rows + s * kChunkBytes), kbase + (int64_t)c * ROWS * RB, bytes, smem_u32(s_bar + s));
     };
     if (tid == 0) {
         for (int s = 0; s < kScanStages; s++) mbar_init(smem_u32(s_bar + s), 1);
@@ -611,8 +618,28 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
 #pragma unroll
     for (int x = 0; x < 8; x++) qv[x] = s_q[cg * 8 + x];
     uint32_t *keys = w.keys + qg * w.key_stride + r_begin;
+    // FP8: warp `warp` scores rows it * NWARP * RPW + warp * RPW + sub of a
+    // chunk (it < ITERS); their scales are loaded one chunk ahead into
+    // registers, scale u = it * RPW + sub of the warp in lane u % 32, slot u / 32
+    constexpr int ITERS = ROWS / (NWARP * RPW);
+    constexpr int SPL = FP8 ? (ITERS * RPW + 31) / 32 : 1;
+    static_assert(ROWS % (NWARP * RPW) == 0 && 32 % RPW == 0, "scan tiling");
+    float sc_cur[SPL], sc_nxt[SPL];
+    auto load_scales = [&](int c, float (&sc)[SPL]) {
+        const int rows = rows_of(c);
+#pragma unroll
+        for (int j = 0; j < SPL; j++) {
+            const int u = 32 * j + lane;
+            const int row = (u / RPW) * (NWARP * RPW) + warp * RPW + u % RPW;
+            sc[j] = row < rows ? __ldg(sbase + (int64_t)c * ROWS + row) : 0.f;
+        }
+    };
+    if constexpr (FP8) load_scales(0, sc_cur);
     for (int c = 0; c < nchunks; c++) {
         const int s = c % kScanStages;
+        if constexpr (FP8) {
+            if (c + 1 < nchunks) load_scales(c + 1, sc_nxt);
+        }
         const bool landed = mbar_wait(smem_u32(s_bar + s), (uint32_t)((c / kScanStages) & 1));
         if (__syncthreads_or(!landed)) {
             // the histogram stays incomplete: the select kernel sees a count
@@ -624,23 +651,51 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
         const int rows = rows_of(c);
         const uint8_t *src = s_rows + s * kChunkBytes;
         uint32_t *kc = keys + (int64_t)c * ROWS;
-        for (int rb = warp * RPW; rb < ROWS; rb += NWARP * RPW) {
-            const int row = rb + sub;
-            const bool in = row < rows;
-            const uint4 v = in ? *reinterpret_cast<const uint4 *>(src + row * (2 * DI) + cg * 16) : make_uint4(0, 0, 0, 0);
-            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-            float acc = 0.f;
+        if constexpr (FP8) {
 #pragma unroll
-            for (int k = 0; k < 4; k++) {
-                acc = fmaf(qv[2 * k], bf16_lo(wd[k]), acc);
-                acc = fmaf(qv[2 * k + 1], bf16_hi(wd[k]), acc);
+            for (int it = 0; it < ITERS; it++) {
+                const int row = it * (NWARP * RPW) + warp * RPW + sub;
+                const bool in = row < rows;
+                // 8 codes per lane; E4M3 -> f16 is exact
+                const uint2 v = in ? *reinterpret_cast<const uint2 *>(src + row * RB + cg * 8) : make_uint2(0, 0);
+                const uint32_t wd[2] = {v.x, v.y};
+                float acc = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)(wd[k >> 1] >> (16 * (k & 1)));
+                    const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
+                    acc = fmaf(qv[2 * k], f.x, acc);
+                    acc = fmaf(qv[2 * k + 1], f.y, acc);
+                }
+#pragma unroll
+                for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                const float scl = __shfl_sync(0xffffffffu, sc_cur[(it * RPW) / 32], (it * RPW) % 32 + sub);
+                const bool valid = cg == 0 && in;
+                const uint32_t key = score_key(acc * scl);
+                if (valid) kc[row] = key;
+                if (valid) atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);
             }
 #pragma unroll
-            for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            const bool valid = cg == 0 && in;
-            const uint32_t key = score_key(acc);
-            if (valid) kc[row] = key;
-            if (valid) atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);   // few lanes per step: no aggregation
+            for (int j = 0; j < SPL; j++) sc_cur[j] = sc_nxt[j];
+        } else {
+            for (int rb = warp * RPW; rb < ROWS; rb += NWARP * RPW) {
+                const int row = rb + sub;
+                const bool in = row < rows;
+                float acc = 0.f;
+                const uint4 v = in ? *reinterpret_cast<const uint4 *>(src + row * RB + cg * 16) : make_uint4(0, 0, 0, 0);
+                const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    acc = fmaf(qv[2 * k], bf16_lo(wd[k]), acc);
+                    acc = fmaf(qv[2 * k + 1], bf16_hi(wd[k]), acc);
+                }
+#pragma unroll
+                for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                const bool valid = cg == 0 && in;
+                const uint32_t key = score_key(acc);
+                if (valid) kc[row] = key;
+                if (valid) atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);   // few lanes per step: no aggregation
+            }
         }
         __syncthreads();   // stage s has been read
         if (tid == 0 && c + kScanStages < nchunks) issue(c + kScanStages);
@@ -974,12 +1029,13 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
     // scan_done: after the last key scan of the multi-kernel paths; the
     // single-kernel paths mark it up front (their kernel holds the GPU to the end)
     auto mark = [&]() -> cudaError_t { return a.scan_done ? cudaEventRecord(a.scan_done, st) : cudaSuccess; };
-    if (index_block_applicable(a) || use_cta_path(a)) {
+    const bool fp8 = a.k_fp8 != nullptr;   // FP8 keys: the chunk scan and the select only
+    if (!fp8 && (index_block_applicable(a) || use_cta_path(a))) {
         cudaError_t e = mark();
         if (e != cudaSuccess) return e;
     }
-    if (index_block_applicable(a)) return launch_index_block(a, st);
-    if (use_cta_path(a)) {
+    if (!fp8 && index_block_applicable(a)) return launch_index_block(a, st);
+    if (!fp8 && use_cta_path(a)) {
         const int64_t nsm = max_n < 1 ? 1 : max_n;
         const size_t smem = (size_t)nsm * 4;
         for (int64_t q0 = 0; q0 < a.total_q; q0 += 1 << 30) {
@@ -996,7 +1052,7 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
     const int64_t nchunks = (max_n <= 0 ? 1 : (max_n + kScanChunk - 1) / kScanChunk);
     WsD w = carve_wsd(a.ws, gq, max_n < 1 ? 1 : max_n, a.top_k);
     if (max_n <= kSelMaxN) {
-        constexpr int ROWS = kChunkBytes / (2 * DI);
+        const int ROWS = kChunkBytes / (fp8 ? DI : 2 * DI);
         const int64_t nch = max_n <= 0 ? 1 : (max_n + ROWS - 1) / ROWS;
         // chunks per CTA: the group's chunks over about two CTAs per SM
         const int64_t slots = 2 * (int64_t)device_sms();
@@ -1006,10 +1062,15 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
             if (cpc < 1) cpc = 1;
             if (cpc > nch) cpc = nch;
             const int64_t gx = (nch + cpc - 1) / cpc;
-            cudaError_t e = launch_kernel("index_scan", index_chunk_scan_kernel<DI>, dim3((unsigned)gx, (unsigned)nq),
-                                          dim3(kScanThreads), (size_t)kScanStages * kChunkBytes, st, a.pdl, a.batch,
-                                          a.cu_kv, a.cu_q, a.cu_csa, q0, a.q_idx, a.k_idx, a.n_heads_idx, a.ratio,
-                                          (int)cpc, w, a.err);
+            cudaError_t e =
+                a.k_fp8 ? launch_kernel("index_scan", index_chunk_scan_kernel<DI, true>, dim3((unsigned)gx, (unsigned)nq),
+                                        dim3(kScanThreads), (size_t)kScanStages * kChunkBytes, st, a.pdl, a.batch,
+                                        a.cu_kv, a.cu_q, a.cu_csa, q0, a.q_idx, (const void *)a.k_fp8, a.k_scale,
+                                        a.n_heads_idx, a.ratio, (int)cpc, w, a.err)
+                        : launch_kernel("index_scan", index_chunk_scan_kernel<DI, false>, dim3((unsigned)gx, (unsigned)nq),
+                                        dim3(kScanThreads), (size_t)kScanStages * kChunkBytes, st, a.pdl, a.batch,
+                                        a.cu_kv, a.cu_q, a.cu_csa, q0, a.q_idx, (const void *)a.k_idx, a.k_scale,
+                                        a.n_heads_idx, a.ratio, (int)cpc, w, a.err);
             if (e == cudaSuccess && q0 + nq >= a.total_q) e = mark();
             if (e != cudaSuccess) return e;
             e = launch_select(a, max_n, q0, nq, w, st);
@@ -1017,6 +1078,7 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
         }
         return cudaSuccess;
     }
+    if (fp8) return cudaErrorInvalidValue;   // rows longer than index_fp8_max_n(): refused by the caller
     for (int64_t q0 = 0; q0 < a.total_q; q0 += gq) {
         const int64_t nq = a.total_q - q0 < gq ? a.total_q - q0 : gq;
         dim3 grid((unsigned)nchunks, (unsigned)nq);
@@ -1045,6 +1107,68 @@ size_t index_workspace_bytes(const IndexArgs &a)
     if (a.total_q <= 0) return 0;
     if (index_block_applicable(a)) return index_block_ws_bytes(a);
     if (use_cta_path(a)) return 0;
+    const int64_t max_n = a.max_kv_len / a.ratio;
+    return (size_t)wsd_total_bytes(group_size(a), max_n < 1 ? 1 : max_n, a.top_k);
+}
+
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) indexer keys: one warp per key row.  Lane l holds values
+// l*V .. l*V + V - 1 (V = d_idx / 32); the row's absolute maximum a gives
+// inv = 448 / a and scale = a / 448 (IEEE fp32), each value k * inv is
+// converted to E4M3 rounding to nearest even and saturating at +-448.
+// ---------------------------------------------------------------------------
+template <int DI>
+__global__ void __launch_bounds__(256)
+quantize_index_keys_kernel(const uint16_t *__restrict__ k_idx, int64_t rows, uint8_t *__restrict__ k_fp8,
+                           float *__restrict__ k_scale)
+{
+    constexpr int V = DI / 32;
+    static_assert(DI % 32 == 0 && V >= 1 && V <= 4, "row width");
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const uint16_t *src = k_idx + row * DI + lane * V;
+    float v[V];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; i++) {
+        v[i] = __uint_as_float((uint32_t)__ldg(src + i) << 16);
+        amax = fmaxf(amax, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+    uint8_t code[V];
+#pragma unroll
+    for (int i = 0; i < V; i++)
+        code[i] = amax > 0.f ? (uint8_t)__nv_cvt_float_to_fp8(__fmul_rn(v[i], inv), __NV_SATFINITE, __NV_E4M3)
+                             : (uint8_t)0;
+    uint8_t *dst = k_fp8 + row * DI + lane * V;
+#pragma unroll
+    for (int i = 0; i < V; i++) dst[i] = code[i];
+    if (lane == 0) k_scale[row] = __fdiv_rn(amax, 448.f);
+}
+
+cudaError_t launch_quantize_index_keys(const uint16_t *k_idx, int64_t rows, int d_idx, uint8_t *k_fp8,
+                                       float *k_scale, cudaStream_t st)
+{
+    if (rows <= 0) return cudaSuccess;
+    const int64_t blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)blocks);
+    switch (d_idx) {
+    case 32: return launch_kernel("quantize_index_keys", quantize_index_keys_kernel<32>, grid, dim3(256), 0, st, false, k_idx, rows, k_fp8, k_scale);
+    case 64: return launch_kernel("quantize_index_keys", quantize_index_keys_kernel<64>, grid, dim3(256), 0, st, false, k_idx, rows, k_fp8, k_scale);
+    case 128: return launch_kernel("quantize_index_keys", quantize_index_keys_kernel<128>, grid, dim3(256), 0, st, false, k_idx, rows, k_fp8, k_scale);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int64_t index_fp8_max_n() { return kSelMaxN; }
+
+size_t index_fp8_workspace_bytes(const IndexArgs &a)
+{
+    if (a.total_q <= 0) return 0;
     const int64_t max_n = a.max_kv_len / a.ratio;
     return (size_t)wsd_total_bytes(group_size(a), max_n < 1 ? 1 : max_n, a.top_k);
 }

@@ -106,6 +106,8 @@ struct IndexArgs {
     cudaEvent_t scan_done;  // if set: recorded on the stream once every key has been scored
     const int64_t *cu_kv, *cu_q, *cu_csa;
     const uint16_t *q_idx, *k_idx;
+    const uint8_t *k_fp8;   // if set: the keys as E4M3 codes with k_scale (k_idx unused)
+    const float *k_scale;
     int n_heads_idx, d_idx, ratio, top_k;
     int32_t *idx_out;
     float *score_out;
@@ -121,6 +123,13 @@ size_t index_block_ws_bytes(const IndexArgs &a);      // for a full grid of pers
 size_t index_block_min_ws_bytes();                      // one CTA (the kernel fits its grid to ws_bytes)
 cudaError_t launch_index_block(const IndexArgs &a, cudaStream_t st);
 size_t index_workspace_bytes(const IndexArgs &a);
+// FP8 keys (k_fp8 set): the chunk scan and the clustered select, rows of up
+// to index_fp8_max_n() entries
+int64_t index_fp8_max_n();
+size_t index_fp8_workspace_bytes(const IndexArgs &a);
+// E4M3 codes and per-row fp32 scales of rows indexer keys (d_idx values each)
+cudaError_t launch_quantize_index_keys(const uint16_t *k_idx, int64_t rows, int d_idx, uint8_t *k_fp8,
+                                       float *k_scale, cudaStream_t st);
 cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t st);
 // Library-owned scratch of lightning_index_topk_static (see indexer.cu):
 // its device address on the current device (looked up on first use), and the

@@ -192,6 +192,40 @@ csa_status_t lightning_index_topk_static(const csa_layout *layout, const csa_bf1
                                          csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 indexer keys: a low-precision lightning indexer ("DeepSeek-V4 core
+ * architecture", §9 "key innovations summary", table row 5: the indexer's
+ * QK product is quantised, there to FP4 through quantisation-aware
+ * training).  This library takes the inference-side form of that idea with
+ * FP8 E4M3 keys and one scale per key row.  It is an option next to the
+ * bf16 indexer above, for callers that keep the indexer keys in FP8, and
+ * reads half the bytes per entry, the dominant traffic of a decode step.
+ *
+ * csa_quantize_index_keys turns each indexer key row j (d_idx bf16 values)
+ * into FP8 E4M3 codes with one fp32 scale, all arithmetic in fp32 (IEEE
+ * division and multiplication, round to nearest even):
+ *     a_j = max_i |k_ji|,  inv_j = 448 / a_j,
+ *     code_ji = e4m3(k_ji * inv_j)   round to nearest even, saturating at +-448,
+ *     scale_j = a_j / 448            (a_j = 0: every code 0 and scale 0)
+ *   k_idx   [total_csa, d_idx] bf16
+ *   k_fp8   [total_csa, d_idx] E4M3 bytes;   k_scale [total_csa] fp32
+ *
+ * lightning_index_topk_fp8 is lightning_index_topk on the dequantised keys:
+ *     s(t, j) = scale_j * sum_i (sum_h q^I_{t,h,i}) * e4m3_value(code_ji)   (fp32)
+ * with the same selection rules, outputs and padding.  Rows of up to 262144
+ * entries (longer: CSA_ERR_UNSUPPORTED).  Workspace from
+ * csa_index_fp8_workspace_size, zero-filled, as for lightning_index_topk.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_quantize_index_keys(const csa_layout *layout, const csa_bf16 *k_idx, int d_idx,
+                                     uint8_t *k_fp8, float *k_scale, csa_stream_t stream);
+csa_status_t lightning_index_topk_fp8(const csa_layout *layout, const csa_bf16 *q_idx,
+                                      const uint8_t *k_fp8, const float *k_scale,
+                                      int n_heads_idx, int d_idx, int ratio, int top_k,
+                                      int32_t *idx_out, float *score_out, void *ws, size_t ws_bytes,
+                                      csa_stream_t stream);
+csa_status_t csa_index_fp8_workspace_size(const csa_layout *layout, int n_heads_idx, int d_idx,
+                                          int ratio, int top_k, size_t *bytes);
+
+/* ---------------------------------------------------------------------------
  * Sparse shared-KV multi-query attention (§2.2 step 3).
  *
  * Query row i at position t of sequence b attends, with every one of its
@@ -237,6 +271,7 @@ csa_status_t csa_attend_workspace_size(const csa_layout *layout, int n_heads, in
  * attention) concurrently, and returns both branches' outputs.
  * ------------------------------------------------------------------------- */
 #define CSA_SKIP_COMPRESS 0x1   /* caches already hold every needed entry */
+#define CSA_INDEX_FP8 0x2       /* index with k_idx_fp8 / k_idx_scale (see csa_quantize_index_keys) */
 
 typedef struct csa_hybrid_params {
     csa_layout layout;
@@ -259,6 +294,8 @@ typedef struct csa_hybrid_params {
     float *lse_hca;            /* [total_q, n_heads] or NULL */
     void *ws;
     size_t ws_bytes;
+    const uint8_t *k_idx_fp8;  /* [total_csa, d_idx] E4M3 codes, with CSA_INDEX_FP8 (else NULL) */
+    const float *k_idx_scale;  /* [total_csa] fp32 scales, with CSA_INDEX_FP8 (else NULL) */
 } csa_hybrid_params;
 
 csa_status_t hybrid_attend(const csa_hybrid_params *params, csa_stream_t stream);

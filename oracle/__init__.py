@@ -57,8 +57,15 @@ def _load():
                                            P, I64, P, P, I, I, P, P, P, P, P]
         lib.orc_compress_packed.argtypes = [I, P, P, P, P, I, I, P]
         lib.orc_compress_selected.argtypes = [I, P, P, P, P, I, I, I64, P, P]
+        lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_decode.restype = D
+        lib.orc_e4m3_encode.argtypes = [D]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_quantize_index_keys.argtypes = [P, I64, I, P, P]
+        lib.orc_index_scores_fp8.argtypes = [P, P, P, I64, I, I, P]
         for f in ("orc_compress", "orc_index_scores", "orc_topk", "orc_attend",
-                  "orc_hybrid_queries", "orc_compress_packed", "orc_compress_selected"):
+                  "orc_hybrid_queries", "orc_compress_packed", "orc_compress_selected",
+                  "orc_quantize_index_keys", "orc_index_scores_fp8"):
             getattr(lib, f).restype = I
         _lib = lib
     return _lib
@@ -125,6 +132,40 @@ def index_scores(qI_bits, kI_bits):
     n = kI_bits.shape[0]
     s = np.empty(n, np.float64)
     _check(_load().orc_index_scores(_ptr(qI_bits), _ptr(kI_bits), n, HI, dI, _ptr(s)), "index_scores")
+    return s
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one FP8 E4M3 code (NaN for 0x7f / 0xff)."""
+    return float(_load().orc_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest E4M3 code, ties to even, saturating at +-448, sign kept."""
+    return int(_load().orc_e4m3_encode(float(x)))
+
+
+def quantize_index_keys(kI_bits):
+    """kI: [n, dI] bf16 bits -> (codes [n, dI] uint8, scale [n] float32)."""
+    kI_bits = _c(kI_bits, np.uint16)
+    n, dI = kI_bits.shape
+    codes = np.empty((n, dI), np.uint8)
+    scale = np.empty(n, np.float32)
+    _check(_load().orc_quantize_index_keys(_ptr(kI_bits), n, dI, _ptr(codes), _ptr(scale)),
+           "quantize_index_keys")
+    return codes, scale
+
+
+def index_scores_fp8(qI_bits, codes, scale):
+    """qI: [HI, dI] bf16 bits; codes [n, dI]; scale [n] -> s[n] fp64."""
+    qI_bits = _c(qI_bits, np.uint16)
+    codes = _c(codes, np.uint8)
+    scale = _c(scale, np.float32)
+    HI, dI = qI_bits.shape
+    n = codes.shape[0]
+    s = np.empty(n, np.float64)
+    _check(_load().orc_index_scores_fp8(_ptr(qI_bits), _ptr(codes), _ptr(scale), n, HI, dI, _ptr(s)),
+           "index_scores_fp8")
     return s
 
 

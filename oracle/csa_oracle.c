@@ -11,7 +11,9 @@
  *   [V4]   "DeepSeek-V4 core architecture" (gitcode.csdn.net article),
  *          §2.2 "CSA: compressed sparse attention" -- step 1 token-level
  *          compression, step 2 lightning indexer, step 3 shared-KV MQA;
- *          §2.3 "HCA: heavily compressed attention".
+ *          §2.3 "HCA: heavily compressed attention";
+ *          §9 "key innovations summary" (table row 5: the indexer QK
+ *          product is quantised);
  *   [DEBT] "DeepSeek V4's architecture debt chain" (vendordeep.com),
  *          "Constraint 1 -> Innovation 1: CSA+HCA hybrid attention"
  *          (128x fusion of many tokens' KV into one compressed token).
@@ -30,6 +32,9 @@
  *       the block's weights are the softmax of its tokens' logits.
  *   A7  top-k order: higher score first, ties to the lower entry index;
  *       the selected indices are returned ascending, padded with -1.
+ *   R8  the low-precision indexer stores each key row as FP8 E4M3 codes
+ *       scaled so the row's largest magnitude maps to 448, plus an fp32
+ *       scale (see the FP8 section below).
  *
  * Everything is computed in double precision; bf16 and fp32 inputs
  * convert to double exactly.  Plain loops, no blocking or reordering
@@ -118,6 +123,100 @@ int orc_index_scores(const uint16_t *qI, const uint16_t *kI, int64_t n,
             for (int i = 0; i < dI; i++)
                 acc += bf16_to_double(qI[h * dI + i]) *
                        bf16_to_double(kI[j * (int64_t)dI + i]);
+        s[j] = acc;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * FP8 indexer keys ([V4] §9 "key innovations summary", table row 5: the
+ * indexer's QK product runs quantised).  Reading R8: each key row j is
+ * scaled so its largest magnitude maps to 448, the largest finite FP8 E4M3
+ * value, and stored as E4M3 codes plus one fp32 scale; the score is then
+ * the R1 score on the dequantised keys.  The pages give no quantiser; the
+ * tests pin these functions to the E4M3 format's definition instead.
+ *
+ * E4M3 ("e4m3fn"): sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * no infinities; exponent 15 with mantissa 7 is NaN, so the largest finite
+ * value is 1.75 * 2^8 = 448; exponent 0 holds the subnormals m/8 * 2^-6.
+ * ---------------------------------------------------------------------- */
+double orc_e4m3_decode(uint8_t c)
+{
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp(m / 8.0, -6);
+    else        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Round to the nearest finite E4M3 value, ties to the code with an even
+ * mantissa, magnitudes above 448 saturate to 448 (the "satfinite" mode).
+ * The sign is kept, so negative values that round to zero give -0 (0x80).
+ * Plain scan over the 127 finite magnitudes 0x00 .. 0x7e, which ascend. */
+uint8_t orc_e4m3_encode(double x)
+{
+    if (isnan(x)) return 0x7f;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs(x);
+    if (a >= 448.0) return sign | 0x7e;
+    int lo = 0;
+    while (lo + 1 <= 0x7e && orc_e4m3_decode((uint8_t)(lo + 1)) <= a) lo++;
+    if (lo == 0x7e) return sign | 0x7e;
+    const double dlo = a - orc_e4m3_decode((uint8_t)lo);
+    const double dhi = orc_e4m3_decode((uint8_t)(lo + 1)) - a;
+    int c;
+    if (dlo < dhi)      c = lo;
+    else if (dhi < dlo) c = lo + 1;
+    else                c = (lo & 1) ? lo + 1 : lo;
+    return sign | (uint8_t)c;
+}
+
+/* Quantise n key rows of width dI (bf16) to E4M3 codes and fp32 scales.
+ * The scaling arithmetic is fp32 with IEEE rounding, as the format of the
+ * stored scale fixes it: a = max |k|, inv = 448 / a, q = k * inv,
+ * scale = a / 448; a row of zeros gets codes 0 and scale 0. */
+int orc_quantize_index_keys(const uint16_t *kI, int64_t n, int dI,
+                            uint8_t *codes, float *scale)
+{
+    if ((n > 0 && (!kI || !codes || !scale)) || dI <= 0) return 1;
+    for (int64_t j = 0; j < n; j++) {
+        float a = 0.0f;
+        for (int i = 0; i < dI; i++) {
+            const float v = (float)bf16_to_double(kI[j * (int64_t)dI + i]);
+            if (fabsf(v) > a) a = fabsf(v);
+        }
+        if (a == 0.0f) {
+            for (int i = 0; i < dI; i++) codes[j * (int64_t)dI + i] = 0;
+            scale[j] = 0.0f;
+            continue;
+        }
+        const float inv = 448.0f / a;
+        for (int i = 0; i < dI; i++) {
+            const float v = (float)bf16_to_double(kI[j * (int64_t)dI + i]);
+            const float q = v * inv;
+            codes[j * (int64_t)dI + i] = orc_e4m3_encode((double)q);
+        }
+        scale[j] = a / 448.0f;
+    }
+    return 0;
+}
+
+/* R1 score on the dequantised keys: s_j = sum_h sum_i qI[h,i] * kq[j,i]
+ * with kq[j,i] = scale_j * e4m3(codes[j,i]) (exact in double). */
+int orc_index_scores_fp8(const uint16_t *qI, const uint8_t *codes,
+                         const float *scale, int64_t n, int HI, int dI,
+                         double *s)
+{
+    if (!qI || (n > 0 && (!codes || !scale || !s)) || HI <= 0 || dI <= 0)
+        return 1;
+    for (int64_t j = 0; j < n; j++) {
+        double acc = 0.0;
+        for (int h = 0; h < HI; h++)
+            for (int i = 0; i < dI; i++)
+                acc += bf16_to_double(qI[h * dI + i]) *
+                       ((double)scale[j] *
+                        orc_e4m3_decode(codes[j * (int64_t)dI + i]));
         s[j] = acc;
     }
     return 0;

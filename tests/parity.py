@@ -77,11 +77,12 @@ class GpuProblem:
             csa.hca_compress(self.full, self.kv, self.gate, hca_cache)
         return csa_cache, hca_cache
 
-    def hybrid(self, prebuilt=True, skip_compress=False, with_scores=True):
+    def hybrid(self, prebuilt=True, skip_compress=False, with_scores=True, fp8=False):
         caches = self.build_caches() if prebuilt else (None, None)
+        k_idx_fp8 = csa.quantize_index_keys(self.full, self.kI) if fp8 else None
         h = csa.Hybrid(self.layout, self.kv, self.gate, self.qI, self.kI, self.q, self.p["top_k"],
                        self.p["scale"], csa_cache=caches[0], hca_cache=caches[1],
-                       skip_compress=skip_compress, with_scores=with_scores)
+                       skip_compress=skip_compress, with_scores=with_scores, k_idx_fp8=k_idx_fp8)
         h()
         torch.cuda.synchronize()
         return h
@@ -91,11 +92,28 @@ def oracle_inputs(p):
     return wl.to_numpy(p)
 
 
-def score_abs_bound(qI_bits, kI_bits, js):
+def score_abs_bound(qI_bits, kI_bits, js, dequant=None):
     """sum_h sum_i |q_hi k_ji| for the listed entries (the fp32 error scale)."""
     q = np.abs(oracle_f64(qI_bits)).sum(0)                 # [dI]
-    k = np.abs(oracle_f64(kI_bits[js]))                     # [len(js), dI]
+    k = np.abs(dequant(js) if dequant is not None else oracle_f64(kI_bits[js]))   # [len(js), dI]
     return k @ q
+
+
+_E4M3 = None
+
+
+def e4m3_table():
+    """Value of every E4M3 code, from the oracle's decoder (fp64, exact)."""
+    global _E4M3
+    if _E4M3 is None:
+        _E4M3 = np.array([oracle.e4m3_decode(c) for c in range(256)], np.float64)
+    return _E4M3
+
+
+def fp8_dequant(codes, scale):
+    """js -> scale_j * e4m3(codes_j) for rows js of one sequence's FP8 keys."""
+    tab = e4m3_table()
+    return lambda js: scale[js].astype(np.float64)[:, None] * tab[codes[js]]
 
 
 def oracle_f64(bits):
@@ -103,8 +121,11 @@ def oracle_f64(bits):
     return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).double().numpy()
 
 
-def check_topk_row(gpu_row, orc_row, scores, n_vis, k, qI_bits, kI_seq_bits):
-    """Returns ('equal'|'tie'|'fp32tie', n_swaps); raises AssertionError on a real mismatch."""
+def check_topk_row(gpu_row, orc_row, scores, n_vis, k, qI_bits, kI_seq_bits, dequant=None):
+    """Returns ('equal'|'tie'|'fp32tie', n_swaps); raises AssertionError on a real mismatch.
+
+    dequant: for FP8 keys, a callable js -> [len(js), dI] fp64 dequantised keys
+    (then kI_seq_bits is unused); the fp32 score has one more rounding (the scale)."""
     g = gpu_row[gpu_row >= 0]
     o = orc_row[orc_row >= 0]
     want = min(k, n_vis)
@@ -124,10 +145,10 @@ def check_topk_row(gpu_row, orc_row, scores, n_vis, k, qI_bits, kI_seq_bits):
         return "tie", len(diff) // 2
     # fp32 forward-error band of the library's score (head sum, then a dI-term dot)
     HI, dI = qI_bits.shape
-    n_terms = HI + dI + 2
+    n_terms = HI + dI + 2 + (1 if dequant is not None else 0)
     gam = n_terms * U32 / (1 - n_terms * U32)
     j_k = int(o[np.argmin(scores[o])])
-    bnd = gam * score_abs_bound(qI_bits, kI_seq_bits, np.concatenate([diff, [j_k]]))
+    bnd = gam * score_abs_bound(qI_bits, kI_seq_bits, np.concatenate([diff, [j_k]]), dequant)
     tol = bnd[:-1] + bnd[-1]
     bad = gap > np.maximum(band, tol)
     assert not bad.any(), \
@@ -149,9 +170,12 @@ def assert_att(gpu, ref, what):
     return m, r
 
 
-def check_hybrid(p, h: "csa.Hybrid", eval_q=None, check_entries="all", entry_sample=None, seed=0):
+def check_hybrid(p, h: "csa.Hybrid", eval_q=None, check_entries="all", entry_sample=None, seed=0,
+                 fp8=None):
     """Compare a finished hybrid run with the oracle on `eval_q` (default: all queries).
 
+    fp8: the oracle's (codes, scales) of the indexer keys when the run used the
+    FP8 indexer; the oracle then selects on its FP8 scores.
     Returns a report dict (errors, tie counts)."""
     inp = oracle_inputs(p)
     total_q = int(inp["cu_q"][-1])
@@ -178,7 +202,26 @@ def check_hybrid(p, h: "csa.Hybrid", eval_q=None, check_entries="all", entry_sam
     rep["entry_err_csa"], rep["entry_err_hca"] = e_csa, e_hca
 
     # --- oracle on its own selection ---
-    orc = oracle.hybrid_queries(inp, eval_q=eval_q, hca_entries=orc_hca)
+    cu_kv, cu_q, cu_csa = inp["cu_kv"], inp["cu_q"], inp["cu_csa"]
+
+    def visible(qi):
+        b = int(np.searchsorted(cu_q, qi, side="right") - 1)
+        L = cu_kv[b + 1] - cu_kv[b]
+        t = L - (cu_q[b + 1] - cu_q[b]) + (qi - cu_q[b])
+        return b, int((t + 1) // p["mC"])
+
+    def fp8_row(qi):
+        b, n_vis = visible(qi)
+        codes, scale = fp8[0][cu_csa[b]:cu_csa[b] + n_vis], fp8[1][cu_csa[b]:cu_csa[b] + n_vis]
+        s = oracle.index_scores_fp8(inp["qI"][qi], codes, scale) if n_vis else np.zeros(0)
+        return s, fp8_dequant(codes, scale)
+
+    if fp8 is None:
+        orc = oracle.hybrid_queries(inp, eval_q=eval_q, hca_entries=orc_hca)
+    else:
+        orc_idx = np.stack([oracle.topk(fp8_row(qi)[0], p["top_k"]) for qi in eval_q])
+        orc = oracle.hybrid_queries(inp, eval_q=eval_q, given_idx=orc_idx, hca_entries=orc_hca)
+        orc["idx"] = orc_idx
     rows = torch.from_numpy(eval_q).to(h.idx.device)
     gpu_idx = h.idx[rows].cpu().numpy()
     gpu_oC = bf16_to_f64(h.o_csa[rows])
@@ -187,17 +230,17 @@ def check_hybrid(p, h: "csa.Hybrid", eval_q=None, check_entries="all", entry_sam
     gpu_lH = h.lse_hca[rows].cpu().numpy()
 
     # --- top-k ---
-    cu_kv, cu_q, cu_csa = inp["cu_kv"], inp["cu_q"], inp["cu_csa"]
     kinds = {"equal": 0, "tie": 0, "fp32tie": 0}
     swapped = []
     for r, qi in enumerate(eval_q):
-        b = int(np.searchsorted(cu_q, qi, side="right") - 1)
-        L = cu_kv[b + 1] - cu_kv[b]
-        t = L - (cu_q[b + 1] - cu_q[b]) + (qi - cu_q[b])
-        n_vis = int((t + 1) // p["mC"])
+        b, n_vis = visible(qi)
         kI_seq = inp["kI"][cu_csa[b]:cu_csa[b] + n_vis]
-        scores = oracle.index_scores(inp["qI"][qi], kI_seq) if n_vis else np.zeros(0)
-        kind, _ = check_topk_row(gpu_idx[r], orc["idx"][r], scores, n_vis, p["top_k"], inp["qI"][qi], kI_seq)
+        if fp8 is None:
+            scores, dq = (oracle.index_scores(inp["qI"][qi], kI_seq) if n_vis else np.zeros(0)), None
+        else:
+            scores, dq = fp8_row(qi)
+        kind, _ = check_topk_row(gpu_idx[r], orc["idx"][r], scores, n_vis, p["top_k"], inp["qI"][qi], kI_seq,
+                                 dq)
         kinds[kind] += 1
         if kind != "equal":
             swapped.append(r)

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.csa_version() == 100
+    assert lib.csa_version() == 110
     assert lib.csa_status_string(0) == b"ok"
     assert lib.csa_status_string(3) == b"workspace missing or too small"
 

@@ -90,21 +90,28 @@ def test_compress_fused_and_decode_append():
 # ---------------------------------------------------------------------------
 # a2/a3: indexer + top-k, both paths
 # ---------------------------------------------------------------------------
-def _check_index(p, idx, score):
+def _check_index(p, idx, score, fp8=None):
+    """fp8: the oracle's (codes, scales) of the keys; the oracle then scores and selects on them."""
     inp = wl.to_numpy(p)
     idx = idx.cpu().numpy()
     score = score.cpu().numpy()
     total_q = int(inp["cu_q"][-1])
-    orc = oracle.hybrid_queries(inp, do_hca=False)
+    orc = oracle.hybrid_queries(inp, do_hca=False) if fp8 is None else None
     kinds = {"equal": 0, "tie": 0, "fp32tie": 0}
     for qi in range(total_q):
         b = int(np.searchsorted(inp["cu_q"], qi, side="right") - 1)
         L = inp["cu_kv"][b + 1] - inp["cu_kv"][b]
         t = L - (inp["cu_q"][b + 1] - inp["cu_q"][b]) + (qi - inp["cu_q"][b])
         n = int((t + 1) // p["mC"])
-        kseq = inp["kI"][inp["cu_csa"][b]:inp["cu_csa"][b] + n]
-        s = oracle.index_scores(inp["qI"][qi], kseq) if n else np.zeros(0)
-        kind, _ = P.check_topk_row(idx[qi], orc["idx"][qi], s, n, p["top_k"], inp["qI"][qi], kseq)
+        rows = slice(inp["cu_csa"][b], inp["cu_csa"][b] + n)
+        kseq = inp["kI"][rows]
+        if fp8 is None:
+            s = oracle.index_scores(inp["qI"][qi], kseq) if n else np.zeros(0)
+            o_idx, dq = orc["idx"][qi], None
+        else:
+            s = oracle.index_scores_fp8(inp["qI"][qi], fp8[0][rows], fp8[1][rows]) if n else np.zeros(0)
+            o_idx, dq = oracle.topk(s, p["top_k"]), P.fp8_dequant(fp8[0][rows], fp8[1][rows])
+        kind, _ = P.check_topk_row(idx[qi], o_idx, s, n, p["top_k"], inp["qI"][qi], kseq, dq)
         kinds[kind] += 1
         v = idx[qi] >= 0
         # returned scores are the fp32 scores of the returned indices
@@ -152,6 +159,87 @@ def test_index_topk_all_ties_lowest_index_wins(queries):
         n = (t + 1) // 4
         want = list(range(min(64, n))) + [-1] * (64 - min(64, n))
         assert list(idx[qi]) == want
+
+
+# ---------------------------------------------------------------------------
+# f2: FP8 indexer keys
+# ---------------------------------------------------------------------------
+def _plant_fp8_rows(kI):
+    """Rows that exercise the quantiser's special cases (kI: [n, dI] bf16, n >= 6)."""
+    dI = kI.shape[1]
+    kI[0] = 0.0                                        # all zero: codes 0, scale 0
+    kI[1] = 0.0
+    kI[1, dI - 1] = -2.5                               # one non-zero: it maps to -448
+    kI[2, 0] = 1.0
+    kI[2, 1:] = -1e-6                                  # far below the smallest subnormal: -0
+    kI[3] = torch.tensor(([448.0, 1.0625, 1.1875, 17.0, 2.0 ** -10, 3 * 2.0 ** -10, -1.0625, -0.0]
+                          * dI)[:dI])                  # scale 1: exact midpoints, ties to even
+    kI[4] = -kI[4].abs()
+    kI[4, 0] = -kI[4].abs().max() * 2                  # the largest magnitude is negative
+    kI[5] *= 1e-30                                     # tiny but normal row scale
+    return kI
+
+
+@pytest.mark.parametrize("dI", [32, 64, 128])
+def test_quantize_index_keys_bit_exact(dI):
+    lengths = [1, 4, 5, 27, 1000, 4099]                # 1282 rows: several blocks of 8 and a ragged tail
+    p = problem(lengths, [1] * len(lengths), HI=2, dI=dI, seed=40 + dI)
+    p["kI"] = _plant_fp8_rows(p["kI"].clone())
+    g = P.GpuProblem(p)
+    codes, scale = csa.quantize_index_keys(g.full, g.kI)
+    torch.cuda.synchronize()
+    o_codes, o_scale = oracle.quantize_index_keys(wl.bits(p["kI"]))
+    got_c, got_s = codes.cpu().numpy(), scale.cpu().numpy()
+    assert got_c.shape == o_codes.shape
+    bad = np.argwhere(got_c != o_codes)
+    assert len(bad) == 0, f"{len(bad)} codes differ, first {bad[:4].tolist()}"
+    assert np.array_equal(got_s.view(np.uint32), o_scale.view(np.uint32))
+
+
+@pytest.mark.parametrize("HI,dI,k", [(2, 32, 64), (4, 64, 512), (4, 128, 1024), (1, 128, 7)])
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_index_topk_fp8(HI, dI, k, mode):
+    if mode == "decode":
+        lengths = [1, 5, 100, 4096, 5001, 20000, 70001]
+        n_q = [1] * len(lengths)
+    else:
+        lengths = [1500, 700]
+        n_q = lengths
+    p = problem(lengths, n_q, HI=HI, dI=dI, k=k, seed=50 + dI)
+    g = P.GpuProblem(p)
+    codes, scale = csa.quantize_index_keys(g.full, g.kI)
+    idx, score = csa.lightning_index_topk_fp8(g.layout, g.qI, codes, scale, k)
+    torch.cuda.synchronize()
+    fp8 = oracle.quantize_index_keys(wl.bits(p["kI"]))
+    kinds = _check_index(p, idx, score, fp8=fp8)
+    if mode == "decode":
+        assert kinds["equal"] >= len(lengths) - 1
+
+
+@pytest.mark.parametrize("case", ["decode_small", "chunked"])
+def test_hybrid_fp8_small(case):
+    if case == "decode_small":
+        p = problem([4, 4097, 8191, 30001], [1] * 4, H=128, d=512, HI=4, dI=64, k=256, seed=35)
+    else:
+        p = problem([1000, 2000], [37, 300], H=64, d=512, HI=4, dI=64, k=64, seed=36)
+    g = P.GpuProblem(p)
+    h = g.hybrid(prebuilt=True, fp8=True)
+    rep = P.check_hybrid(p, h, fp8=oracle.quantize_index_keys(wl.bits(p["kI"])))
+    assert rep["topk"]["equal"] >= rep["queries"] - 2
+    o1 = h.o_csa.clone()
+    h()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, h.o_csa)
+
+
+def test_workload_decode_64k_fp8_every_query():
+    w = wl.WORKLOADS["decode_64k"]
+    p = wl.make_problem(w)
+    g = P.GpuProblem(p)
+    h = g.hybrid(prebuilt=True, fp8=True)
+    rep = P.check_hybrid(p, h, check_entries="sampled", fp8=oracle.quantize_index_keys(wl.bits(p["kI"])))
+    assert csa.check_device_error() == 0
+    print("decode_64k fp8", rep)
 
 
 # ---------------------------------------------------------------------------

@@ -312,3 +312,110 @@ def test_structural_counts_golden(orc):
     assert n_csa == rows["csa_entries"]
     assert abs(out["lseH"][0, 0] - math.log(rows["hca_entries"])) < 1e-9
     assert rows["csa_entries"] * 4 == L and rows["hca_entries"] * 128 == L
+
+
+# ----------------------------------------------------------------------------
+# FP8 indexer keys (DeepSeek-V4 core architecture, §9 key innovations, row 5:
+# the indexer's QK product is quantised).  The E4M3 format's definition and
+# torch's float8_e4m3fn conversion pin the codec; closed forms pin the scaling.
+# ----------------------------------------------------------------------------
+
+def test_e4m3_decode_matches_torch_for_every_code(orc):
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([orc.e4m3_decode(c) for c in range(256)])
+    assert np.array_equal(got, ref, equal_nan=True)
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+    assert np.signbit(got[0x80]) and got[0x80] == 0.0
+
+
+def test_e4m3_encode_round_trip_and_saturation(orc):
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        assert orc.e4m3_encode(orc.e4m3_decode(c)) == c, hex(c)
+    assert orc.e4m3_encode(449.0) == 0x7E and orc.e4m3_encode(1e30) == 0x7E
+    assert orc.e4m3_encode(-470.0) == 0xFE
+    assert orc.e4m3_encode(-1e-9) == 0x80 and orc.e4m3_encode(1e-9) == 0x00
+
+
+def test_e4m3_encode_ties_to_even(orc):
+    # midpoints between neighbouring codes go to the code with an even mantissa
+    assert orc.e4m3_encode(1.0625) == 0x38           # 1.0 (m=0) | 1.125 (m=1)
+    assert orc.e4m3_encode(1.1875) == 0x3A           # 1.125 (m=1) | 1.25 (m=2)
+    assert orc.e4m3_encode(17.0) == orc.e4m3_encode(16.0)
+    assert orc.e4m3_encode(2.0 ** -10) == 0x00       # half the smallest subnormal
+    assert orc.e4m3_encode(3 * 2.0 ** -10) == 0x02   # subnormal m=1 | m=2
+    assert orc.e4m3_encode(-1.0625) == 0xB8
+    # 0.25 ulp off a midpoint goes to the nearer side
+    assert orc.e4m3_encode(1.0625 + 2.0 ** -6) == 0x39
+
+
+def test_e4m3_encode_matches_torch_on_random_and_midpoint_values(orc):
+    rng = np.random.default_rng(17)
+    tab = np.array([orc.e4m3_decode(c) for c in range(0x7F)])
+    mids = (tab[:-1] + tab[1:]) / 2
+    x = np.concatenate([rng.uniform(-448, 448, 4000), rng.standard_normal(4000) * 0.01,
+                        mids, -mids, tab, -tab]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.e4m3_encode(float(v)) for v in x], np.uint8)
+    bad = np.flatnonzero(got != ref)
+    assert len(bad) == 0, (x[bad[:4]], got[bad[:4]], ref[bad[:4]])
+
+
+def test_quantize_index_keys_hand_example(orc):
+    k = bf([[0.5, -1.0, 0.25, 0.0], [0.0, 0.0, 0.0, 0.0], [448.0, 17.0, -1.0625, 2.0 ** -10]])
+    codes, scale = orc.quantize_index_keys(k)
+    # row 0: a = 1, inv = 448: 224 = 1.75*2^7, -448, 112 = 1.75*2^6, 0
+    assert codes[0].tolist() == [0x76, 0xFE, 0x6E, 0x00]
+    assert scale[0] == np.float32(1.0) / np.float32(448.0)
+    assert codes[1].tolist() == [0, 0, 0, 0] and scale[1] == 0.0
+    # row 2: a = 448, inv = 1, scale = 1: the values themselves, ties to even
+    assert codes[2].tolist() == [0x7E, orc.e4m3_encode(16.0), 0xB8, 0x00] and scale[2] == 1.0
+
+
+def test_quantize_index_keys_matches_fp32_torch_route(orc):
+    # the same steps through torch's float32 arithmetic and its E4M3 conversion
+    rng = np.random.default_rng(18)
+    for dI in (32, 64, 128):
+        kb = bf(rng.standard_normal((300, dI)) * rng.uniform(1e-3, 1e3, (300, 1)))
+        codes, scale = orc.quantize_index_keys(kb)
+        kf = torch.from_numpy(f(kb)).float()
+        a = kf.abs().amax(1)
+        inv = torch.tensor(448.0, dtype=torch.float32) / a
+        ref = (kf * inv[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(codes, ref)
+        assert np.array_equal(scale, (a / torch.tensor(448.0, dtype=torch.float32)).numpy())
+
+
+def test_quantize_dequantize_error_bound(orc):
+    # E4M3 keeps 3 mantissa bits: relative error <= 2^-4 in the normal range,
+    # absolute error <= 2^-10 * scale in the subnormal range; the row max survives
+    rng = np.random.default_rng(19)
+    kb = bf(rng.standard_normal((200, 64)))
+    codes, scale = orc.quantize_index_keys(kb)
+    tab = np.array([orc.e4m3_decode(c) for c in range(256)])
+    kq = scale.astype(np.float64)[:, None] * tab[codes]
+    kf = f(kb)
+    err = np.abs(kq - kf)
+    bound = np.maximum(2.0 ** -4 * np.abs(kf), 2.0 ** -10 * scale[:, None]) * (1 + 2.0 ** -20)
+    assert (err <= bound).all()
+    amax = np.abs(kf).max(1)
+    assert np.allclose(np.abs(kq).max(1), amax, rtol=2.0 ** -22, atol=0)
+
+
+def test_index_scores_fp8_is_dot_with_dequantised_keys(orc):
+    rng = np.random.default_rng(20)
+    HI, dI, n = 3, 32, 40
+    qI = bf(rng.standard_normal((HI, dI)))
+    kb = bf(rng.standard_normal((n, dI)))
+    codes, scale = orc.quantize_index_keys(kb)
+    tab = np.array([orc.e4m3_decode(c) for c in range(256)])
+    kq = scale.astype(np.float64)[:, None] * tab[codes]
+    s = orc.index_scores_fp8(qI, codes, scale)
+    assert np.allclose(s, kq @ f(qI).sum(0), rtol=1e-12, atol=1e-12)
+    # keys that E4M3 holds exactly with scale 1 (row max 448) score as the bf16 indexer does
+    kx = bf(np.concatenate([np.full((n, 1), 448.0), rng.integers(-8, 9, (n, dI - 1)) / 4.0], 1))
+    c2, s2 = orc.quantize_index_keys(kx)
+    assert (s2 == 1.0).all()
+    assert np.array_equal(orc.index_scores_fp8(qI, c2, s2), orc.index_scores(qI, kx))
