@@ -560,6 +560,34 @@ index_filter_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
 // and a cluster-wide prefix of the CTAs' counts.  The cluster returns the
 // histogram to zero.
 // ---------------------------------------------------------------------------
+// Sums V partial values per lane over groups of lanes (lane bits below 2M)
+// so that the sums end spread over the group: at a mask bit m with v > 1
+// values left, the lanes with bit m set keep the upper half of the values and
+// send the lower half, the others the reverse, and each adds what it
+// receives; with one value left the remaining bits are plain xor reductions.
+// Lane L ends with its first max(1, V / 2M) entries holding the full sums of
+// the original entries j + off(L), off(L) = sum over the halving steps of
+// (bit m of L) * v / 2.
+template <int V, int M>
+__device__ __forceinline__ void row_butterfly(float *a, int lane)
+{
+    if constexpr (M >= 1) {
+        if constexpr (V > 1) {
+            const bool hi = (lane & M) != 0;
+#pragma unroll
+            for (int j = 0; j < V / 2; j++) {
+                const float send = hi ? a[j] : a[j + V / 2];
+                const float keep = hi ? a[j + V / 2] : a[j];
+                a[j] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+            }
+            row_butterfly<V / 2, M / 2>(a, lane);
+        } else {
+            a[0] += __shfl_xor_sync(0xffffffffu, a[0], M);
+            row_butterfly<1, M / 2>(a, lane);
+        }
+    }
+}
+
 constexpr int kChunkBytes = 32 * 1024;
 constexpr int kScanStages = 3;   // chunks in flight per CTA (two CTAs per SM)
 
@@ -618,19 +646,35 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
 #pragma unroll
     for (int x = 0; x < 8; x++) qv[x] = s_q[cg * 8 + x];
     uint32_t *keys = w.keys + qg * w.key_stride + r_begin;
-    // FP8: warp `warp` scores rows it * NWARP * RPW + warp * RPW + sub of a
-    // chunk (it < ITERS); their scales are loaded one chunk ahead into
-    // registers, scale u = it * RPW + sub of the warp in lane u % 32, slot u / 32
-    constexpr int ITERS = ROWS / (NWARP * RPW);
-    constexpr int SPL = FP8 ? (ITERS * RPW + 31) / 32 : 1;
-    static_assert(ROWS % (NWARP * RPW) == 0 && 32 % RPW == 0, "scan tiling");
-    float sc_cur[SPL], sc_nxt[SPL];
-    auto load_scales = [&](int c, float (&sc)[SPL]) {
+    // Warp `warp` scores the rows wbase .. wbase + ROWS_W - 1 of every chunk,
+    // RPW rows per step (LPR lanes per row, 8 elements per lane), all ITERS
+    // steps' loads and products first.  A transposing butterfly then sums
+    // each row over its LPR lanes and leaves whole row sums spread over the
+    // lanes: lane L ends with VF of them, those of steps j + it_off(L),
+    // j < VF; when LPR > ITERS, DUP lanes hold each sum and only the first
+    // of them emits it.
+    constexpr int ROWS_W = ROWS / NWARP;
+    constexpr int ITERS = ROWS_W / RPW;
+    constexpr int VF = ITERS >= LPR ? ITERS / LPR : 1;
+    constexpr int DUP = LPR > ITERS ? LPR / ITERS : 1;
+    static_assert(ROWS % NWARP == 0 && ROWS_W % RPW == 0 && (ITERS & (ITERS - 1)) == 0, "scan tiling");
+    const int wbase = warp * ROWS_W;
+    int it_off = 0;
+#pragma unroll
+    for (int m = LPR / 2, v = ITERS; m >= 1; m >>= 1)
+        if (v > 1) {
+            if (lane & m) it_off += v / 2;
+            v /= 2;
+        }
+    const bool emits = (lane & (DUP - 1)) == 0;
+    auto row_of = [&](int j) { return wbase + (j + it_off) * RPW + sub; };
+    // FP8: the scales of this lane's VF rows, loaded one chunk ahead
+    float sc_cur[VF], sc_nxt[VF];
+    auto load_scales = [&](int c, float (&sc)[VF]) {
         const int rows = rows_of(c);
 #pragma unroll
-        for (int j = 0; j < SPL; j++) {
-            const int u = 32 * j + lane;
-            const int row = (u / RPW) * (NWARP * RPW) + warp * RPW + u % RPW;
+        for (int j = 0; j < VF; j++) {
+            const int row = row_of(j);
             sc[j] = row < rows ? __ldg(sbase + (int64_t)c * ROWS + row) : 0.f;
         }
     };
@@ -650,16 +694,16 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
         }
         const int rows = rows_of(c);
         const uint8_t *src = s_rows + s * kChunkBytes;
-        uint32_t *kc = keys + (int64_t)c * ROWS;
-        if constexpr (FP8) {
+        float a[ITERS];
 #pragma unroll
-            for (int it = 0; it < ITERS; it++) {
-                const int row = it * (NWARP * RPW) + warp * RPW + sub;
-                const bool in = row < rows;
+        for (int it = 0; it < ITERS; it++) {
+            const int row = wbase + it * RPW + sub;
+            const bool in = row < rows;
+            float acc = 0.f;
+            if constexpr (FP8) {
                 // 8 codes per lane; E4M3 -> f16 is exact
                 const uint2 v = in ? *reinterpret_cast<const uint2 *>(src + row * RB + cg * 8) : make_uint2(0, 0);
                 const uint32_t wd[2] = {v.x, v.y};
-                float acc = 0.f;
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
                     const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)(wd[k >> 1] >> (16 * (k & 1)));
@@ -667,21 +711,7 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
                     acc = fmaf(qv[2 * k], f.x, acc);
                     acc = fmaf(qv[2 * k + 1], f.y, acc);
                 }
-#pragma unroll
-                for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                const float scl = __shfl_sync(0xffffffffu, sc_cur[(it * RPW) / 32], (it * RPW) % 32 + sub);
-                const bool valid = cg == 0 && in;
-                const uint32_t key = score_key(acc * scl);
-                if (valid) kc[row] = key;
-                if (valid) atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);
-            }
-#pragma unroll
-            for (int j = 0; j < SPL; j++) sc_cur[j] = sc_nxt[j];
-        } else {
-            for (int rb = warp * RPW; rb < ROWS; rb += NWARP * RPW) {
-                const int row = rb + sub;
-                const bool in = row < rows;
-                float acc = 0.f;
+            } else {
                 const uint4 v = in ? *reinterpret_cast<const uint4 *>(src + row * RB + cg * 16) : make_uint4(0, 0, 0, 0);
                 const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -689,13 +719,23 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
                     acc = fmaf(qv[2 * k], bf16_lo(wd[k]), acc);
                     acc = fmaf(qv[2 * k + 1], bf16_hi(wd[k]), acc);
                 }
-#pragma unroll
-                for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                const bool valid = cg == 0 && in;
-                const uint32_t key = score_key(acc);
-                if (valid) kc[row] = key;
-                if (valid) atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);   // few lanes per step: no aggregation
             }
+            a[it] = acc;
+        }
+        row_butterfly<ITERS, LPR / 2>(a, lane);
+        uint32_t *kc = keys + (int64_t)c * ROWS;
+#pragma unroll
+        for (int j = 0; j < VF; j++) {
+            const int row = row_of(j);
+            const uint32_t key = score_key(FP8 ? a[j] * sc_cur[j] : a[j]);
+            if (emits && row < rows) {
+                kc[row] = key;
+                atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);
+            }
+        }
+        if constexpr (FP8) {
+#pragma unroll
+            for (int j = 0; j < VF; j++) sc_cur[j] = sc_nxt[j];
         }
         __syncthreads();   // stage s has been read
         if (tid == 0 && c + kScanStages < nchunks) issue(c + kScanStages);
