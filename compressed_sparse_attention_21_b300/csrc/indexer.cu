@@ -684,14 +684,9 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
         if constexpr (FP8) {
             if (c + 1 < nchunks) load_scales(c + 1, sc_nxt);
         }
+        // each thread's own wait makes the stage's bytes visible to it; a
+        // wait that gave up is acted on at the barrier that ends the chunk
         const bool landed = mbar_wait(smem_u32(s_bar + s), (uint32_t)((c / kScanStages) & 1));
-        if (__syncthreads_or(!landed)) {
-            // the histogram stays incomplete: the select kernel sees a count
-            // mismatch and pads the row
-            if (tid == 0) set_error(err, CSA_ERR_TIMEOUT);
-            griddep_wait();
-            return;
-        }
         const int rows = rows_of(c);
         const uint8_t *src = s_rows + s * kChunkBytes;
         float a[ITERS];
@@ -737,7 +732,14 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
 #pragma unroll
             for (int j = 0; j < VF; j++) sc_cur[j] = sc_nxt[j];
         }
-        __syncthreads();   // stage s has been read
+        // stage s has been read by every thread
+        if (__syncthreads_or(!landed)) {
+            // the histogram stays incomplete: the select kernel sees a count
+            // mismatch and pads the row
+            if (tid == 0) set_error(err, CSA_ERR_TIMEOUT);
+            griddep_wait();
+            return;
+        }
         if (tid == 0 && c + kScanStages < nchunks) issue(c + kScanStages);
     }
     uint32_t *ghist = w.hist + qg * kHistBins;
