@@ -101,3 +101,53 @@ def test_ops_refuse_cpu_tensors():
     kv = torch.zeros(8, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         _lib.csa_compress(L, kv, torch.zeros(8), torch.zeros(2, 128, dtype=torch.bfloat16))
+
+
+def test_fp8_index_entry_points_check_arguments_on_host(lib):
+    L = layout()
+    n = ctypes.c_size_t(0)
+    # quantiser: unsupported width, missing codes, misaligned or missing scales
+    assert lib.csa_quantize_index_keys(ctypes.byref(L), 256, 48, 256, 256, None) == 2
+    assert lib.csa_quantize_index_keys(ctypes.byref(L), 256, 64, None, 256, None) == 1
+    assert lib.csa_quantize_index_keys(ctypes.byref(L), 256, 64, 256, 258, None) == 1
+    assert lib.csa_quantize_index_keys(ctypes.byref(L), 256, 64, 256, None, None) == 1
+    # FP8 indexer: missing or misaligned scales, missing codes, unsupported sizes
+    assert lib.lightning_index_topk_fp8(ctypes.byref(L), 256, 256, None, 2, 32, 4, 8, 256, None, None, 0,
+                                        None) == 1
+    assert lib.lightning_index_topk_fp8(ctypes.byref(L), 256, 256, 258, 2, 32, 4, 8, 256, None, None, 0,
+                                        None) == 1
+    assert lib.lightning_index_topk_fp8(ctypes.byref(L), 256, None, 256, 2, 32, 4, 8, 256, None, None, 0,
+                                        None) == 1
+    assert lib.lightning_index_topk_fp8(ctypes.byref(L), 256, 256, 256, 2, 48, 4, 8, 256, None, None, 0,
+                                        None) == 2
+    assert lib.csa_index_fp8_workspace_size(ctypes.byref(L), 2, 32, 4, 8, None) == 1
+    assert lib.csa_index_fp8_workspace_size(ctypes.byref(L), 2, 32, 4, 8, ctypes.byref(n)) == 0
+    # rows longer than the FP8 select holds (262144 entries at ratio 4) are refused
+    long_L = layout(max_kv_len=4 * 262144 + 4, total_kv=4 * 262144 + 4, total_csa=262145)
+    assert lib.csa_index_fp8_workspace_size(ctypes.byref(long_L), 2, 32, 4, 8, ctypes.byref(n)) == 2
+    assert lib.lightning_index_topk_fp8(ctypes.byref(long_L), 256, 256, 256, 2, 32, 4, 8, 256, None, None, 0,
+                                        None) == 2
+
+
+def test_hybrid_flags_checked_on_host(lib):
+    p = _lib.csa_hybrid_params()
+    p.layout = layout()
+    p.d, p.n_heads, p.n_heads_idx, p.d_idx, p.ratio_csa, p.ratio_hca, p.top_k = 128, 8, 2, 32, 4, 128, 8
+    p.scale = 1.0
+    for name in ("kv", "gate", "q_idx", "k_idx", "q", "csa_cache", "hca_cache", "idx_out", "o_csa", "o_hca"):
+        setattr(p, name, 256)
+    p.flags = 0x4                                            # no such flag
+    assert lib.hybrid_attend(ctypes.byref(p), None) == 1
+    p.flags = _lib.CSA_INDEX_FP8                             # FP8 keys named but not given
+    assert lib.hybrid_attend(ctypes.byref(p), None) == 1
+    p.k_idx_fp8 = 256
+    p.k_idx_scale = 258                                      # scales misaligned
+    assert lib.hybrid_attend(ctypes.byref(p), None) == 1
+    # with valid arguments the host checks pass and, without a GPU, the call
+    # stops at the device (status 4).  Where a GPU is present these fake
+    # pointers must never reach a launch, so the control runs only without one.
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        p.k_idx_scale = 256
+        assert lib.hybrid_attend(ctypes.byref(p), None) == 4
+        assert lib.csa_quantize_index_keys(ctypes.byref(layout()), 256, 64, 256, 256, None) == 4
