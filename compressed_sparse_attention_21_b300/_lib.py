@@ -50,7 +50,8 @@ class csa_hybrid_params(ctypes.Structure):
 
 # Every symbol include/csa.h declares (checked by the CPU test suite).
 EXPORTS = ("csa_compress", "hca_compress", "lightning_index_topk", "csa_index_workspace_size",
-           "lightning_index_topk_static", "csa_quantize_index_keys", "lightning_index_topk_fp8",
+           "lightning_index_topk_static", "csa_quantize_index_keys", "csa_quantize_index_keys_closed",
+           "lightning_index_topk_fp8",
            "csa_index_fp8_workspace_size",
            "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size", "hybrid_attend",
            "csa_workspace_size", "csa_workspace_init", "csa_status_string", "csa_check_device_error",
@@ -74,6 +75,7 @@ def load():
     lib.csa_index_workspace_size.argtypes = [LP, I, I, I, I, ctypes.POINTER(Z)]
     lib.lightning_index_topk_static.argtypes = [LP, P, P, I, I, I, I, P, P, P]
     lib.csa_quantize_index_keys.argtypes = [LP, P, I, P, P, P]
+    lib.csa_quantize_index_keys_closed.argtypes = [LP, P, I, I, P, P, P]
     lib.lightning_index_topk_fp8.argtypes = [LP, P, P, P, I, I, I, I, P, P, P, Z, P]
     lib.csa_index_fp8_workspace_size.argtypes = [LP, I, I, I, I, ctypes.POINTER(Z)]
     lib.sparse_mqa_attend.argtypes = [LP, P, P, P, P, I, I, I, I, F, P, P, P, Z, P]
@@ -92,8 +94,8 @@ def load():
     lib.csa_timing_read.restype = I
     lib.csa_timing_reset.restype = None
     for f in ("csa_compress", "hca_compress", "lightning_index_topk", "csa_index_workspace_size",
-              "lightning_index_topk_static", "csa_quantize_index_keys", "lightning_index_topk_fp8",
-              "csa_index_fp8_workspace_size", "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size",
+              "lightning_index_topk_static", "csa_quantize_index_keys", "csa_quantize_index_keys_closed",
+              "lightning_index_topk_fp8", "csa_index_fp8_workspace_size", "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size",
               "hybrid_attend",
               "csa_workspace_size", "csa_workspace_init", "csa_check_device_error", "csa_timing_enable"):
         getattr(lib, f).restype = I
@@ -225,6 +227,15 @@ def quantize_index_keys(layout, k_idx, k_fp8=None, k_scale=None, stream=None):
         k_scale = torch.empty((layout.total_csa,), dtype=torch.float32, device=dev)
     _check(load().csa_quantize_index_keys(ctypes.byref(layout.c), _ptr(k_idx), dI, _ptr(k_fp8), _ptr(k_scale),
                                           _stream(stream)), "csa_quantize_index_keys")
+    return k_fp8, k_scale
+
+
+def quantize_closed_index_keys(layout, k_idx, k_fp8, k_scale, ratio=None, stream=None):
+    """Update k_fp8 / k_scale in place for the entries the layout's query positions close."""
+    ratio = layout.ratio_csa if ratio is None else ratio
+    _check(load().csa_quantize_index_keys_closed(ctypes.byref(layout.c), _ptr(k_idx), k_idx.shape[-1], ratio,
+                                                 _ptr(k_fp8), _ptr(k_scale), _stream(stream)),
+           "csa_quantize_index_keys_closed")
     return k_fp8, k_scale
 
 

@@ -369,6 +369,24 @@ csa_status_t csa_quantize_index_keys(const csa_layout *layout, const csa_bf16 *k
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
+csa_status_t csa_quantize_index_keys_closed(const csa_layout *layout, const csa_bf16 *k_idx, int d_idx, int ratio,
+                                            uint8_t *k_fp8, float *k_scale, csa_stream_t stream)
+{
+    CSA_TRY(check_layout(layout, true, false));
+    if (ratio <= 0 || ratio > 1024) return CSA_ERR_INVALID_ARG;
+    if (d_idx != 32 && d_idx != 64 && d_idx != 128) return CSA_ERR_UNSUPPORTED;
+    const bool any = layout->total_q > 0 && layout->total_csa > 0;
+    CSA_TRY(check_ptr(k_idx, any));
+    CSA_TRY(check_ptr(k_fp8, any));
+    if (any && (!k_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u))) return CSA_ERR_INVALID_ARG;
+    if (!any) return CSA_OK;
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    return from_cuda(launch_quantize_closed_keys(layout->batch, layout->cu_kv, layout->cu_q, layout->cu_csa,
+                                                 layout->total_q, ratio, k_idx, d_idx, k_fp8, k_scale, ds->err,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 csa_status_t lightning_index_topk_fp8(const csa_layout *layout, const csa_bf16 *q_idx, const uint8_t *k_fp8,
                                       const float *k_scale, int n_heads_idx, int d_idx, int ratio, int top_k,
                                       int32_t *idx_out, float *score_out, void *ws, size_t ws_bytes,
@@ -660,7 +678,7 @@ csa_status_t csa_check_device_error(csa_stream_t stream, csa_status_t *device_st
     return CSA_OK;
 }
 
-int csa_version(void) { return 110; }   // 1.1: FP8 indexer keys
+int csa_version(void) { return 111; }   // 1.1: FP8 indexer keys; .1: the closed-rows quantiser
 
 csa_status_t csa_timing_enable(int enable)
 {

@@ -1159,16 +1159,14 @@ size_t index_workspace_bytes(const IndexArgs &a)
 // inv = 448 / a and scale = a / 448 (IEEE fp32), each value k * inv is
 // converted to E4M3 rounding to nearest even and saturating at +-448.
 // ---------------------------------------------------------------------------
+// One key row by one warp (every lane calls it with the same row).
 template <int DI>
-__global__ void __launch_bounds__(256)
-quantize_index_keys_kernel(const uint16_t *__restrict__ k_idx, int64_t rows, uint8_t *__restrict__ k_fp8,
-                           float *__restrict__ k_scale)
+__device__ __forceinline__ void quantize_row(const uint16_t *__restrict__ k_idx, int64_t row, uint8_t *__restrict__ k_fp8,
+                                             float *__restrict__ k_scale)
 {
     constexpr int V = DI / 32;
     static_assert(DI % 32 == 0 && V >= 1 && V <= 4, "row width");
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (row >= rows) return;
     const uint16_t *src = k_idx + row * DI + lane * V;
     float v[V];
     float amax = 0.f;
@@ -1191,6 +1189,39 @@ quantize_index_keys_kernel(const uint16_t *__restrict__ k_idx, int64_t rows, uin
     if (lane == 0) k_scale[row] = __fdiv_rn(amax, 448.f);
 }
 
+// Every row of the key array.
+template <int DI>
+__global__ void __launch_bounds__(256)
+quantize_index_keys_kernel(const uint16_t *__restrict__ k_idx, int64_t rows, uint8_t *__restrict__ k_fp8,
+                           float *__restrict__ k_scale)
+{
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    quantize_row<DI>(k_idx, row, k_fp8, k_scale);
+}
+
+// Only the rows of the entries that the layout's query positions close: the
+// query at position t closes entry (t + 1) / ratio - 1 of its sequence when
+// (t + 1) is a multiple of ratio, and no other query closes that entry.  One
+// warp per query.
+template <int DI>
+__global__ void __launch_bounds__(256)
+quantize_closed_keys_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                            const int64_t *__restrict__ cu_csa, int64_t total_q, int ratio,
+                            const uint16_t *__restrict__ k_idx, uint8_t *__restrict__ k_fp8,
+                            float *__restrict__ k_scale, int *err)
+{
+    const int64_t qi = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (qi >= total_q) return;
+    const QueryPos p = query_pos(cu_kv, cu_q, cu_csa, batch, qi);
+    if (!entry_count_ok(cu_csa, p, ratio)) {
+        if ((threadIdx.x & 31) == 0) set_error(err, CSA_ERR_DEVICE);
+        return;
+    }
+    if ((p.t + 1) % ratio != 0) return;
+    quantize_row<DI>(k_idx, p.e0 + (p.t + 1) / ratio - 1, k_fp8, k_scale);
+}
+
 cudaError_t launch_quantize_index_keys(const uint16_t *k_idx, int64_t rows, int d_idx, uint8_t *k_fp8,
                                        float *k_scale, cudaStream_t st)
 {
@@ -1202,6 +1233,22 @@ cudaError_t launch_quantize_index_keys(const uint16_t *k_idx, int64_t rows, int 
     case 32: return launch_kernel("quantize_index_keys", quantize_index_keys_kernel<32>, grid, dim3(256), 0, st, false, k_idx, rows, k_fp8, k_scale);
     case 64: return launch_kernel("quantize_index_keys", quantize_index_keys_kernel<64>, grid, dim3(256), 0, st, false, k_idx, rows, k_fp8, k_scale);
     case 128: return launch_kernel("quantize_index_keys", quantize_index_keys_kernel<128>, grid, dim3(256), 0, st, false, k_idx, rows, k_fp8, k_scale);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_quantize_closed_keys(int batch, const int64_t *cu_kv, const int64_t *cu_q, const int64_t *cu_csa,
+                                        int64_t total_q, int ratio, const uint16_t *k_idx, int d_idx, uint8_t *k_fp8,
+                                        float *k_scale, int *err, cudaStream_t st)
+{
+    if (total_q <= 0) return cudaSuccess;
+    const int64_t blocks = (total_q + 7) / 8;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)blocks);
+    switch (d_idx) {
+    case 32: return launch_kernel("quantize_closed_keys", quantize_closed_keys_kernel<32>, grid, dim3(256), 0, st, false, batch, cu_kv, cu_q, cu_csa, total_q, ratio, k_idx, k_fp8, k_scale, err);
+    case 64: return launch_kernel("quantize_closed_keys", quantize_closed_keys_kernel<64>, grid, dim3(256), 0, st, false, batch, cu_kv, cu_q, cu_csa, total_q, ratio, k_idx, k_fp8, k_scale, err);
+    case 128: return launch_kernel("quantize_closed_keys", quantize_closed_keys_kernel<128>, grid, dim3(256), 0, st, false, batch, cu_kv, cu_q, cu_csa, total_q, ratio, k_idx, k_fp8, k_scale, err);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -130,6 +130,10 @@ size_t index_fp8_workspace_bytes(const IndexArgs &a);
 // E4M3 codes and per-row fp32 scales of rows indexer keys (d_idx values each)
 cudaError_t launch_quantize_index_keys(const uint16_t *k_idx, int64_t rows, int d_idx, uint8_t *k_fp8,
                                        float *k_scale, cudaStream_t st);
+// the same, only for the rows of the entries the layout's query positions close
+cudaError_t launch_quantize_closed_keys(int batch, const int64_t *cu_kv, const int64_t *cu_q, const int64_t *cu_csa,
+                                        int64_t total_q, int ratio, const uint16_t *k_idx, int d_idx, uint8_t *k_fp8,
+                                        float *k_scale, int *err, cudaStream_t st);
 cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t st);
 // Library-owned scratch of lightning_index_topk_static (see indexer.cu):
 // its device address on the current device (looked up on first use), and the

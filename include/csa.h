@@ -217,6 +217,17 @@ csa_status_t lightning_index_topk_static(const csa_layout *layout, const csa_bf1
  * ------------------------------------------------------------------------- */
 csa_status_t csa_quantize_index_keys(const csa_layout *layout, const csa_bf16 *k_idx, int d_idx,
                                      uint8_t *k_fp8, float *k_scale, csa_stream_t stream);
+/* csa_quantize_index_keys_closed is the incremental form for decode and
+ * chunked prefill: it quantises, with the same arithmetic, only the rows of
+ * the entries that the layout's query positions close (the query at position
+ * t closes entry (t+1)/ratio - 1 of its sequence when (t+1) is a multiple of
+ * ratio; "DeepSeek-V4 core architecture", §2.2 step 1: an entry exists once
+ * its m tokens do) and leaves every other row of k_fp8 and k_scale as it is.
+ * ratio is the CSA ratio (1 .. 1024).  An entry count that is not L/ratio
+ * sets the device error word (CSA_ERR_DEVICE) and that query's row is not
+ * written. */
+csa_status_t csa_quantize_index_keys_closed(const csa_layout *layout, const csa_bf16 *k_idx, int d_idx, int ratio,
+                                            uint8_t *k_fp8, float *k_scale, csa_stream_t stream);
 csa_status_t lightning_index_topk_fp8(const csa_layout *layout, const csa_bf16 *q_idx,
                                       const uint8_t *k_fp8, const float *k_scale,
                                       int n_heads_idx, int d_idx, int ratio, int top_k,

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.csa_version() == 110
+    assert lib.csa_version() == 111
     assert lib.csa_status_string(0) == b"ok"
     assert lib.csa_status_string(3) == b"workspace missing or too small"
 
@@ -111,6 +111,11 @@ def test_fp8_index_entry_points_check_arguments_on_host(lib):
     assert lib.csa_quantize_index_keys(ctypes.byref(L), 256, 64, None, 256, None) == 1
     assert lib.csa_quantize_index_keys(ctypes.byref(L), 256, 64, 256, 258, None) == 1
     assert lib.csa_quantize_index_keys(ctypes.byref(L), 256, 64, 256, None, None) == 1
+    # the closed-rows form: bad ratio, unsupported width, misaligned scales
+    assert lib.csa_quantize_index_keys_closed(ctypes.byref(L), 256, 64, 0, 256, 256, None) == 1
+    assert lib.csa_quantize_index_keys_closed(ctypes.byref(L), 256, 48, 4, 256, 256, None) == 2
+    assert lib.csa_quantize_index_keys_closed(ctypes.byref(L), 256, 64, 4, 256, 258, None) == 1
+    assert lib.csa_quantize_index_keys_closed(ctypes.byref(L), None, 64, 4, 256, 256, None) == 1
     # FP8 indexer: missing or misaligned scales, missing codes, unsupported sizes
     assert lib.lightning_index_topk_fp8(ctypes.byref(L), 256, 256, None, 2, 32, 4, 8, 256, None, None, 0,
                                         None) == 1

@@ -196,6 +196,41 @@ def test_quantize_index_keys_bit_exact(dI):
     assert np.array_equal(got_s.view(np.uint32), o_scale.view(np.uint32))
 
 
+def closed_rows(lengths, n_q, m):
+    """Entry rows closed by the query positions: entry j of a sequence exists once
+    its m tokens do, so the query at t = (j+1)m - 1 closes it."""
+    rows, e0 = [], 0
+    for L, nq in zip(lengths, n_q):
+        rows += [e0 + (t + 1) // m - 1 for t in range(L - nq, L) if (t + 1) % m == 0]
+        e0 += L // m
+    return np.array(rows, dtype=np.int64)
+
+
+@pytest.mark.parametrize("dI", [32, 64, 128])
+@pytest.mark.parametrize("case", ["decode", "chunked", "prefill"])
+def test_quantize_closed_index_keys(dI, case):
+    lengths = [4, 5, 8, 127, 128, 4096, 4099, 1000]
+    n_q = {"decode": [1] * 8, "chunked": [4, 1, 8, 37, 64, 300, 3, 999], "prefill": lengths}[case]
+    p = problem(lengths, n_q, HI=2, dI=dI, seed=60 + dI)
+    p["kI"] = _plant_fp8_rows(p["kI"].clone())
+    g = P.GpuProblem(p)
+    n = g.full.total_csa
+    codes = torch.full((n, dI), 0x55, dtype=torch.uint8, device="cuda")
+    scale = torch.full((n,), -1.0, dtype=torch.float32, device="cuda")
+    csa.quantize_closed_index_keys(g.layout, g.kI, codes, scale)
+    torch.cuda.synchronize()
+    assert csa.check_device_error() == 0
+    rows = closed_rows(lengths, n_q, 4)
+    o_codes, o_scale = oracle.quantize_index_keys(wl.bits(p["kI"]))
+    got_c, got_s = codes.cpu().numpy(), scale.cpu().numpy()
+    assert np.array_equal(got_c[rows], o_codes[rows])
+    assert np.array_equal(got_s[rows].view(np.uint32), o_scale[rows].view(np.uint32))
+    other = np.setdiff1d(np.arange(n), rows)
+    assert (got_c[other] == 0x55).all() and (got_s[other] == -1.0).all(), "a row no query closes was written"
+    if case == "prefill":   # every entry is closed by some position: the same as quantising every row
+        assert len(rows) == n
+
+
 @pytest.mark.parametrize("HI,dI,k", [(2, 32, 64), (4, 64, 512), (4, 128, 1024), (1, 128, 7)])
 @pytest.mark.parametrize("mode", ["decode", "prefill"])
 def test_index_topk_fp8(HI, dI, k, mode):
