@@ -419,3 +419,46 @@ def test_index_scores_fp8_is_dot_with_dequantised_keys(orc):
     c2, s2 = orc.quantize_index_keys(kx)
     assert (s2 == 1.0).all()
     assert np.array_equal(orc.index_scores_fp8(qI, c2, s2), orc.index_scores(qI, kx))
+
+
+def test_quantize_is_exactly_invariant_to_power_of_two_row_scaling(orc):
+    # k -> 2^e k (exact in bf16) leaves a * inv unchanged in fp32, so the codes
+    # stay and the scale moves by exactly 2^e: catches a wrong amax, a wrong row
+    # or a scale formula that is not a / 448
+    rng = np.random.default_rng(21)
+    kb = bf(rng.standard_normal((50, 64)))
+    c0, s0 = orc.quantize_index_keys(kb)
+    for e in (-20, -3, 1, 7, 30):
+        c1, s1 = orc.quantize_index_keys(bf(f(kb) * 2.0 ** e))
+        assert np.array_equal(c1, c0)
+        assert np.array_equal(s1, (s0.astype(np.float64) * 2.0 ** e).astype(np.float32))
+
+
+def test_quantize_sign_flip_flips_only_sign_bits(orc):
+    rng = np.random.default_rng(22)
+    kb = bf(rng.standard_normal((40, 32)))
+    c0, s0 = orc.quantize_index_keys(kb)
+    c1, s1 = orc.quantize_index_keys(bf(-f(kb)))
+    assert np.array_equal(c1, c0 ^ 0x80) and np.array_equal(s1, s0)
+
+
+def test_e4m3_encode_is_monotone(orc):
+    rng = np.random.default_rng(23)
+    x = np.sort(np.concatenate([rng.uniform(-500, 500, 3000), rng.standard_normal(3000) * 1e-2]))
+    tab = np.array([orc.e4m3_decode(c) for c in range(256)])
+    vals = np.array([tab[orc.e4m3_encode(float(v))] for v in x])
+    assert (np.diff(vals) >= 0).all()
+    # and the nearest: no finite code lies strictly closer to x
+    fin = tab[np.isfinite(tab)]
+    for v, q in zip(x[::50], vals[::50]):
+        assert abs(q - v) <= np.min(np.abs(fin - np.clip(v, -448, 448))) + abs(v - np.clip(v, -448, 448)) + 1e-12
+
+
+def test_attention_ignores_the_order_of_the_selected_indices(orc):
+    p = tiny_problem(64, d=8, H=2, HI=2, dI=4, mC=4, k=8, seed=24, n_q=[3])
+    base = orc.hybrid_queries(p, do_hca=False)
+    rng = np.random.default_rng(24)
+    perm = np.stack([rng.permutation(row) for row in base["idx"]])
+    again = orc.hybrid_queries(p, given_idx=perm, do_hca=False)
+    assert np.allclose(again["oC"], base["oC"], rtol=0, atol=1e-12)
+    assert np.allclose(again["lseC"], base["lseC"], rtol=0, atol=1e-12)
