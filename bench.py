@@ -35,17 +35,17 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # keyed by (workload, call, indexer key format), with the sha256 of the sources at capture time;
 # a changed source makes the figure stale and it is reported as null.
 NCU_TRAFFIC = {
-    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,599,488 B read +
-    # index_select_kernel 1,352,192 B read, 0 B written (means of two captured calls)
+    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,598,976 B read +
+    # index_select_kernel 1,352,064 B read, 0 B written (means of two captured calls)
     ("decode_64k", "index_topk", "bf16"): {
-        "bytes_per_launch": 34951680,
-        "sources": {"indexer.cu": "0b797e5582691bba768f0c1e111f87796df5cad8fd5858ba2003e5828ec8aa84",
+        "bytes_per_launch": 34951040,
+        "sources": {"indexer.cu": "a1e1289bf84ad5178c2e4026409408b38ad3de278e5f61d6f4c0c2a571b4998d",
                     "common.cuh": "c163a7f706451d39f03aab7a1b3d9ca5dd901eb0067e2031b1f8ae5268757c9d"},
     },
-    # the same call on FP8 E4M3 keys: scan 17,879,168 B read + select 1,355,264 B read, 0 B written
+    # the same call on FP8 E4M3 keys: scan 17,875,328 B read + select 1,352,192 B read, 0 B written
     ("decode_64k", "index_topk", "fp8"): {
-        "bytes_per_launch": 19234432,
-        "sources": {"indexer.cu": "0b797e5582691bba768f0c1e111f87796df5cad8fd5858ba2003e5828ec8aa84",
+        "bytes_per_launch": 19227520,
+        "sources": {"indexer.cu": "a1e1289bf84ad5178c2e4026409408b38ad3de278e5f61d6f4c0c2a571b4998d",
                     "common.cuh": "c163a7f706451d39f03aab7a1b3d9ca5dd901eb0067e2031b1f8ae5268757c9d"},
     },
 }

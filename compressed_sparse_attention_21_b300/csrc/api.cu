@@ -144,6 +144,7 @@ IndexArgs index_args(const csa_layout *L, const csa_bf16 *q_idx, const csa_bf16 
     a.cu_csa = L->cu_csa;
     a.q_idx = q_idx;
     a.k_idx = k_idx;
+    a.fp8 = false;
     a.k_fp8 = nullptr;
     a.k_scale = nullptr;
     a.n_heads_idx = hi;
@@ -399,6 +400,7 @@ csa_status_t lightning_index_topk_fp8(const csa_layout *layout, const csa_bf16 *
     CSA_TRY(device_state(&ds));
     IndexArgs a = index_args(layout, q_idx, nullptr, n_heads_idx, d_idx, ratio, top_k, idx_out, score_out, ws,
                              ws_bytes, ds->err);
+    a.fp8 = true;
     a.k_fp8 = k_fp8;
     a.k_scale = k_scale;
     const size_t need = index_fp8_workspace_bytes(a);
@@ -605,6 +607,7 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
         ia.scan_done = ds->sdone;
         ia.pdl = compress;
         if (fp8) {
+            ia.fp8 = true;
             ia.k_fp8 = p->k_idx_fp8;
             ia.k_scale = p->k_idx_scale;
         }

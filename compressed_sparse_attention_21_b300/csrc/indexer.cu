@@ -1071,7 +1071,7 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
     // scan_done: after the last key scan of the multi-kernel paths; the
     // single-kernel paths mark it up front (their kernel holds the GPU to the end)
     auto mark = [&]() -> cudaError_t { return a.scan_done ? cudaEventRecord(a.scan_done, st) : cudaSuccess; };
-    const bool fp8 = a.k_fp8 != nullptr;   // FP8 keys: the chunk scan and the select only
+    const bool fp8 = a.fp8;   // FP8 keys: the chunk scan and the select only
     if (!fp8 && (index_block_applicable(a) || use_cta_path(a))) {
         cudaError_t e = mark();
         if (e != cudaSuccess) return e;
@@ -1105,7 +1105,7 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
             if (cpc > nch) cpc = nch;
             const int64_t gx = (nch + cpc - 1) / cpc;
             cudaError_t e =
-                a.k_fp8 ? launch_kernel("index_scan", index_chunk_scan_kernel<DI, true>, dim3((unsigned)gx, (unsigned)nq),
+                fp8 ? launch_kernel("index_scan", index_chunk_scan_kernel<DI, true>, dim3((unsigned)gx, (unsigned)nq),
                                         dim3(kScanThreads), (size_t)kScanStages * kChunkBytes, st, a.pdl, a.batch,
                                         a.cu_kv, a.cu_q, a.cu_csa, q0, a.q_idx, (const void *)a.k_fp8, a.k_scale,
                                         a.n_heads_idx, a.ratio, (int)cpc, w, a.err)

@@ -106,7 +106,8 @@ struct IndexArgs {
     cudaEvent_t scan_done;  // if set: recorded on the stream once every key has been scored
     const int64_t *cu_kv, *cu_q, *cu_csa;
     const uint16_t *q_idx, *k_idx;
-    const uint8_t *k_fp8;   // if set: the keys as E4M3 codes with k_scale (k_idx unused)
+    bool fp8;               // the keys are E4M3 codes k_fp8 with row scales k_scale (k_idx unused);
+    const uint8_t *k_fp8;   // null only when there are no entries
     const float *k_scale;
     int n_heads_idx, d_idx, ratio, top_k;
     int32_t *idx_out;
@@ -123,7 +124,7 @@ size_t index_block_ws_bytes(const IndexArgs &a);      // for a full grid of pers
 size_t index_block_min_ws_bytes();                      // one CTA (the kernel fits its grid to ws_bytes)
 cudaError_t launch_index_block(const IndexArgs &a, cudaStream_t st);
 size_t index_workspace_bytes(const IndexArgs &a);
-// FP8 keys (k_fp8 set): the chunk scan and the clustered select, rows of up
+// FP8 keys (fp8 set): the chunk scan and the clustered select, rows of up
 // to index_fp8_max_n() entries
 int64_t index_fp8_max_n();
 size_t index_fp8_workspace_bytes(const IndexArgs &a);

@@ -337,6 +337,51 @@ def test_hybrid_small(case):
     assert torch.equal(o1, h.o_csa)
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("nseq", [3, 1200])
+def test_hybrid_without_complete_blocks(fp8, nseq):
+    # no sequence reaches one block: no CSA or HCA entry exists, every query
+    # attends only the raw tokens of its own open block, and the selection is
+    # empty.  1200 sequences give 2400 queries, the size at which the bf16
+    # indexer takes its prefill paths (FP8 keys must still take their own).
+    lengths = ([1, 2, 3] * (nseq // 3))[:nseq]
+    p = problem(lengths, lengths, H=64, d=512, HI=4, dI=64, k=32, seed=70)
+    g = P.GpuProblem(p)
+    assert g.full.total_csa == 0 and g.full.total_hca == 0
+    h = g.hybrid(prebuilt=False, fp8=fp8)
+    P.check_hybrid(p, h, fp8=oracle.quantize_index_keys(wl.bits(p["kI"])) if fp8 else None)
+    assert (h.idx.cpu() == -1).all()
+    assert csa.check_device_error() == 0
+
+
+def test_hybrid_with_query_free_sequences():
+    # sequences without queries contribute entries to the packed arrays but no output rows
+    p = problem([300, 1000, 77, 4099], [0, 5, 0, 1], H=64, d=512, HI=4, dI=64, k=64, seed=71)
+    g = P.GpuProblem(p)
+    h = g.hybrid(prebuilt=True)
+    rep = P.check_hybrid(p, h)
+    assert rep["queries"] == 6
+    assert csa.check_device_error() == 0
+
+
+def test_calls_without_queries_do_nothing():
+    # total_q = 0: every call succeeds without launching and leaves its outputs alone
+    p = problem([100, 37], [0, 0], H=64, d=512, HI=4, dI=64, k=16, seed=72)
+    g = P.GpuProblem(p)
+    assert g.layout.total_q == 0
+    idx, _ = csa.lightning_index_topk(g.layout, g.qI, g.kI, 16)
+    codes, scale = csa.quantize_index_keys(g.full, g.kI)
+    idx8, _ = csa.lightning_index_topk_fp8(g.layout, g.qI, codes, scale, 16)
+    sentinel = torch.full((g.full.total_csa, 64), 7, dtype=torch.uint8, device="cuda")
+    sc = torch.full((g.full.total_csa,), 3.0, device="cuda")
+    csa.quantize_closed_index_keys(g.layout, g.kI, sentinel, sc)
+    h = g.hybrid(prebuilt=True)
+    torch.cuda.synchronize()
+    assert idx.shape[0] == 0 and idx8.shape[0] == 0 and h.o_csa.shape[0] == 0
+    assert (sentinel == 7).all() and (sc == 3.0).all()
+    assert csa.check_device_error() == 0
+
+
 def test_hybrid_ratio_one_is_dense_causal():
     # m_C = 1, k >= L: the CSA branch is dense causal MQA (and so is HCA with m_H = 1)
     L = 300
