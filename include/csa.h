@@ -282,7 +282,11 @@ csa_status_t csa_attend_workspace_size(const csa_layout *layout, int n_heads, in
  * attention) concurrently, and returns both branches' outputs.
  * ------------------------------------------------------------------------- */
 #define CSA_SKIP_COMPRESS 0x1   /* caches already hold every needed entry */
-#define CSA_INDEX_FP8 0x2       /* index with k_idx_fp8 / k_idx_scale (see csa_quantize_index_keys) */
+#define CSA_INDEX_FP8 0x2       /* index with k_idx_fp8 / k_idx_scale (see csa_quantize_index_keys);
+                                   the codes of every entry the step can see, including those its own
+                                   positions close, must be in place before the call (a decode loop runs
+                                   csa_quantize_index_keys_closed on the step's layout first); k_idx
+                                   is then not read */
 
 typedef struct csa_hybrid_params {
     csa_layout layout;
