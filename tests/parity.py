@@ -13,7 +13,11 @@ Acceptance (per query or entry):
     and reported; they arise where the k-th score sits near zero;
   * attention: max abs error <= 2e-2 and relative L2 error <= 5e-3, checked
     end-to-end where the selections agree and always on the GPU's own
-    selection (the oracle re-run with the GPU's indices).
+    selection (the oracle re-run with the GPU's indices);
+  * FP8 indexer keys: the library's E4M3 codes and fp32 scales equal the
+    oracle's bit for bit; the oracle then selects on its own fp64 scores of
+    the dequantised keys and the top-k rule above applies to those scores,
+    with one more fp32 rounding (the scale) in the error band.
 """
 from __future__ import annotations
 
