@@ -3,8 +3,10 @@
 
 One step = one ``hybrid_attend`` over one batch: compression of the blocks the
 step's tokens close, the lightning indexer and top-k, sparse shared-KV MQA
-and HCA dense MQA.  Default workload: 64K-context decode, batch 16 (H=64,
-d=512, indexer 4x64, top-k 512), caches built before the timed region.
+and HCA dense MQA.  Headline workload: 64K-context decode, batch 16 (H=64,
+d=512, indexer 4x64, top-k 512), caches built before the timed region.  The
+same JSON line also carries, under ``workloads``, the step time, throughput
+and rooflines of the 128K prefill, the ragged decode and the 1M-token decode.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -29,6 +31,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "CSA+HCA attention tokens/s at 64K–1M ctx; % of HBM / tensor-core roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+EXTRA_WORKLOADS = ("prefill_128k", "ragged_decode", "decode_1m")
 
 # DRAM traffic per call of the dominant call from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum over the call's kernels),
@@ -51,7 +54,7 @@ NCU_TRAFFIC = {
 }
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -62,12 +65,16 @@ def parse():
     ap.add_argument("--min-seconds", type=float, default=2.0, help="repeat the K-step region this long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="measure only --workload (no 'workloads' object for the other configurations)")
+    ap.add_argument("--extra", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated workloads measured after the headline one")
     ap.add_argument("--index-fp8", action="store_true",
                     help="the indexer reads FP8 E4M3 keys with per-row scales (quantised once with the caches)")
     ap.add_argument("--ctx", type=int, default=0,
                     help="every sequence this long instead of the workload's lengths (smaller cases of the same "
                          "shape, e.g. for a profiler capture); the JSON line then names the override")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def load_peaks():
@@ -138,6 +145,43 @@ def step_work_fast(p, fp8=False):
         flops["sparse"] += int((4 * H * d * (sel + rC)).sum())
         flops["dense"] += int((4 * H * d * (nH + rH)).sum())
     return w, flops
+
+
+def call_roofline(name, us, work, flops, decode, peaks, peak_src):
+    """Roofline of one C-ABI call timed alone: HBM bytes for decode calls and the
+    indexer, bf16 tensor flops for prefill attention.  A call timed alone is
+    measured against the burst peak; the sustained peak's fraction is given
+    beside it."""
+    s = us * 1e-6
+    if decode or name not in ("sparse_attend", "dense_attend"):
+        alg = work[name]
+        achieved = alg / s / 1e9
+        peak = float(peaks["hbm_gbs"])
+        return {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "frac_of_8TBps": achieved / 8000.0,
+                "peak_source": f"hbm_gbs ({peak_src})", "alg_bytes_per_launch": alg, "avg_us": us}
+    fl = flops["sparse" if name == "sparse_attend" else "dense"]
+    achieved = fl / s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    sus = float(peaks.get("bf16_tflops_sustained", peak))
+    return {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "frac_of_sustained": achieved / sus, "peak_sustained": sus,
+            "peak_source": f"bf16_tflops burst ({peak_src}); call timed alone",
+            "alg_flops_per_launch": fl, "avg_us": us}
+
+
+def step_roofline(work, flops, ms_step, peaks):
+    step_bytes = sum(work.values())
+    step_flops = sum(flops.values())
+    s = ms_step * 1e-3
+    sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    return {"alg_bytes": step_bytes, "alg_flops": step_flops,
+            "GBps": step_bytes / s / 1e9,
+            "frac_hbm_measured": step_bytes / s / 1e9 / float(peaks["hbm_gbs"]),
+            "frac_hbm_8TBps": step_bytes / s / 8e12,
+            "TFLOPs": step_flops / s / 1e12,
+            "frac_bf16_burst": step_flops / s / 1e12 / float(peaks["bf16_tflops"]),
+            "frac_bf16_sustained": step_flops / s / 1e12 / sus}
 
 
 # ---------------------------------------------------------------------------
@@ -217,7 +261,7 @@ class ClockSampler:
 # oracle on the host cores
 # ---------------------------------------------------------------------------
 def oracle_sample(p, n_queries):
-    """Inputs restricted to the first n_queries decode sequences (a bounded sample)."""
+    """Inputs restricted to the first n_queries queries (a bounded sample of the workload)."""
     from compressed_sparse_attention_21_b300 import workloads as wl
     import numpy as np
     inp = wl.to_numpy(p)
@@ -235,6 +279,11 @@ def oracle_sample(p, n_queries):
     sub["q"] = inp["q"][:inp["cu_q"][B]]
     sub["kI"] = inp["kI"][:inp["cu_csa"][B]]
     return sub, np.arange(n_queries)
+
+
+def oracle_queries_per_step(w, p):
+    """Queries of one oracle step: every query of a decode batch, a 64-query sample of a prefill."""
+    return sum(p["n_q"]) if w.decode else min(64, sum(p["n_q"]))
 
 
 def time_oracle(p, target_s=10.0, max_reps=50, n_queries=None):
@@ -259,7 +308,7 @@ def time_oracle(p, target_s=10.0, max_reps=50, n_queries=None):
 
 
 # ---------------------------------------------------------------------------
-# reference arm: the oracle, timed on the host cores
+# reference arm: the oracle, timed on the host cores, on the same workload
 # ---------------------------------------------------------------------------
 def run_reference(args):
     from compressed_sparse_attention_21_b300 import workloads as wl
@@ -269,21 +318,29 @@ def run_reference(args):
     import oracle
     oracle.build()
     w = wl.WORKLOADS[args.workload]
-    p = wl.make_problem(w)
-    inp, eval_q = oracle_sample(p, 1)
+    p = wl.make_problem(w, lengths=[args.ctx] * w.batch if args.ctx > 0 else None)
+    nq = oracle_queries_per_step(w, p)
+    inp, eval_q = oracle_sample(p, nq)
     for _ in range(max(args.warmup, 0)):
         oracle.hybrid_queries(inp, eval_q=eval_q)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle.hybrid_queries(inp, eval_q=eval_q)
     dt = time.perf_counter() - t0
-    value = args.steps / dt
+    value = nq * args.steps / dt
+    total_q = sum(p["n_q"])
+    sample = (f"every query of {w.name} per step ({nq} decode queries, whole step from raw inputs)"
+              if nq == total_q else
+              f"{nq} of {total_q} queries of {w.name} per step (whole step from raw inputs)")
+    cfg = workload_config(w, p)
+    if args.ctx > 0:
+        cfg["ctx_override"] = args.ctx
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(w, p),
+            "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": f"one decode query of {w.name} per step (whole step from raw inputs)"},
+                             "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -300,43 +357,44 @@ def workload_config(w, p):
 # ---------------------------------------------------------------------------
 # native arm
 # ---------------------------------------------------------------------------
-def main():
-    args = parse()
-    if args.impl == "reference":
-        return run_reference(args)
+def ncu_traffic(wname, dom, fp8):
+    t_rec = NCU_TRAFFIC.get((wname, dom, "fp8" if fp8 else "bf16"))
+    if not t_rec:
+        return None
+    csrc = os.path.join(ROOT, "compressed_sparse_attention_21_b300", "csrc")
+    for f, sha in t_rec["sources"].items():
+        path = os.path.join(csrc, f)
+        if not os.path.exists(path) or hashlib.sha256(open(path, "rb").read()).hexdigest() != sha:
+            return None
+    return t_rec["bytes_per_launch"]
 
+
+def measure(w, args, dev, peaks, peak_src, world, rank, local, headline):
+    """Time one workload: the hybrid step (CUDA graph over rotating state copies),
+    each C-ABI call alone, and, for the headline, e2e and the CPU baseline."""
     import torch
     import torch.distributed as dist
     from compressed_sparse_attention_21_b300 import _lib as csa
-    from compressed_sparse_attention_21_b300 import build as csa_build
     from compressed_sparse_attention_21_b300 import workloads as wl
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if rank == 0:
-        csa_build.build()
-    if world > 1:
-        dist.barrier()
-    csa.load()
-
-    w = wl.WORKLOADS[args.workload]
     p = wl.make_problem(w, lengths=[args.ctx] * w.batch if args.ctx > 0 else None)   # each rank: its own batch
-    peaks, peak_src = load_peaks()
+    work, flops = step_work_fast(p, args.index_fp8)
+    step_bytes = sum(work.values())
 
-    # CPU baseline first (oracle threads run before heavy GPU work; rank 0 only, N=1 only)
     cpu_base = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_base = time_oracle(p, target_s=10.0, n_queries=None if w.decode else 64)
+    if headline and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = time_oracle(p, target_s=10.0, n_queries=oracle_queries_per_step(w, p))
 
     layout = csa.Layout(p["lengths"], p["n_q"], w.mC, w.mH, device=dev)
     full = csa.Layout(p["lengths"], p["lengths"], w.mC, w.mH, device=dev)
     base = {k: p[k].to(dev) for k in ("kv", "gate", "qI", "kI", "q")}
-    ncopies = max(1, args.copies if w.decode else 1)
+    if not headline:   # host copies of the large tensors are not needed again
+        del p["kv"], p["q"]
+    if w.decode:
+        # rotate enough copies that one rotation's bytes exceed the 126 MB L2 several times
+        ncopies = max(1, args.copies if headline else min(args.copies, max(2, -(-(4 * 126 << 20) // step_bytes))))
+    else:
+        ncopies = 1
     copies = []
     for c in range(ncopies):
         t = {k: (v if c == 0 else v.clone()) for k, v in base.items()}
@@ -350,8 +408,8 @@ def main():
         h = csa.Hybrid(layout, t["kv"], t["gate"], t["qI"], t["kI"], t["q"], w.top_k, w.scale,
                        csa_cache=csa_cache, hca_cache=hca_cache, k_idx_fp8=fp8)
         copies.append(h)
+    del base
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
 
     # cache build time (prefill-shaped compression of the whole context), reported apart
     cache_build_ms = None
@@ -369,7 +427,7 @@ def main():
         torch.cuda.synchronize()
         cache_build_ms = ev0.elapsed_time(ev1) / 10
 
-    # warm-up (eager; also creates the library's per-device stream/events)
+    # warm-up (eager; also creates the library's per-stream helper)
     for i in range(max(args.warmup, 3)):
         copies[i % ncopies]()
     torch.cuda.synchronize()
@@ -383,6 +441,10 @@ def main():
     for _ in range(2):
         graph.replay()
     torch.cuda.synchronize()
+
+    # K steps per timed region: the headline times exactly --steps; a prefill
+    # step of the other workloads takes ~0.1 s, so it times two steps a region
+    K = args.steps if (headline or w.decode) else min(args.steps, 2)
 
     def timed_region(K):
         """Exactly K steps (graph replays of ncopies steps plus eager remainder)."""
@@ -404,31 +466,33 @@ def main():
     sampler.start()
     time.sleep(0.3)
     reps = []
+    min_s = args.min_seconds if headline else min(args.min_seconds, 1.0)
     t_start = time.perf_counter()
     while True:
-        reps.append(timed_region(args.steps))
-        if time.perf_counter() - t_start >= args.min_seconds and len(reps) >= 3:
+        reps.append(timed_region(K))
+        if time.perf_counter() - t_start >= min_s and len(reps) >= 3:
             break
     clocks = sampler.stop()
     ms_region = statistics.median(reps)
-    ms_step = ms_region / args.steps
+    ms_step = ms_region / K
     tokens_per_step = sum(p["n_q"])
     value = job_value(tokens_per_step, world, ms_step)
 
     # launches inside the step: an instrumented eager pass counts them per kernel
     csa.timing_reset()
     csa.timing_enable(True)
-    for i in range(args.steps):
+    for i in range(K):
         copies[i % ncopies]()
     torch.cuda.synchronize()
     kt = csa.timing_read()
     csa.timing_enable(False)
     csa.timing_reset()
-    launches_per_step = sum(n for n, _ in kt.values()) / args.steps
+    launches_per_step = sum(n for n, _ in kt.values()) / K
 
     # per-call durations: each C-ABI call of the step alone, back to back over
     # the rotating copies in one CUDA graph (no host gaps), CUDA events around
     # the replays on the capturing stream
+    ws_idx, ws_sp, ws_de = {}, {}, {}
     calls = {
         "compress": lambda h: (csa.csa_compress(layout, h.kv, h.gate, h.csa_cache),
                                csa.hca_compress(layout, h.kv, h.gate, h.hca_cache)),
@@ -443,7 +507,6 @@ def main():
         "dense_attend": lambda h: csa.hca_dense_attend(layout, h.q, h.hca_cache, h.kv, w.scale, out=h.o_hca,
                                                        lse=h.lse_hca, ws=ws_de[id(h)]),
     }
-    ws_idx, ws_sp, ws_de = {}, {}, {}
     for h in copies:
         ws_n = (csa.index_fp8_workspace_size if args.index_fp8 else csa.index_workspace_size)(layout, w.HI, w.dI,
                                                                                                w.top_k)
@@ -476,9 +539,10 @@ def main():
                 break
             reps_c *= 4
         call_us[name] = ms * 1e3 / (reps_c * ncopies)
-    assert csa.check_device_error() == 0
+        del g
+    if csa.check_device_error() != 0:
+        raise RuntimeError(f"device error word set during the {w.name} measurement")
 
-    work, flops = step_work_fast(p, args.index_fp8)
     kernels = {}
     for name, us in call_us.items():
         entry = {"avg_us": us, "kernels": sorted(k for k in kt if k.split("_")[0] in name.split("_")[0] or
@@ -489,120 +553,194 @@ def main():
         if fl:
             entry["alg_TFLOPs"] = fl / (us * 1e-6) / 1e12
         kernels[name] = entry
-    kernels["launches_per_step"] = {k: n / args.steps for k, (n, _) in kt.items()}
-    step_bytes = sum(work.values())
-    step_flops = sum(flops.values())
+    kernels["launches_per_step"] = {k: n / K for k, (n, _) in kt.items()}
 
     # dominant call and its roofline: HBM-bound for decode (bytes), tensor-bound
     # for prefill attention (flops)
     dom = max(call_us, key=lambda k: call_us[k])
-    avg_dom_s = call_us[dom] * 1e-6
-    if w.decode or dom not in ("sparse_attend", "dense_attend"):
-        alg = work[dom]
-        achieved = alg / avg_dom_s / 1e9
-        peak = float(peaks["hbm_gbs"])
-        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": f"hbm_gbs ({peak_src})", "alg_bytes_per_launch": alg,
-                "avg_us": call_us[dom]}
-    else:
-        fl = flops["sparse" if dom == "sparse_attend" else "dense"]
-        achieved = fl / avg_dom_s / 1e12
-        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": f"bf16_tflops_sustained ({peak_src})",
-                "alg_flops_per_launch": fl, "avg_us": call_us[dom]}
-    traffic = None
-    t_rec = NCU_TRAFFIC.get((w.name, dom, "fp8" if args.index_fp8 else "bf16"))
-    if t_rec:
-        ok = all(os.path.exists(os.path.join(ROOT, "compressed_sparse_attention_21_b300", "csrc", f)) and
-                 hashlib.sha256(open(os.path.join(ROOT, "compressed_sparse_attention_21_b300", "csrc", f),
-                                     "rb").read()).hexdigest() == sha
-                 for f, sha in t_rec["sources"].items())
-        if ok:
-            traffic = t_rec["bytes_per_launch"]
-    roof["traffic"] = traffic
+    roof = call_roofline(dom, call_us[dom], work, flops, w.decode, peaks, peak_src)
+    roof["traffic"] = ncu_traffic(w.name, dom, args.index_fp8) if args.ctx == 0 else None
+    step_roof = step_roofline(work, flops, ms_step, peaks)
 
-    # whole-step roofline (context)
-    step_roof = {"alg_bytes": step_bytes, "alg_flops": step_flops,
-                 "GBps": step_bytes / (ms_step * 1e-3) / 1e9,
-                 "frac_hbm_measured": step_bytes / (ms_step * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
-                 "frac_hbm_8TBps": step_bytes / (ms_step * 1e-3) / 8e12,
-                 "TFLOPs": step_flops / (ms_step * 1e-3) / 1e12}
-
-    # end to end through the public API with host buffers (pinned), eager calls
+    # end to end through the public API with host buffers (pinned)
     e2e = None
-    if not args.no_e2e:
-        h = copies[0]
-        q_host = p["q"].pin_memory()
-        qI_host = p["qI"].pin_memory()
-        oC_host = torch.empty(h.o_csa.shape, dtype=h.o_csa.dtype).pin_memory()
-        oH_host = torch.empty(h.o_hca.shape, dtype=h.o_hca.dtype).pin_memory()
-        lC_host = torch.empty(h.lse_csa.shape, dtype=torch.float32).pin_memory()
-        lH_host = torch.empty(h.lse_hca.shape, dtype=torch.float32).pin_memory()
-        bi = q_host.numel() * 2 + qI_host.numel() * 2
-        bo = (oC_host.numel() + oH_host.numel()) * 2 + (lC_host.numel() + lH_host.numel()) * 4
+    if headline and not args.no_e2e:
+        e2e = measure_e2e(copies, p, args, world, dev, tokens_per_step, ncopies)
 
-        def e2e_step(hh):
-            hh.q.copy_(q_host, non_blocking=True)
-            hh.q_idx.copy_(qI_host, non_blocking=True)
-            hh()
-            oC_host.copy_(hh.o_csa, non_blocking=True)
-            oH_host.copy_(hh.o_hca, non_blocking=True)
-            lC_host.copy_(hh.lse_csa, non_blocking=True)
-            lH_host.copy_(hh.lse_hca, non_blocking=True)
-
-        def timed_e2e(run):
-            if world > 1:
-                dist.barrier()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            run()
-            e1.record()
-            torch.cuda.synchronize()
-            return max_over_ranks(e0.elapsed_time(e1), dev)
-
-        # eager: one hybrid_attend call per step, host copies around it
-        for i in range(3):
-            e2e_step(copies[i % ncopies])
-        ms_eager = timed_e2e(lambda: [e2e_step(copies[i % ncopies]) for i in range(args.steps)])
-        # captured: the same per-step sequence (copies in, the C-ABI call, copies out)
-        # recorded once in a CUDA graph and replayed per step, as a serving loop runs it
-        g_e2e = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_e2e):
-            for h in copies:
-                e2e_step(h)
-        g_e2e.replay()
-        torch.cuda.synchronize()
-        full, rem = divmod(args.steps, ncopies)
-        ms_graph = timed_e2e(lambda: ([g_e2e.replay() for _ in range(full)], [e2e_step(copies[i]) for i in range(rem)]))
-        e2e = {"value": job_value(tokens_per_step, world, ms_graph / args.steps), "unit": "tokens/s",
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": ms_graph / args.steps,
-               "path": "per step: pinned host q/q_idx copied in, hybrid_attend through the C ABI, both outputs "
-                       "and LSEs copied out to pinned host memory; the step sequence captured once in a CUDA "
-                       "graph and replayed",
-               "eager": {"value": job_value(tokens_per_step, world, ms_eager / args.steps),
-                         "ms_per_step": ms_eager / args.steps,
-                         "path": "the same sequence issued eagerly from Python each step"}}
-
-    touched = step_bytes
     cfg = workload_config(w, p)
     if args.ctx > 0:
         cfg["ctx_override"] = args.ctx
     cfg["index_keys"] = "fp8_e4m3 + fp32 row scale" if args.index_fp8 else "bf16"
-    cfg["l2"] = (f"{ncopies} rotating copies of the step state; {touched / 2**20:.1f} MiB algorithmic per step, "
-                 f"{ncopies * touched / 2**20:.0f} MiB per rotation vs 126 MB L2") if ncopies > 1 else \
+    cfg["l2"] = (f"{ncopies} rotating copies of the step state; {step_bytes / 2**20:.1f} MiB algorithmic per step, "
+                 f"{ncopies * step_bytes / 2**20:.0f} MiB per rotation vs 126 MB L2") if ncopies > 1 else \
         "inputs larger than L2"
+    out = {"value": value, "ms_per_step": ms_step, "steps": K, "config": cfg, "roofline": roof,
+           "step_roofline": step_roof, "cpu_baseline": cpu_base, "e2e": e2e,
+           "gpu_launches": int(round(launches_per_step * K)), "launches_per_step": launches_per_step,
+           "kernels": kernels, "clocks": clocks, "cache_build_ms": cache_build_ms, "timed_region_reps": len(reps)}
+    del copies, graph, layout, full
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_e2e(copies, p, args, world, dev, tokens_per_step, ncopies):
+    """The same metric through the C ABI with host buffers: every step copies its
+    queries in from pinned host memory and both outputs and LSEs out.
+
+    Pipelined: a copy-in stream, the compute stream and a copy-out stream, one
+    state copy per step in flight, so one step's copies overlap the
+    neighbouring steps' compute; the whole rotation of steps is captured once in
+    a CUDA graph and replayed, as a serving loop runs it.  The serial form (copy
+    in, step, copy out, one after the other on one stream) is given beside it."""
+    import torch
+    q_host = p["q"].pin_memory()
+    qI_host = p["qI"].pin_memory()
+    outs = [dict(oC=torch.empty(c.o_csa.shape, dtype=c.o_csa.dtype).pin_memory(),
+                 oH=torch.empty(c.o_hca.shape, dtype=c.o_hca.dtype).pin_memory(),
+                 lC=torch.empty(c.lse_csa.shape, dtype=torch.float32).pin_memory(),
+                 lH=torch.empty(c.lse_hca.shape, dtype=torch.float32).pin_memory()) for c in copies]
+    bi = q_host.numel() * 2 + qI_host.numel() * 2
+    o0 = outs[0]
+    bo = (o0["oC"].numel() + o0["oH"].numel()) * 2 + (o0["lC"].numel() + o0["lH"].numel()) * 4
+
+    def copy_out(hh, o):
+        o["oC"].copy_(hh.o_csa, non_blocking=True)
+        o["oH"].copy_(hh.o_hca, non_blocking=True)
+        o["lC"].copy_(hh.lse_csa, non_blocking=True)
+        o["lH"].copy_(hh.lse_hca, non_blocking=True)
+
+    def serial_step(i):
+        hh = copies[i % ncopies]
+        hh.q.copy_(q_host, non_blocking=True)
+        hh.q_idx.copy_(qI_host, non_blocking=True)
+        hh()
+        copy_out(hh, outs[i % ncopies])
+
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def pipelined_rotation():
+        """Every copy once: copy-in on s_in, the step on the current stream, copy-out on s_out."""
+        cur = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(cur)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        ev_out = []
+        for i, hh in enumerate(copies):
+            ev_in, ev_done, ev_o = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                hh.q.copy_(q_host, non_blocking=True)
+                hh.q_idx.copy_(qI_host, non_blocking=True)
+                ev_in.record(s_in)
+            cur.wait_event(ev_in)
+            hh()
+            ev_done.record(cur)
+            s_out.wait_event(ev_done)
+            with torch.cuda.stream(s_out):
+                copy_out(hh, outs[i])
+                ev_o.record(s_out)
+            ev_out.append(ev_o)
+        for ev in ev_out:
+            cur.wait_event(ev)
+
+    def timed(run):
+        import torch.distributed as dist
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run()
+        e1.record()
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1), dev)
+
+    # serial, captured: copy in, step, copy out on one stream
+    for i in range(3):
+        serial_step(i)
+    g_ser = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_ser):
+        for i in range(ncopies):
+            serial_step(i)
+    g_ser.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // ncopies)
+    ms_ser = timed(lambda: [g_ser.replay() for _ in range(reps)]) / (reps * ncopies)
+
+    # pipelined, captured
+    pipelined_rotation()
+    torch.cuda.synchronize()
+    g_pipe = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_pipe):
+        pipelined_rotation()
+    g_pipe.replay()
+    torch.cuda.synchronize()
+    ms_pipe = timed(lambda: [g_pipe.replay() for _ in range(reps)]) / (reps * ncopies)
+    return {"value": job_value(tokens_per_step, world, ms_pipe), "unit": "tokens/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": ms_pipe,
+            "steps": reps * ncopies,
+            "path": "per step: pinned host q/q_idx copied in, hybrid_attend through the C ABI, both outputs and "
+                    "LSEs copied out to pinned host memory; copy-in, compute and copy-out on three streams with "
+                    f"one of {ncopies} state copies per step, so copies overlap the neighbouring steps; the "
+                    "rotation captured once in a CUDA graph and replayed",
+            "serial": {"value": job_value(tokens_per_step, world, ms_ser), "ms_per_step": ms_ser,
+                       "path": "copy in, step, copy out one after the other on one stream (CUDA graph)"}}
+
+
+def main(argv=None):
+    args = parse(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    from compressed_sparse_attention_21_b300 import _lib as csa
+    from compressed_sparse_attention_21_b300 import build as csa_build
+    from compressed_sparse_attention_21_b300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        csa_build.build()
+    if world > 1:
+        dist.barrier()
+    csa.load()
+    peaks, peak_src = load_peaks()
+
+    w = wl.WORKLOADS[args.workload]
+    head = measure(w, args, dev, peaks, peak_src, world, rank, local, headline=True)
+
+    extra = {}
+    if not args.no_extra and args.ctx == 0:
+        for name in [x for x in args.extra.split(",") if x and x != w.name]:
+            r = measure(wl.WORKLOADS[name], args, dev, peaks, peak_src, world, rank, local, headline=False)
+            extra[name] = {k: r[k] for k in ("value", "ms_per_step", "steps", "roofline", "step_roofline", "clocks",
+                                             "launches_per_step", "cache_build_ms")}
+            extra[name]["unit"] = "tokens/s"
+            extra[name]["config"] = r["config"]
+            extra[name]["calls_us"] = {k: v["avg_us"] for k, v in r["kernels"].items() if isinstance(v, dict)
+                                       and "avg_us" in v}
+
+    cfg = head["config"]
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+    line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 (indexer keys fp8 e4m3)" if args.index_fp8 else "bf16",
-            "data": "synthetic", "config": cfg, "roofline": roof,
-            "step_roofline": step_roof, "cpu_baseline": cpu_base, "e2e": e2e,
-            "gpu_launches": int(round(launches_per_step * args.steps)), "launches_per_step": launches_per_step,
-            "kernels": kernels, "clocks": clocks, "cache_build_ms": cache_build_ms,
-            "timed_region_reps": len(reps), "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
-                                                      "bf16_tflops": peaks["bf16_tflops"]}}
+            "data": "synthetic", "config": cfg, "roofline": head["roofline"],
+            "step_roofline": head["step_roofline"], "cpu_baseline": head["cpu_baseline"], "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"], "launches_per_step": head["launches_per_step"],
+            "kernels": head["kernels"], "clocks": head["clocks"], "cache_build_ms": head["cache_build_ms"],
+            "timed_region_reps": head["timed_region_reps"],
+            "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
+                      "bf16_tflops_sustained": peaks.get("bf16_tflops_sustained")}}
+    if extra:
+        line["workloads"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

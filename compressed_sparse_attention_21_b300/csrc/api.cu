@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <utility>
@@ -23,8 +24,6 @@ namespace {
 struct DeviceState {
     bool ready = false;
     int *err = nullptr;
-    cudaStream_t aux = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr, sdone = nullptr;
     int num_sms = 0;
 };
 
@@ -45,13 +44,50 @@ csa_status_t device_state(DeviceState **out)
         s.err = static_cast<int *>(p);
         if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return CSA_ERR_CUDA;
-        if (cudaStreamCreateWithFlags(&s.aux, cudaStreamNonBlocking) != cudaSuccess) return CSA_ERR_CUDA;
-        if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
-        if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
-        if (cudaEventCreateWithFlags(&s.sdone, cudaEventDisableTiming) != cudaSuccess) return CSA_ERR_CUDA;
         s.ready = true;
     }
     *out = &s;
+    return CSA_OK;
+}
+
+// The helper stream and events of hybrid_attend, one set per (device, caller
+// stream), so that calls on different streams (or captured into different
+// graphs) never record or wait on each other's events.  `mu` is held while a
+// call issues its work, so two host threads issuing on the same stream do not
+// interleave their event records either.  Created on first use and kept until
+// the process exits.
+struct Helper {
+    cudaStream_t aux = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, sdone = nullptr;
+    std::mutex mu;
+};
+constexpr size_t kMaxHelpers = 256;
+std::map<std::pair<int, cudaStream_t>, std::unique_ptr<Helper>> g_helpers;
+std::mutex g_helpers_mu;
+
+// The helper of (current device, st); null once kMaxHelpers pairs have one
+// (the call then runs both branches on `st`, one after the other).
+csa_status_t helper_for(cudaStream_t st, Helper **out)
+{
+    *out = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_helpers_mu);
+    const auto key = std::make_pair(dev, st);
+    auto it = g_helpers.find(key);
+    if (it != g_helpers.end()) {
+        *out = it->second.get();
+        return CSA_OK;
+    }
+    if (g_helpers.size() >= kMaxHelpers) return CSA_OK;
+    std::unique_ptr<Helper> h(new Helper);
+    if (cudaStreamCreateWithFlags(&h->aux, cudaStreamNonBlocking) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->sdone, cudaEventDisableTiming) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    *out = h.get();
+    g_helpers.emplace(key, std::move(h));
     return CSA_OK;
 }
 
@@ -562,15 +598,23 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
     if (L->total_q == 0) return CSA_OK;
     char *ws = static_cast<char *>(p->ws);
 
+    Helper *hp = nullptr;
+    CSA_TRY(helper_for(st, &hp));
+    std::unique_lock<std::mutex> issue_lock;
+    if (hp) issue_lock = std::unique_lock<std::mutex>(hp->mu);
+
     // Streams.  The caller's stream `st` runs the compression and the CSA
     // branch (indexer, top-k, sparse attention) as one chain of dependent
     // launches: the key scan reads no compressed entry and overlaps the
     // compression, each later kernel starts while its predecessor finishes.
-    // The helper stream runs the HCA branch once the key scan (the part of
-    // the indexer that fills the GPU) is done, so it overlaps the top-k
-    // selection and the sparse attention.
-    if (cudaEventRecord(ds->fork, st) != cudaSuccess) return CSA_ERR_CUDA;
-    if (cudaStreamWaitEvent(ds->aux, ds->fork, 0) != cudaSuccess) return CSA_ERR_CUDA;
+    // The helper stream of (device, st) runs the HCA branch once the key scan
+    // (the part of the indexer that fills the GPU) is done, so it overlaps the
+    // top-k selection and the sparse attention.  Without a helper (the table
+    // is full) the HCA branch follows the CSA branch on `st`.
+    if (hp) {
+        if (cudaEventRecord(hp->fork, st) != cudaSuccess) return CSA_ERR_CUDA;
+        if (cudaStreamWaitEvent(hp->aux, hp->fork, 0) != cudaSuccess) return CSA_ERR_CUDA;
+    }
 
     // a1: compression of the blocks closed by this call's query positions
     csa_status_t s_c = CSA_OK;
@@ -604,7 +648,7 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
     if (s_c == CSA_OK) {
         IndexArgs ia = index_args(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k,
                                   p->idx_out, p->score_out, w_idx ? ws : nullptr, w_idx, ds->err);
-        ia.scan_done = ds->sdone;
+        ia.scan_done = hp ? hp->sdone : nullptr;
         ia.pdl = compress;
         if (fp8) {
             ia.fp8 = true;
@@ -612,21 +656,23 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
             ia.k_scale = p->k_idx_scale;
         }
         s_c = from_cuda(launch_index_topk(ia, st));
-    } else {
-        cudaEventRecord(ds->sdone, st);
+    } else if (hp) {
+        cudaEventRecord(hp->sdone, st);
     }
 
+    // the SM shares that sized the workspace (kept when the branches run one after the other)
     int sh_s = 0, sh_d = 0;
     hybrid_shares(p, ds->num_sms, &sh_s, &sh_d);
+    const AttendArgs ha = attend_args(L, false, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d, p->ratio_hca,
+                                      0, p->scale, p->o_hca, p->lse_hca, w_hc ? ws + w_idx + w_sp : nullptr, w_hc,
+                                      ds->err, ds->num_sms, sh_d);
 
     // a5 on the helper stream, behind the compression and the key scan
-    const bool c1 = cudaStreamWaitEvent(ds->aux, ds->sdone, 0) == cudaSuccess;
+    bool c1 = true;
     csa_status_t s_h = s_c;
-    if (s_h == CSA_OK) {
-        AttendArgs ha = attend_args(L, false, p->q, p->hca_cache, p->kv, nullptr, p->n_heads, p->d,
-                                    p->ratio_hca, 0, p->scale, p->o_hca, p->lse_hca,
-                                    w_hc ? ws + w_idx + w_sp : nullptr, w_hc, ds->err, ds->num_sms, sh_d);
-        s_h = from_cuda(launch_attend(ha, ds->aux));
+    if (hp) {
+        c1 = cudaStreamWaitEvent(hp->aux, hp->sdone, 0) == cudaSuccess;
+        if (s_h == CSA_OK) s_h = from_cuda(launch_attend(ha, hp->aux));
     }
 
     // a4, launched behind the selection
@@ -637,9 +683,15 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
         sa.pdl = true;
         s_c = from_cuda(launch_attend(sa, st));
     }
+    if (!hp) {
+        // a5 after a4 on the caller's stream
+        if (s_c == CSA_OK) s_h = from_cuda(launch_attend(ha, st));
+        if (s_c != CSA_OK) return s_c;
+        return s_h;
+    }
     // join (always, so the helper stream never dangles inside a capture)
-    const bool j1 = cudaEventRecord(ds->join, ds->aux) == cudaSuccess;
-    const bool j2 = cudaStreamWaitEvent(st, ds->join, 0) == cudaSuccess;
+    const bool j1 = cudaEventRecord(hp->join, hp->aux) == cudaSuccess;
+    const bool j2 = cudaStreamWaitEvent(st, hp->join, 0) == cudaSuccess;
     if (s_c != CSA_OK) return s_c;
     if (s_h != CSA_OK) return s_h;
     return (c1 && j1 && j2) ? CSA_OK : CSA_ERR_CUDA;

@@ -46,9 +46,19 @@
  *     be seen on the device (for example an entry count that does not equal
  *     floor(L/m), or an index that is not visible) set the device error word,
  *     which csa_check_device_error reads; the offending rows are skipped.
- *   - The first call on a device creates one helper stream and three events
- *     for that device (hybrid_attend runs its two branches concurrently on
- *     them).  Make that first call outside any CUDA graph capture.
+ *   - hybrid_attend runs its two branches concurrently on the caller's
+ *     stream and one helper stream.  The first hybrid_attend call on a given
+ *     (device, stream) pair creates that pair's helper stream and three
+ *     events, kept until the process exits; make that first call outside
+ *     any CUDA graph capture.  Calls on different streams (or captured into
+ *     different graphs) use different helpers and do not interfere; calls
+ *     on one stream are issued one at a time (the library holds a host lock
+ *     per pair while it issues a call).  Past 256 pairs, a call on a new
+ *     pair runs the two branches one after the other on its own stream.
+ *   - The library keeps per-device state (the device error word's address,
+ *     the static scratch's address, the helper streams).  It must not be
+ *     used across a device reset (cudaDeviceReset or a primary-context
+ *     reset) in the same process.
  *   - Inside a call, kernels that follow another kernel of the same call may
  *     be launched with programmatic dependent launch (they start early and
  *     wait on the device for their predecessor).  The first kernel of every
@@ -180,10 +190,15 @@ csa_status_t csa_index_workspace_size(const csa_layout *layout, int n_heads_idx,
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current).  Make that first call before
  *     any stream capture.
- *   - Every call shares the one array, which keeps the last call's contents;
- *     each call clears the histograms and counters it needs on `stream`
- *     first.  Calls that overlap on the GPU (on different streams or host
- *     threads) race on the array and must not be issued.
+ *   - Every call shares the one array, which keeps the last call's contents.
+ *     Each call therefore clears the histograms and counters it needs first:
+ *     one cudaMemsetAsync of about 16 KiB per query of the call (a per-query
+ *     histogram and counters; never more than the array) on `stream`, a
+ *     memset node when the call is captured into a graph.  The workspace
+ *     calls above need no such clear: their caller zero-fills the workspace
+ *     once.
+ *     Calls that overlap on the GPU (on different streams or host threads)
+ *     race on the array and must not be issued.
  * ------------------------------------------------------------------------- */
 #define CSA_INDEX_STATIC_SCRATCH_BYTES (32u << 20)
 csa_status_t lightning_index_topk_static(const csa_layout *layout, const csa_bf16 *q_idx,

@@ -59,6 +59,27 @@ def entry_err(gpu, ref):
     return float(err.max()), float((err / bound).max())
 
 
+def entry_ulp_check(gpu, ref, abs_mix, m):
+    """Entries against the arithmetic they come from: an fp32 softmax-weighted
+    sum of m bf16 tokens, rounded to bf16 once.
+
+    |gpu - ref| <= 1 bf16 ulp of ref (the final rounding, with a binade step to
+    spare) + (m + 4) * 2^-23 * sum_t w_t |c_t| (the fp32 exponentials, the
+    weighted sum and the normalisation).  abs_mix is the oracle's entry of the
+    same block on |c|, i.e. sum_t w_t |c_t|.  A dropped or doubled token, a
+    wrong weight or a misplaced block moves an entry far beyond this bound.
+    Returns the worst ratio of error to bound."""
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7)
+    bound = ulp + (m + 4) * 2.0 ** -23 * abs_mix + 1e-30
+    err = np.abs(gpu - ref)
+    return float((err / bound).max()) if err.size else 0.0
+
+
+def abs_bits(bits):
+    """bf16 bit patterns of |x| (sign bit cleared)."""
+    return np.ascontiguousarray(bits, np.uint16) & np.uint16(0x7FFF)
+
+
 class GpuProblem:
     """Device copies of a seeded problem and the two layouts it needs."""
 

@@ -54,8 +54,12 @@ def test_compress_prefill(d, ratio, side):
     (csa.csa_compress if side == "csa" else csa.hca_compress)(g.full, g.kv, g.gate, out, ratio=ratio)
     torch.cuda.synchronize()
     ref = oracle.compress_packed(inp["cu_kv"], cu, inp["kv"], inp["gate"], ratio)
-    err, ratio_to_bound = P.entry_err(P.bf16_to_f64(out), ref)
+    got = P.bf16_to_f64(out)
+    err, ratio_to_bound = P.entry_err(got, ref)
     assert ratio_to_bound <= 1.0, err
+    # tighter: one bf16 rounding of an fp32 weighted sum (see parity.entry_ulp_check)
+    mix = oracle.compress_packed(inp["cu_kv"], cu, P.abs_bits(inp["kv"]), inp["gate"], ratio)
+    assert P.entry_ulp_check(got, ref, mix, ratio) <= 1.0
 
 
 def test_compress_fused_and_decode_append():
@@ -337,6 +341,26 @@ def test_hybrid_small(case):
     assert torch.equal(o1, h.o_csa)
 
 
+def test_hybrid_on_two_streams_at_once():
+    # Two hybrid steps issued back to back on two streams (each with its own
+    # buffers and workspace) run concurrently, each with the helper stream and
+    # events of its own stream: both give exactly the results they give alone.
+    cases = [problem([4097, 8191, 30001], [1] * 3, H=64, d=512, HI=4, dI=64, k=256, seed=35),
+             problem([1000, 5000, 65536], [1] * 3, H=64, d=512, HI=4, dI=64, k=512, seed=36)]
+    hs = [P.GpuProblem(p).hybrid(prebuilt=True) for p in cases]
+    ref = [(h.idx.clone(), h.o_csa.clone(), h.o_hca.clone()) for h in hs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(20):
+        for h, s in zip(hs, streams):
+            with torch.cuda.stream(s):
+                h()
+    torch.cuda.synchronize()
+    for h, (idx, oC, oH) in zip(hs, ref):
+        assert torch.equal(h.idx, idx) and torch.equal(h.o_csa, oC) and torch.equal(h.o_hca, oH)
+    assert csa.check_device_error() == 0
+
+
 @pytest.mark.parametrize("fp8", [False, True])
 @pytest.mark.parametrize("nseq", [3, 1200])
 def test_hybrid_without_complete_blocks(fp8, nseq):
@@ -420,6 +444,9 @@ def _workload_check(name, eval_q=None, entries="all"):
     rep = P.check_hybrid(p, h, eval_q=eval_q, check_entries=entries)
     assert csa.check_device_error() == 0
     print(name, rep)
+    # swaps accepted only by the fp32 error band (a k-th score near zero) stay rare:
+    # at most 1% of the queries (and 2 on a small batch)
+    assert rep["topk"]["fp32tie"] <= max(2, rep["queries"] // 100), rep["topk"]
     return rep
 
 

@@ -462,3 +462,105 @@ def test_attention_ignores_the_order_of_the_selected_indices(orc):
     again = orc.hybrid_queries(p, given_idx=perm, do_hca=False)
     assert np.allclose(again["oC"], base["oC"], rtol=0, atol=1e-12)
     assert np.allclose(again["lseC"], base["lseC"], rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# packed batches and query positions (§2.2 step 1: one entry per m tokens of a
+# sequence; queries are a sequence's last n_q positions)
+# ----------------------------------------------------------------------------
+
+def packed_problem(lengths, n_q, d=8, H=2, HI=2, dI=4, mC=4, mH=16, k=5, seed=0):
+    w = wl.Workload("packed", len(lengths), list(lengths), False, H=H, d=d, HI=HI, dI=dI, top_k=k, mC=mC,
+                    mH=mH, seed=seed)
+    return wl.to_numpy(wl.make_problem(w, n_q=n_q))
+
+
+def one_sequence(p, b):
+    """Sequence b of a packed problem as a batch of one (every offset 0)."""
+    cu = {key: p[key] for key in ("cu_kv", "cu_q", "cu_csa", "cu_hca")}
+    kv0, kv1 = cu["cu_kv"][b], cu["cu_kv"][b + 1]
+    q0, q1 = cu["cu_q"][b], cu["cu_q"][b + 1]
+    c0, c1 = cu["cu_csa"][b], cu["cu_csa"][b + 1]
+    h0, h1 = cu["cu_hca"][b], cu["cu_hca"][b + 1]
+    s = dict(p)
+    s.update(cu_kv=np.array([0, kv1 - kv0]), cu_q=np.array([0, q1 - q0]), cu_csa=np.array([0, c1 - c0]),
+             cu_hca=np.array([0, h1 - h0]), kv=p["kv"][kv0:kv1], gate=p["gate"][kv0:kv1], qI=p["qI"][q0:q1],
+             q=p["q"][q0:q1], kI=p["kI"][c0:c1])
+    return s
+
+
+def test_packed_batch_equals_each_sequence_alone(orc):
+    # Prefill, decode and chunked sequences packed together (and one without
+    # queries): every query's selection, outputs and LSEs equal those of its
+    # sequence run alone, bit for bit.  A wrong cu_kv / cu_csa / cu_hca / cu_q
+    # offset, or a query assigned to the wrong sequence, reads another
+    # sequence's tokens, entries or indexer keys and fails here.
+    lengths = [70, 1, 45, 130, 9, 64]
+    n_q = [70, 1, 0, 12, 9, 1]
+    p = packed_problem(lengths, n_q, seed=40)
+    packed = orc.hybrid_queries(p)
+    row = 0
+    for b, nq in enumerate(n_q):
+        if nq == 0:
+            continue
+        alone = orc.hybrid_queries(one_sequence(p, b))
+        for key in ("idx", "oC", "lseC", "oH", "lseH"):
+            assert np.array_equal(packed[key][row:row + nq], alone[key]), (b, key)
+        row += nq
+    assert row == packed["idx"].shape[0]
+
+
+def test_decode_and_chunked_queries_equal_the_same_positions_of_a_prefill(orc):
+    # The queries of a sequence are its last n_q positions: t = L - n_q + i.
+    # The same tokens with n_q = L (prefill), n_q = 1 (decode) and n_q = 7
+    # (chunked) give, for each position, the same result bit for bit, when the
+    # query rows of the shorter layouts are the prefill's rows of those positions.
+    L = 203
+    full = packed_problem([L], [L], seed=41)
+    pre = orc.hybrid_queries(full)
+    for nq in (1, 7, 64):
+        s = dict(full)
+        s["cu_q"] = np.array([0, nq])
+        s["qI"] = full["qI"][L - nq:]
+        s["q"] = full["q"][L - nq:]
+        got = orc.hybrid_queries(s)
+        for key in ("idx", "oC", "lseC", "oH", "lseH"):
+            assert np.array_equal(got[key], pre[key][L - nq:]), (nq, key)
+
+
+def test_decode_position_against_library_attention(orc):
+    # m_C = m_H = 1 and k >= L: both branches are dense causal MQA, so a decode
+    # query (n_q = 1) over a packed batch equals the last row of causal SDPA (a
+    # library routine) on its own sequence; a chunked query set the last rows.
+    lengths, n_q = [37, 50, 23], [1, 5, 1]
+    p = packed_problem(lengths, n_q, d=8, H=2, mC=1, mH=1, k=64, seed=42)
+    out = orc.hybrid_queries(p)
+    full = packed_problem(lengths, lengths, d=8, H=2, mC=1, mH=1, k=64, seed=42)
+    row = 0
+    for b, (L, nq) in enumerate(zip(lengths, n_q)):
+        kv = full["kv"][full["cu_kv"][b]:full["cu_kv"][b + 1]]
+        q = np.concatenate([full["q"][full["cu_q"][b]:full["cu_q"][b + 1] - nq], p["q"][row:row + nq]])
+        ref = sdpa_causal(q, kv, p["scale"])[L - nq:]
+        assert np.allclose(out["oC"][row:row + nq], ref, atol=1e-12), b
+        assert np.allclose(out["oH"][row:row + nq], ref, atol=1e-12), b
+        row += nq
+
+
+def test_compress_packed_and_selected_equal_the_single_sequence_compressor(orc):
+    # compress_packed writes sequence b's entries at rows cu[b] ..; compress_selected
+    # finds the owner of a global entry row; both must give the single-sequence
+    # compressor's entries (pinned above to closed forms) bit for bit.
+    lengths = [9, 130, 3, 64, 257]
+    for m in (4, 16):
+        p = packed_problem(lengths, [1] * len(lengths), d=8, mC=m, mH=128, seed=43 + m)
+        cu = p["cu_csa"]
+        packed = orc.compress_packed(p["cu_kv"], cu, p["kv"], p["gate"], m)
+        for b, L in enumerate(lengths):
+            kv0 = p["cu_kv"][b]
+            alone = orc.compress(p["kv"][kv0:kv0 + L], p["gate"][kv0:kv0 + L], m)
+            assert np.array_equal(packed[cu[b]:cu[b + 1]], alone), (m, b)
+        rng = np.random.default_rng(m)
+        rows = np.concatenate([[0, cu[-1] - 1], cu[1:-1], cu[1:-1] - 1, rng.integers(0, cu[-1], 20)])
+        rows = rows[(rows >= 0) & (rows < cu[-1])]
+        sel = orc.compress_selected(p["cu_kv"], cu, p["kv"], p["gate"], m, rows)
+        assert np.array_equal(sel, packed[rows]), m

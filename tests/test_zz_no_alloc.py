@@ -69,8 +69,15 @@ def test_static_scratch_prefill_sized_batch():
         pytest.skip("needs a CUDA GPU")
     csa_build.build()
     csa.load()
-    lengths = [1500, 700]                  # 2200 queries: the per-query CTA path (no scratch)
-    _run_both(_problem(lengths, lengths, HI=2, dI=32, k=64, seed=44), 64)
+    # 2200 queries at top-k 64 over at most 375 entries: the prefill block
+    # path.  Its full workspace holds one 512 KiB candidate slot for each of
+    # the 138 query blocks (on 148 SMs); the 32 MiB array holds 64 slots, so
+    # the scratch-free call runs fewer persistent CTAs than the workspace call.
+    lengths = [1500, 700]
+    p = _problem(lengths, lengths, HI=2, dI=32, k=64, seed=44)
+    full_ws = csa.index_workspace_size(csa.Layout(lengths, lengths, 4, 128, device="cuda"), 2, 32, 64)
+    assert full_ws > csa.STATIC_SCRATCH_BYTES
+    _run_both(p, 64)
 
 
 def test_static_scratch_rejects_oversized_problem_on_host():
