@@ -210,7 +210,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     uint8_t *misc = sm + OFF_MISC;
     float *s_m = reinterpret_cast<float *>(misc + MISC_M);
     float *s_l = reinterpret_cast<float *>(misc + MISC_L);
-    float *s_mn = reinterpret_cast<float *>(misc + MISC_MN);
     float *s_al = reinterpret_cast<float *>(misc + MISC_AL);
     float *s_rmax = reinterpret_cast<float *>(misc + MISC_RMAX);   // [4 warps][64 heads]
     float *s_rsum = reinterpret_cast<float *>(misc + MISC_RSUM);
@@ -402,24 +401,28 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax (128 threads)
+        // Thread (w, l) takes key 16 w + l % 16 of each tile for heads
+        // 32 hh .. 32 hh + 31 (hh = l / 16).  It keeps the running maximum of
+        // those heads in registers (the same in every thread of the half) and
+        // its own partial sums of their weights over its keys; the sums are
+        // reduced over keys once, after the last tile.  A tile reduces its
+        // maximum over keys only when one of its scores exceeds the running
+        // maximum by more than 2^8 (one OR-reducing barrier per tile decides),
+        // which after the first tiles is rare.
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const int hh = lane >> 4;                 // head half: heads 32 hh .. 32 hh + 31
         const int key = 16 * warp + (lane & 15);  // key of the tile this thread takes
         bool ok = true;
-        // tid 0 waits on `b` with `parity`, then every softmax thread learns the outcome
-        auto wait_all = [&](int b, uint32_t parity) -> bool {
-            if (tid == 0) s_flag[0] = mbar_wait(bar(b), parity) ? 1 : 0;
-            tc::named_bar(1, 128);
-            const bool r = s_flag[0] != 0;
-            tc::named_bar(1, 128);
-            return r;
-        };
+        bool fail = false;   // a wait of this thread gave up (acted on at the next barrier reduction)
+        float m_run[32], l_part[32];
+#pragma unroll
+        for (int j = 0; j < 32; j++) {
+            m_run[j] = -INFINITY;
+            l_part[j] = 0.f;
+        }
         for (int t = 0; t < T; t++) {
             const int sidx = t & 1;
-            if (!wait_all(BAR_SFULL + sidx, (uint32_t)((t >> 1) & 1))) {
-                ok = false;
-                break;
-            }
+            if (!mbar_wait(bar(BAR_SFULL + sidx), (uint32_t)((t >> 1) & 1))) fail = true;
             tc::fence_after_sync();
             float v[64];
             tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sidx, v);
@@ -447,43 +450,57 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             } else {
                 valid = (tile - T_main) * kTcKeys + key < r_tail;
             }
-#pragma unroll
-            for (int j = 0; j < 32; j++) s[j] = valid ? s[j] * scale_log2 : -INFINITY;
-            float r0, r1;
-            halfwarp_reduce32<true>(s, r0, r1);
-            const int h2 = 32 * hh + 2 * (lane & 15);
-            s_rmax[warp * 64 + h2] = r0;
-            s_rmax[warp * 64 + h2 + 1] = r1;
-            if (tid == 0) s_flag[1] = 0;
-            tc::named_bar(1, 128);
-            if (tid < kTcHeads) {
-                const float M = fmaxf(fmaxf(s_rmax[tid], s_rmax[64 + tid]), fmaxf(s_rmax[128 + tid], s_rmax[192 + tid]));
-                const float m_old = s_m[tid];
-                float m_new = m_old, alpha = 1.f;
-                if (M > m_old + kRescaleLog2 || (m_old == -INFINITY && M != -INFINITY)) {
-                    m_new = M;
-                    alpha = fast_exp2(m_old - m_new);   // 0 when nothing was accumulated yet
-                    if (t > 0) s_flag[1] = 1;
-                }
-                s_mn[tid] = m_new;
-                s_al[tid] = alpha;
-            }
-            tc::named_bar(1, 128);
-            const bool rescale = s_flag[1] != 0;
+            bool exceed = false;
 #pragma unroll
             for (int j = 0; j < 32; j++) {
-                const float mn = s_mn[32 * hh + j];
-                s[j] = (mn == -INFINITY) ? 0.f : fast_exp2(s[j] - mn);
+                s[j] = valid ? s[j] * scale_log2 : -INFINITY;
+                exceed |= s[j] > m_run[j] + kRescaleLog2;   // a finite score always exceeds -inf
+            }
+            bool rescale = false;
+            if (tc::named_bar_or(1, 128, exceed || fail)) {
+                if (tc::named_bar_or(1, 128, fail)) {   // a wait gave up: every thread leaves together
+                    ok = false;
+                    break;
+                }
+                float r0, r1;
+                halfwarp_reduce32<true>(s, r0, r1);
+                const int h2 = 32 * hh + 2 * (lane & 15);
+                s_rmax[warp * 64 + h2] = r0;
+                s_rmax[warp * 64 + h2 + 1] = r1;
+                if (tid == 0) s_flag[1] = 0;
+                tc::named_bar(1, 128);
+                if (tid < kTcHeads) {
+                    const float M = fmaxf(fmaxf(s_rmax[tid], s_rmax[64 + tid]), fmaxf(s_rmax[128 + tid], s_rmax[192 + tid]));
+                    const float m_old = s_m[tid];
+                    float m_new = m_old, alpha = 1.f;
+                    if (M > m_old + kRescaleLog2 || (m_old == -INFINITY && M != -INFINITY)) {
+                        m_new = M;
+                        alpha = fast_exp2(m_old - m_new);   // 0 when nothing was accumulated yet
+                        if (t > 0) s_flag[1] = 1;
+                    }
+                    s_m[tid] = m_new;
+                    s_al[tid] = alpha;
+                }
+                tc::named_bar(1, 128);
+                rescale = s_flag[1] != 0;
+#pragma unroll
+                for (int j = 0; j < 32; j++) {
+                    m_run[j] = s_m[32 * hh + j];
+                    l_part[j] *= s_al[32 * hh + j];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                s[j] = (m_run[j] == -INFINITY) ? 0.f : fast_exp2(s[j] - m_run[j]);
+                l_part[j] += s[j];
             }
             // This P stage was last read by P V of tile t - 2, which must be done.
             // A rescale of the O^T columns also needs P V of tile t - 1 done; the
             // lazy maximum makes that rare, so P V of the previous tile usually
             // still runs while this tile's probabilities are written.
-            if (rescale ? (t >= 1 && !wait_all(BAR_KFREE + ((t - 1) & 1), (uint32_t)(((t - 1) >> 1) & 1)))
-                        : (t >= 2 && !wait_all(BAR_KFREE + (t & 1), (uint32_t)(((t - 2) >> 1) & 1)))) {
-                ok = false;
-                break;
-            }
+            if (rescale ? (t >= 1 && !mbar_wait(bar(BAR_KFREE + ((t - 1) & 1)), (uint32_t)(((t - 1) >> 1) & 1)))
+                        : (t >= 2 && !mbar_wait(bar(BAR_KFREE + (t & 1)), (uint32_t)(((t - 2) >> 1) & 1))))
+                fail = true;
             {
                 uint8_t *prow = sm + OFF_P + sidx * kReg + key * 128;
 #pragma unroll
@@ -512,21 +529,24 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 }
                 tc::tmem_wait_st();
             }
-            halfwarp_reduce32<false>(s, r0, r1);
-            s_rsum[warp * 64 + h2] = r0;
-            s_rsum[warp * 64 + h2 + 1] = r1;
             tc::fence_proxy_async();
             tc::fence_before_sync();
-            tc::named_bar(1, 128);
-            if (tid < kTcHeads) {
-                const float ls = s_rsum[tid] + s_rsum[64 + tid] + s_rsum[128 + tid] + s_rsum[192 + tid];
-                s_l[tid] = s_l[tid] * s_al[tid] + ls;
-                s_m[tid] = s_mn[tid];
-            }
             mbar_arrive(bar(BAR_PFULL + sidx));
         }
+        // the weights' sums over keys, once: lanes (keys) within each warp, then the warps
+        if (tc::named_bar_or(1, 128, fail)) ok = false;
+        {
+            float r0, r1;
+            halfwarp_reduce32<false>(l_part, r0, r1);
+            const int h2 = 32 * hh + 2 * (lane & 15);
+            s_rsum[warp * 64 + h2] = r0;
+            s_rsum[warp * 64 + h2 + 1] = r1;
+        }
+        tc::named_bar(1, 128);
+        if (tid < kTcHeads) s_l[tid] = s_rsum[tid] + s_rsum[64 + tid] + s_rsum[128 + tid] + s_rsum[192 + tid];
         // epilogue: O^T / l -> out[head][d] (bf16), lse
-        const bool done = ok && wait_all(BAR_OFULL, 0);
+        bool done = ok && mbar_wait(bar(BAR_OFULL), 0);
+        done = !tc::named_bar_or(1, 128, !done);   // also: s_l is complete
         if (done && nsplit > 1) {
             // partial result: unnormalised O^T -> [head][d] fp32 in the key
             // stages (every product is done with them), one bulk store

@@ -112,6 +112,17 @@ __device__ __forceinline__ void named_bar(int id, int count)
 {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
+// Named barrier over `count` threads that also ORs a predicate over them:
+// every participant gets true when any of them passed true.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred)
+{
+    uint32_t r;
+    asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbarrier.cta.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r)
+                 : "r"((uint32_t)pred), "r"(id), "r"(count)
+                 : "memory");
+    return r != 0;
+}
 
 }  // namespace tc
 }  // namespace csa
