@@ -568,12 +568,20 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             if (tid == 0) {
                 bulk_s2g(part_o + slot * kTcD, sb + OFF_K, kTcHeads * kTcD * 4);
                 bulk_commit();
-                bulk_wait_all();
+                bulk_wait_read();
             }
             if (tid < kTcHeads) part_ml[slot + tid] = make_float2(s_m[tid], s_l[tid]);
         } else if (done) {
+            // 1/l once per head; the bf16 result [64 heads][512] is staged in
+            // the key stages (every product is done with them) and leaves with
+            // one bulk copy: the query's 64 head rows are contiguous in `out`
+            if (tid < kTcHeads) {
+                const float l = s_l[tid];
+                s_al[tid] = l > 0.f ? 1.f / l : 0.f;
+            }
+            tc::named_bar(1, 128);
             tc::fence_after_sync();
-            uint16_t *orow = out + (qi * H + (int64_t)hg * kTcHeads) * kTcD;
+            uint16_t *stg = reinterpret_cast<uint16_t *>(sm + OFF_K);
 #pragma unroll 1
             for (int c = 0; c < 8; c++) {
                 float o[32];
@@ -582,11 +590,15 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 const int d = 128 * (c >> 1) + tid;
                 const int h0 = 32 * (c & 1);
 #pragma unroll
-                for (int j = 0; j < 32; j++) {
-                    const float l = s_l[h0 + j];
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
-                    __stcs(orow + (int64_t)(h0 + j) * kTcD + d, (uint16_t)f32_to_bf16_bits(o[j] * inv));   // streaming
-                }
+                for (int j = 0; j < 32; j++)
+                    stg[(h0 + j) * kTcD + d] = (uint16_t)(pack_bf16x2(o[j] * s_al[h0 + j], 0.f) & 0xffffu);
+            }
+            tc::fence_proxy_async();
+            tc::named_bar(1, 128);
+            if (tid == 0) {
+                bulk_s2g(out + (qi * H + (int64_t)hg * kTcHeads) * kTcD, sb + OFF_K, kTcHeads * kTcD * 2);
+                bulk_commit();
+                bulk_wait_read();
             }
             if (lse && tid < kTcHeads)
                 lse[qi * H + (int64_t)hg * kTcHeads + tid] = (s_m[tid] + log2f(s_l[tid])) * kTcLn2;

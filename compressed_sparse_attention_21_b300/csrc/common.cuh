@@ -238,6 +238,10 @@ __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 // every bulk group of this thread complete (its global writes performed)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+// every bulk group of this thread has read its shared-memory source (the
+// source may be reused or the CTA may exit; the global writes complete on
+// their own and are visible once the grid has completed)
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 
 // Warp 0: in a 256-bin histogram walked from the top bin down, find the bin
 // that holds the `remaining`-th largest element; report it and the count of
@@ -271,6 +275,16 @@ __device__ __forceinline__ void find_digit_256(const uint32_t *hist, uint32_t re
             acc += c[i];
         }
     }
+}
+
+// Warp-aggregated shared-memory histogram increment: lanes that hit the same
+// bin add their count with one atomic.  All 32 lanes of the warp must call.
+__device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t bin, bool valid)
+{
+    const unsigned act = __ballot_sync(0xffffffffu, valid);
+    if (!valid) return;
+    const unsigned peers = __match_any_sync(act, bin);
+    if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(hist + bin, (uint32_t)__popc(peers));
 }
 
 // CTA-wide exclusive scan of one value per thread; returns the prefix and

@@ -129,15 +129,6 @@ __device__ __forceinline__ float score_row(const uint16_t *__restrict__ krow, co
     return acc;
 }
 
-// Warp-aggregated shared-memory histogram increment; all 32 lanes must call.
-__device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t bin, bool valid)
-{
-    const unsigned act = __ballot_sync(0xffffffffu, valid);
-    if (!valid) return;
-    const unsigned peers = __match_any_sync(act, bin);
-    if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(hist + bin, (uint32_t)__popc(peers));
-}
-
 __device__ __forceinline__ void write_row_padding(int32_t *idx_row, float *score_row_out, int from, int top_k)
 {
     for (int i = from + threadIdx.x; i < top_k; i += blockDim.x) {
