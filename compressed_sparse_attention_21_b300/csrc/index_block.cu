@@ -45,17 +45,24 @@ struct BCfg {
     static constexpr int RB = 2 * DI;            // bytes of a key row
     static constexpr int PRB = RB + 16;          // padded row stride: ldmatrix without bank conflicts
     static constexpr int CPR = RB / 16;          // 16-byte chunks per row
-    static constexpr int KS = DI / 16;           // k-steps of 16
     static constexpr uint32_t buf_bytes = kBRows * PRB;
+    // chunks in the streaming ring (all but one in flight while one is scored)
+    static constexpr int NB = DI == 32 ? 6 : (DI == 64 ? 5 : 2);
     // shared-memory layout (bytes)
-    static constexpr uint32_t off_buf = 0;                                   // 2 chunk buffers
-    static constexpr uint32_t off_qs = off_buf + 2 * buf_bytes;              // [16][DI] fp32 head sums
+    static constexpr uint32_t off_buf = 0;                                   // NB chunk buffers
+    static constexpr uint32_t off_qs = off_buf + NB * buf_bytes;             // [16][DI] fp32 head sums
     static constexpr uint32_t off_skey = off_qs + kBQ * DI * 4;              // [16][256] sampled keys
     static constexpr uint32_t off_gt = off_skey + kBQ * kBSample * 4;        // bitmaps and their prefixes
     static constexpr uint32_t off_eq = off_gt + kBWords * 4;
     static constexpr uint32_t off_pre = off_eq + kBWords * 4;                // packed (gt << 16 | eq) prefix
     static constexpr uint32_t off_end = off_pre + kBWords * 4;
     static constexpr size_t smem = off_end;
+    // per-warp selection scratch, in the ring once the keys have streamed by:
+    // a 256-bin histogram, the taken-entry bitmap and its 16-bit word prefixes
+    static constexpr uint32_t warp_scratch = 256 * 4 + kBWords * 4 + kBWords * 2;
+    static_assert(kBQ * warp_scratch <= NB * buf_bytes, "selection scratch fits the ring");
+    static_assert(kBQ * 256 * 4 <= buf_bytes, "sampling histograms fit one chunk buffer");
+    static_assert(smem <= 232448, "shared memory per CTA");
 };
 
 struct BlockQ {           // per-query record of the current block
@@ -124,6 +131,139 @@ __device__ __forceinline__ void load_rows(uint32_t buf, const uint16_t *kseq, Ro
         cp_async_16(buf + r * C::PRB + c * 16, e >= 0 ? (const void *)(kseq + e * DI + c * 8) : (const void *)safe,
                     e >= 0 ? 16 : 0);
     }
+}
+
+// The k-th largest of a warp's keys (k >= 1; at least k keys exist): four
+// 8-bit radix levels over the keys that `get(i, key)` hands out for
+// i < count (lane-strided), with a warp-private 256-bin histogram `hist` and
+// two words `dig` of shared memory.  Stops at the first level whose bin is
+// taken whole.  Returns the prefix found (its lower bits zero when it stopped
+// early) in *kstar and the number of keys equal to it still to take in
+// *need_eq (0xffffffff when every key at or above *kstar is taken).  Every
+// lane of the warp calls it.
+template <typename Get>
+__device__ __forceinline__ void warp_radix_select(Get get, int count, uint32_t k, uint32_t *hist, uint32_t *dig,
+                                                  uint32_t *kstar, uint32_t *need_eq)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t prefix = 0, pmask = 0, remaining = k;
+    bool whole = false;
+#pragma unroll 1
+    for (int sh = 24; sh >= 0 && !whole; sh -= 8) {
+#pragma unroll
+        for (int i = 0; i < 8; i++) hist[lane * 8 + i] = 0;
+        __syncwarp();
+        constexpr int U = 8;
+#pragma unroll 1
+        for (int base = 0; base < count; base += 32 * U) {
+            uint32_t kk[U];
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int i = base + 32 * u + lane;
+                kk[u] = 0;
+                if (i < count) get(i, kk[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int i = base + 32 * u + lane;
+                hist_add(hist, (kk[u] >> sh) & 255u, i < count && (kk[u] & pmask) == prefix);
+            }
+        }
+        __syncwarp();
+        find_digit_256(hist, remaining, &dig[0], &dig[1]);
+        __syncwarp();
+        const uint32_t d = dig[0];
+        remaining -= dig[1];
+        prefix |= d << sh;
+        pmask |= 255u << sh;
+        whole = hist[d] == remaining;
+        __syncwarp();   // hist and dig are rewritten by the next level
+    }
+    *kstar = prefix;
+    *need_eq = whole ? 0xffffffffu : remaining;
+}
+
+// One query's top-k by one warp, from its `cnt` candidates (key << 32 | entry,
+// every entry at or above the query's threshold) in global memory: the exact
+// k-th key, then a bitmap of the taken entries, its word prefixes, and the
+// selection written in index order.  Returns false, writing nothing, when keys
+// equal to the k-th key would have to be split (the block-wide selection
+// resolves that case).
+__device__ __forceinline__ bool warp_select_write(const uint64_t *__restrict__ cand, int cnt, int n, int top_k,
+                                                  uint8_t *scratch, uint32_t *dig, int32_t *idx_row, float *sc_row)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t *hist = reinterpret_cast<uint32_t *>(scratch);
+    uint32_t *taken = hist + 256;
+    uint16_t *pre = reinterpret_cast<uint16_t *>(taken + kBWords);
+    const uint32_t k_eff = (uint32_t)(n < top_k ? n : top_k);
+    uint32_t kstar, need_eq;
+    warp_radix_select([&](int i, uint32_t &key) { key = (uint32_t)(__ldcg(cand + i) >> 32); }, cnt, k_eff, hist, dig,
+                      &kstar, &need_eq);
+    if (need_eq != 0xffffffffu) return false;   // ties at the k-th key: the block-wide path
+    const int words = (n + 31) >> 5;
+    for (int w = lane; w < words; w += 32) taken[w] = 0;
+    __syncwarp();
+    constexpr int U = 8;
+#pragma unroll 1
+    for (int base = 0; base < cnt; base += 32 * U) {
+        uint64_t v[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int i = base + 32 * u + lane;
+            v[u] = i < cnt ? __ldcg(cand + i) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int i = base + 32 * u + lane;
+            const uint32_t e = (uint32_t)v[u];
+            if (i < cnt && (uint32_t)(v[u] >> 32) >= kstar) atomicOr(&taken[e >> 5], 1u << (e & 31));
+        }
+    }
+    __syncwarp();
+    // word prefixes: lane takes a contiguous run of words
+    const int wpl = (words + 31) / 32;
+    const int w0 = lane * wpl, w1 = w0 + wpl < words ? w0 + wpl : words;
+    uint32_t mine = 0;
+    for (int w = w0; w < w1; w++) mine += (uint32_t)__popc(taken[w]);
+    uint32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    uint32_t run = incl - mine;
+    for (int w = w0; w < w1; w++) {
+        pre[w] = (uint16_t)run;
+        run += (uint32_t)__popc(taken[w]);
+    }
+    __syncwarp();
+#pragma unroll 1
+    for (int base = 0; base < cnt; base += 32 * U) {
+        uint64_t v[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int i = base + 32 * u + lane;
+            v[u] = i < cnt ? __ldcg(cand + i) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int i = base + 32 * u + lane;
+            const uint32_t key = (uint32_t)(v[u] >> 32), e = (uint32_t)v[u];
+            if (i < cnt && key >= kstar) {
+                const uint32_t pos = pre[e >> 5] + (uint32_t)__popc(taken[e >> 5] & ((1u << (e & 31)) - 1u));
+                if (pos < (uint32_t)top_k) {
+                    idx_row[pos] = (int32_t)e;
+                    if (sc_row) sc_row[pos] = key_score(key);
+                }
+            }
+        }
+    }
+    for (int i = (int)k_eff + lane; i < top_k; i += 32) {
+        idx_row[i] = -1;
+        if (sc_row) sc_row[i] = -INFINITY;
+    }
+    return true;
 }
 
 // Exact selection of one query's top-k among the (key, entry) pairs that
@@ -237,8 +377,11 @@ index_block_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, c4 = lane & 3;
+    __shared__ uint32_t s_wdig[kBQ][2];
+    __shared__ int s_fall[kBQ];
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t buf0 = sbase + C::off_buf, buf1 = buf0 + C::buf_bytes;
+    const uint32_t buf0 = sbase + C::off_buf;
+    auto bufn = [&](int i) { return buf0 + (uint32_t)i * C::buf_bytes; };
     float *qs = reinterpret_cast<float *>(sm + C::off_qs);
     uint32_t *skey = reinterpret_cast<uint32_t *>(sm + C::off_skey);
     uint64_t *cand = cand_ws + (int64_t)blockIdx.x * kBQ * kBCap;
@@ -310,25 +453,21 @@ index_block_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *
                         skey[qq * kBSample + s_i] = v ? score_key(sc[t][r]) : 0u;
                     }
                 __syncthreads();
-                // rank select: 32 threads per query, 8 samples each
+                // the m-th largest sampled key of each query, one warp per query
+                // (the histograms use the second chunk buffer, idle here)
                 {
-                    const int qq = tid >> 5;
+                    const int qq = warp;
                     const BlockQ &Q = s_q[qq];
                     if (qq >= ga && qq < gz && Q.ok && Q.n > kBCap) {
                         int m = (int)(((int64_t)kBSample * 2 * top_k + Q.n - 1) / Q.n);
                         if (m < 1) m = 1;
                         if (m <= kBSample) {
                             const uint32_t *kk = skey + qq * kBSample;
-                            for (int i = 0; i < 8; i++) {
-                                const int s_i = lane * 8 + i;
-                                const uint32_t mine = kk[s_i];
-                                int rank = 0;
-                                for (int o = 0; o < kBSample; o++) {
-                                    const uint32_t other = kk[o];
-                                    rank += (other > mine) || (other == mine && o < s_i);
-                                }
-                                if (rank == m - 1) s_tau[qq] = mine;
-                            }
+                            uint32_t *hist = reinterpret_cast<uint32_t *>(sm + C::off_buf + C::buf_bytes) + qq * 256;
+                            uint32_t tau, need;
+                            warp_radix_select([&](int i, uint32_t &key) { key = kk[i]; }, kBSample, (uint32_t)m, hist,
+                                              s_wdig[qq], &tau, &need);
+                            if (lane == 0) s_tau[qq] = tau;
                         }
                     }
                 }
@@ -336,22 +475,24 @@ index_block_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *
             }
             // ---- stream the keys, keep candidates ----
             const int nchunks = (n_max + kBRows - 1) / kBRows;
-            if (nchunks > 0) {
-                load_rows<DI>(buf0, kseq, [&](int r) -> int64_t { return r < n_max ? r : -1; }, kI);
+            constexpr int NB = C::NB;
+            auto load_chunk = [&](int c) {
+                const int base = c * kBRows;
+                load_rows<DI>(bufn(c % NB), kseq, [&](int r) -> int64_t { return base + r < n_max ? base + r : -1; },
+                              kI);
+            };
+            // ring of NB chunk buffers: chunks c + 1 .. c + NB - 1 load while chunk c is scored
+            for (int c = 0; c < NB - 1; c++) {
+                if (c < nchunks) load_chunk(c);
                 cp_async_commit();
             }
             for (int c = 0; c < nchunks; c++) {
-                const uint32_t cur = (c & 1) ? buf1 : buf0, nxt = (c & 1) ? buf0 : buf1;
-                if (c + 1 < nchunks) {
-                    const int base = (c + 1) * kBRows;
-                    load_rows<DI>(nxt, kseq, [&](int r) -> int64_t { return base + r < n_max ? base + r : -1; },
-                                  kI);
-                }
+                if (c + NB - 1 < nchunks) load_chunk(c + NB - 1);   // the buffer chunk c - 1 left
                 cp_async_commit();
-                cp_async_wait<1>();
+                cp_async_wait<NB - 1>();
                 __syncthreads();
                 float sc[2][4];
-                warp_scores<DI>(cur, afr, sc);
+                warp_scores<DI>(bufn(c % NB), afr, sc);
 #pragma unroll
                 for (int t = 0; t < 2; t++)
 #pragma unroll
@@ -369,23 +510,51 @@ index_block_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *
             }
             cp_async_wait<0>();
             __syncthreads();
-            // ---- exact selection, query by query ----
+            // ---- exact selection: one warp per query (the ring is free now) ----
+            {
+                const int qq = warp;
+                int fall = 0;
+                if (qq >= ga && qq < gz) {
+                    const BlockQ Q = s_q[qq];
+                    const int64_t qi = q0 + qq;
+                    int32_t *idx_row = idx_out + qi * top_k;
+                    float *sc_row = score_out ? score_out + qi * top_k : nullptr;
+                    if (!Q.ok) {
+                        if (lane == 0) set_error(err, CSA_ERR_DEVICE);
+                        for (int i = lane; i < top_k; i += 32) {
+                            idx_row[i] = -1;
+                            if (sc_row) sc_row[i] = -INFINITY;
+                        }
+                    } else {
+                        const uint32_t cnt = s_cnt[qq];
+                        const uint32_t k_eff = (uint32_t)(Q.n < top_k ? Q.n : top_k);
+                        if (k_eff == 0) {
+                            for (int i = lane; i < top_k; i += 32) {
+                                idx_row[i] = -1;
+                                if (sc_row) sc_row[i] = -INFINITY;
+                            }
+                        } else if (cnt >= k_eff && cnt <= (uint32_t)kBCap) {
+                            fall = warp_select_write(cand + qq * kBCap, (int)cnt, Q.n, top_k,
+                                                     sm + C::off_buf + qq * C::warp_scratch, s_wdig[qq], idx_row,
+                                                     sc_row) ? 0 : 1;   // 1: ties at the k-th key
+                        } else {
+                            fall = 2;   // the sample misjudged the row: every score again
+                        }
+                    }
+                }
+                if (lane == 0) s_fall[qq] = fall;
+            }
+            __syncthreads();
+            // ---- the rare queries the warps left: the whole block, one query at a time ----
             for (int qq = ga; qq < gz; qq++) {
+                const int fall = s_fall[qq];
+                if (!fall) continue;
                 const BlockQ Q = s_q[qq];
                 const int64_t qi = q0 + qq;
                 int32_t *idx_row = idx_out + qi * top_k;
                 float *sc_row = score_out ? score_out + qi * top_k : nullptr;
-                if (!Q.ok) {
-                    if (tid == 0) set_error(err, CSA_ERR_DEVICE);
-                    for (int i = tid; i < top_k; i += kBT) {
-                        idx_row[i] = -1;
-                        if (sc_row) sc_row[i] = -INFINITY;
-                    }
-                    continue;
-                }
                 const uint32_t cnt = s_cnt[qq];
-                const uint32_t k_eff = (uint32_t)(Q.n < top_k ? Q.n : top_k);
-                if (cnt >= k_eff && cnt <= (uint32_t)kBCap) {
+                if (fall == 1) {
                     constexpr int KPT = kBCap / kBT;
                     uint64_t cv[KPT];
 #pragma unroll
@@ -405,7 +574,7 @@ index_block_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *
                     select_write<KPT>(src, Q.n, top_k, sm + C::off_gt, sm + C::off_eq, sm + C::off_pre, s_hist, s_w,
                                       s_dig, idx_row, sc_row);
                 } else {
-                    // exact fallback: every score of this query, recomputed when needed
+                    // exact fallback: every score of this query, recomputed
                     const float *qv = qs + qq * DI;
                     const int n = Q.n;
                     auto src = [&](int i, uint32_t &key, int32_t &ent) -> bool {
