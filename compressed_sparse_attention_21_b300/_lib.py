@@ -328,7 +328,9 @@ class Hybrid:
     """One hybrid_attend problem: owns the parameter block and its buffers."""
 
     def __init__(self, layout, kv, gate, q_idx, k_idx, q, top_k, scale, csa_cache=None, hca_cache=None,
-                 skip_compress=False, with_scores=False, ws=None, k_idx_fp8=None):
+                 skip_compress=False, with_scores=False, ws=None, k_idx_fp8=None, outputs=None):
+        """outputs: optional (o_csa, o_hca, lse_csa, lse_hca) device tensors to write into
+        (e.g. views of one buffer that a single copy moves to the host)."""
         dev = q.device
         H, d = q.shape[-2], q.shape[-1]
         self.layout = layout
@@ -339,10 +341,13 @@ class Hybrid:
             torch.empty((layout.total_hca, d), dtype=torch.bfloat16, device=dev)
         self.idx = torch.empty((layout.total_q, top_k), dtype=torch.int32, device=dev)
         self.score = torch.empty((layout.total_q, top_k), dtype=torch.float32, device=dev) if with_scores else None
-        self.o_csa = torch.empty_like(q)
-        self.o_hca = torch.empty_like(q)
-        self.lse_csa = torch.empty((layout.total_q, H), dtype=torch.float32, device=dev)
-        self.lse_hca = torch.empty((layout.total_q, H), dtype=torch.float32, device=dev)
+        if outputs is not None:
+            self.o_csa, self.o_hca, self.lse_csa, self.lse_hca = outputs
+        else:
+            self.o_csa = torch.empty_like(q)
+            self.o_hca = torch.empty_like(q)
+            self.lse_csa = torch.empty((layout.total_q, H), dtype=torch.float32, device=dev)
+            self.lse_hca = torch.empty((layout.total_q, H), dtype=torch.float32, device=dev)
         p = csa_hybrid_params()
         p.layout = layout.c
         p.d, p.n_heads, p.n_heads_idx, p.d_idx = d, H, q_idx.shape[-2], q_idx.shape[-1]

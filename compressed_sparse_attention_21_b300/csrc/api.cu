@@ -310,8 +310,10 @@ csa_status_t compress_impl(const csa_layout *L, bool csa_side, const csa_bf16 *k
 }
 
 // SMs of the two attention branches, which run at the same time in a decode
-// step: in proportion to their largest key counts, so that both split-KV
-// grids fit on the GPU together.
+// step: in proportion to their largest key counts, the sparse branch's keys
+// counted twice (it starts only after the top-k selection, while the dense
+// branch starts after the key scan), so that both split-KV grids fit on the
+// GPU together and finish at about the same time.
 void hybrid_shares(const csa_hybrid_params *p, int num_sms, int *sparse_share, int *dense_share)
 {
     const csa_layout *L = &p->layout;
@@ -322,6 +324,7 @@ void hybrid_shares(const csa_hybrid_params *p, int num_sms, int *sparse_share, i
     int64_t kd = Lmax / p->ratio_hca + p->ratio_hca - 1;
     ks = ks < Lmax ? ks : Lmax;
     kd = kd < Lmax ? kd : Lmax;
+    ks *= 2;
     const int n = num_sms > 0 ? num_sms : 148;
     int64_t d = ks + kd > 0 ? (int64_t)n * kd / (ks + kd) : n / 2;
     if (d < n / 8) d = n / 8;
