@@ -173,6 +173,7 @@ IndexArgs index_args(const csa_layout *L, const csa_bf16 *q_idx, const csa_bf16 
     a.max_kv_len = L->max_kv_len;
     a.max_q_len = L->max_q_len;
     a.total_q = L->total_q;
+    a.total_csa = L->total_csa;
     a.pdl = false;
     a.scan_done = nullptr;
     a.cu_kv = L->cu_kv;

@@ -46,10 +46,15 @@
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
+#include "tma.h"
 
 namespace csa {
 
 namespace {
+
+using tc::policy_evict_first;
+using tc::policy_evict_last;
+using tc::tma_tile2d;
 
 constexpr int kTcThreads = 384;
 constexpr int kGatherBase = 192;             // first cp.async gather thread (warp 6)
@@ -113,32 +118,6 @@ __device__ __forceinline__ void halfwarp_reduce32(const float *v, float &r0, flo
     r1 = a[1];
 }
 
-// L2 eviction policies: the compressed entries are read by many queries and
-// should stay in L2; each query's own rows (its query tile, its raw tail, its
-// output) are touched once and should leave first.
-__device__ __forceinline__ uint64_t policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_first()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
-    return p;
-}
-
-// TMA loads into 128-byte swizzled shared memory, completing on `bar`, with
-// an L2 policy.  64 x box-rows tile at (column x, row y):
-__device__ __forceinline__ void tma_tile2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar,
-                                           uint64_t pol)
-{
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-                 " [%0], [%1, {%2, %3}], [%4], %5;\n"
-                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
-                 : "memory");
-}
 // 16-byte cp.async (src_bytes < 16 zero-fills the rest) with an L2 policy.
 __device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, int src_bytes, uint64_t pol)
 {
@@ -715,36 +694,11 @@ size_t tc_ws_bytes(const AttendArgs &a, const TcPlan &pl, float **part_o, float2
     return ml + slots * kTcD * sizeof(float);
 }
 
-// cuTensorMapEncodeTiled from the driver (looked up once).
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
 // A [rows, 512] bf16 row-major matrix as a TMA source: boxes of 64 columns
 // (128 bytes, swizzled) by box_rows rows.
 cudaError_t rows_map(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 f = encode_fn();
-    if (!f) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)kTcD, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kTcD * 2};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t es[2] = {1, 1};
-    const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return tma_map_bf16(m, base, rows, kTcD, 64, box_rows);
 }
 
 template <bool GATHER>
@@ -791,7 +745,7 @@ bool attend_tc_applicable(const AttendArgs &a)
     // row coordinates of the TMA loads are 32-bit
     return a.d == kTcD && a.n_heads % kTcHeads == 0 && (a.idx == nullptr || a.top_k <= kTcIdxCap) &&
            a.total_q * a.n_heads < 0x7fffffffLL && a.n_kv_rows < 0x7fffffffLL && a.n_ent_rows < 0x7fffffffLL &&
-           encode_fn() != nullptr;
+           tma_available();
 }
 
 size_t attend_tc_workspace_bytes(const AttendArgs &a) { return tc_ws_bytes(a, tc_plan(a), nullptr, nullptr); }
@@ -800,6 +754,42 @@ cudaError_t launch_attend_tc(const AttendArgs &a, cudaStream_t st)
 {
     if (a.total_q <= 0) return cudaSuccess;
     return a.idx ? launch_tc<true>(a, st) : launch_tc<false>(a, st);
+}
+
+// ---- TMA descriptors (declared in tma.h) ----
+namespace {
+// cuTensorMapEncodeTiled from the driver (looked up once).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+}  // namespace
+
+bool tma_available() { return encode_fn() != nullptr; }
+
+cudaError_t tma_map_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t box_cols,
+                         uint32_t box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 f = encode_fn();
+    if (!f) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace csa

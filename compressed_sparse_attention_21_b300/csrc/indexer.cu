@@ -1063,10 +1063,11 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
     // single-kernel paths mark it up front (their kernel holds the GPU to the end)
     auto mark = [&]() -> cudaError_t { return a.scan_done ? cudaEventRecord(a.scan_done, st) : cudaSuccess; };
     const bool fp8 = a.fp8;   // FP8 keys: the chunk scan and the select only
-    if (!fp8 && (index_block_applicable(a) || use_cta_path(a))) {
+    if (!fp8 && (index_tc_applicable(a) || index_block_applicable(a) || use_cta_path(a))) {
         cudaError_t e = mark();
         if (e != cudaSuccess) return e;
     }
+    if (!fp8 && index_tc_applicable(a)) return launch_index_tc(a, st);
     if (!fp8 && index_block_applicable(a)) return launch_index_block(a, st);
     if (!fp8 && use_cta_path(a)) {
         const int64_t nsm = max_n < 1 ? 1 : max_n;
@@ -1138,6 +1139,7 @@ bool index_supported(int n_heads_idx, int d_idx, int top_k)
 size_t index_workspace_bytes(const IndexArgs &a)
 {
     if (a.total_q <= 0) return 0;
+    if (index_tc_applicable(a)) return index_tc_ws_bytes(a);
     if (index_block_applicable(a)) return index_block_ws_bytes(a);
     if (use_cta_path(a)) return 0;
     const int64_t max_n = a.max_kv_len / a.ratio;
@@ -1301,13 +1303,14 @@ cudaError_t index_static_scratch(void **ptr)
 
 size_t index_static_need_bytes(const IndexArgs &a)
 {
+    if (a.total_q > 0 && index_tc_applicable(a)) return index_tc_min_ws_bytes();
     if (a.total_q > 0 && index_block_applicable(a)) return index_block_min_ws_bytes();
     return index_workspace_bytes(a);
 }
 
 size_t index_static_zero_bytes(const IndexArgs &a)
 {
-    if (a.total_q <= 0 || index_block_applicable(a) || use_cta_path(a)) return 0;
+    if (a.total_q <= 0 || index_tc_applicable(a) || index_block_applicable(a) || use_cta_path(a)) return 0;
     const int64_t gq = group_size(a);
     return (size_t)(align_up(gq * kHistBins * 4, 256) + align_up(gq * kMetaWords * 4, 256));
 }

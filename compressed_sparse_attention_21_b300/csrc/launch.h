@@ -102,6 +102,7 @@ struct IndexArgs {
     int batch;
     int max_kv_len, max_q_len;
     int64_t total_q;
+    int64_t total_csa;    // rows of k_idx (all sequences)
     bool pdl;             // the key scan of the multi-kernel paths may overlap the stream's previous kernel
     cudaEvent_t scan_done;  // if set: recorded on the stream once every key has been scored
     const int64_t *cu_kv, *cu_q, *cu_csa;
@@ -123,6 +124,12 @@ bool index_block_applicable(const IndexArgs &a);
 size_t index_block_ws_bytes(const IndexArgs &a);      // for a full grid of persistent CTAs
 size_t index_block_min_ws_bytes();                      // one CTA (the kernel fits its grid to ws_bytes)
 cudaError_t launch_index_block(const IndexArgs &a, cudaStream_t st);
+// prefill-sized batches with d_idx = 64 (index_tc.cu): tensor-memory score
+// tiles of 128 queries x 256 keys, the same selection
+bool index_tc_applicable(const IndexArgs &a);
+size_t index_tc_ws_bytes(const IndexArgs &a);         // for a full grid of persistent CTAs
+size_t index_tc_min_ws_bytes();                         // one CTA (the kernel fits its grid to ws_bytes)
+cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t st);
 size_t index_workspace_bytes(const IndexArgs &a);
 // FP8 keys (fp8 set): the chunk scan and the clustered select, rows of up
 // to index_fp8_max_n() entries

@@ -3,6 +3,7 @@
 // tensor-memory loads and stores.  Inline PTX for sm_103a.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -124,5 +125,31 @@ __device__ __forceinline__ bool named_bar_or(int id, int count, bool pred)
     return r != 0;
 }
 
+// L2 eviction policies: the compressed entries are read by many queries and
+// should stay in L2; each query's own rows (its query tile, its raw tail, its
+// output) are touched once and should leave first.
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
+}
+
+// TMA loads into 128-byte swizzled shared memory, completing on `bar`, with
+// an L2 policy.  64 x box-rows tile at (column x, row y):
+__device__ __forceinline__ void tma_tile2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar,
+                                           uint64_t pol)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%2, %3}], [%4], %5;\n"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+                 : "memory");
+}
 }  // namespace tc
 }  // namespace csa

@@ -135,9 +135,11 @@ def test_index_topk_multi_cta_path(HI, dI, k):
     assert kinds["equal"] >= len(lengths) - 1
 
 
-@pytest.mark.parametrize("HI,dI,k", [(2, 32, 64), (4, 64, 512)])
-def test_index_topk_cta_path(HI, dI, k):
-    lengths = [1500, 700]                  # 2200 queries: the per-query CTA path
+@pytest.mark.parametrize("HI,dI,k", [(2, 32, 64), (4, 64, 512), (4, 64, 7), (1, 128, 100)])
+def test_index_topk_prefill_paths(HI, dI, k):
+    # 2200 queries, rows of at most 375 entries: the prefill paths (tensor-memory
+    # score tiles for d_I = 64, mma.sync tiles otherwise) keep every entry
+    lengths = [1500, 700]
     p = problem(lengths, lengths, HI=HI, dI=dI, k=k, seed=12)
     g = P.GpuProblem(p)
     idx, score = csa.lightning_index_topk(g.layout, g.qI, g.kI, k)
@@ -145,13 +147,51 @@ def test_index_topk_cta_path(HI, dI, k):
     _check_index(p, idx, score)
 
 
+def _check_index_rows(p, idx, score, rows):
+    """_check_index on the listed query rows only (long prefills)."""
+    inp = wl.to_numpy(p)
+    kinds = {"equal": 0, "tie": 0, "fp32tie": 0}
+    for qi in rows:
+        b = int(np.searchsorted(inp["cu_q"], qi, side="right") - 1)
+        L = inp["cu_kv"][b + 1] - inp["cu_kv"][b]
+        t = L - (inp["cu_q"][b + 1] - inp["cu_q"][b]) + (qi - inp["cu_q"][b])
+        n = int((t + 1) // p["mC"])
+        kseq = inp["kI"][inp["cu_csa"][b]:inp["cu_csa"][b] + n]
+        s = oracle.index_scores(inp["qI"][qi], kseq) if n else np.zeros(0)
+        kind, _ = P.check_topk_row(idx[qi], oracle.topk(s, p["top_k"]), s, n, p["top_k"], inp["qI"][qi], kseq)
+        kinds[kind] += 1
+        v = idx[qi] >= 0
+        assert np.allclose(score[qi][v], s[idx[qi][v]], rtol=1e-5, atol=1e-3)
+    return kinds
+
+
+@pytest.mark.parametrize("k", [64, 512, 1024])
+def test_index_topk_prefill_sampled_threshold(k):
+    # rows longer than the candidate buffer (n > 4096): the sampled threshold,
+    # the candidate filter and the warp selection; three sequences share the
+    # first 128-query block of the tensor-memory path
+    lengths = [60, 5, 20000, 3000]
+    p = problem(lengths, lengths, HI=4, dI=64, k=k, seed=14)
+    g = P.GpuProblem(p)
+    idx, score = csa.lightning_index_topk(g.layout, g.qI, g.kI, k)
+    torch.cuda.synchronize()
+    idx, score = idx.cpu().numpy(), score.cpu().numpy()
+    rng = np.random.default_rng(15)
+    total = sum(lengths)
+    rows = np.unique(np.concatenate([np.arange(0, 200), np.arange(16380, 16420), np.arange(20060, 20070),
+                                     np.arange(total - 40, total), rng.integers(0, total, 300)]))
+    kinds = _check_index_rows(p, idx, score, rows)
+    assert kinds["equal"] >= len(rows) - 3, kinds
+
+
+@pytest.mark.parametrize("dI", [32, 64])
 @pytest.mark.parametrize("queries", ["decode", "prefill", "prefill_overflow"])
-def test_index_topk_all_ties_lowest_index_wins(queries):
+def test_index_topk_all_ties_lowest_index_wins(queries, dI):
     # prefill_overflow: rows longer than the prefill path's candidate buffer, all
     # scores equal, so the exact fallback selection must run
     lengths = {"prefill": [3000, 4100], "decode": [3000, 4100, 9000], "prefill_overflow": [17000]}[queries]
     queries = "prefill" if queries.startswith("prefill") else queries
-    p = problem(lengths, lengths if queries == "prefill" else [1] * len(lengths), HI=2, dI=32, k=64, seed=13)
+    p = problem(lengths, lengths if queries == "prefill" else [1] * len(lengths), HI=2, dI=dI, k=64, seed=13)
     p["kI"] = torch.ones_like(p["kI"])      # every entry scores the same
     g = P.GpuProblem(p)
     idx, _ = csa.lightning_index_topk(g.layout, g.qI, g.kI, 64)
