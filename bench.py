@@ -38,18 +38,12 @@ EXTRA_WORKLOADS = ("prefill_128k", "ragged_decode", "decode_1m")
 # keyed by (workload, call, indexer key format), with the sha256 of the sources at capture time;
 # a changed source makes the figure stale and it is reported as null.
 NCU_TRAFFIC = {
-    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,598,976 B read +
+    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,599,360 B read +
     # index_select_kernel 1,352,064 B read, 0 B written (means of two captured calls)
     ("decode_64k", "index_topk", "bf16"): {
-        "bytes_per_launch": 34951040,
-        "sources": {"indexer.cu": "a1e1289bf84ad5178c2e4026409408b38ad3de278e5f61d6f4c0c2a571b4998d",
-                    "common.cuh": "c163a7f706451d39f03aab7a1b3d9ca5dd901eb0067e2031b1f8ae5268757c9d"},
-    },
-    # the same call on FP8 E4M3 keys: scan 17,875,328 B read + select 1,352,192 B read, 0 B written
-    ("decode_64k", "index_topk", "fp8"): {
-        "bytes_per_launch": 19227520,
-        "sources": {"indexer.cu": "a1e1289bf84ad5178c2e4026409408b38ad3de278e5f61d6f4c0c2a571b4998d",
-                    "common.cuh": "c163a7f706451d39f03aab7a1b3d9ca5dd901eb0067e2031b1f8ae5268757c9d"},
+        "bytes_per_launch": 34951424,
+        "sources": {"indexer.cu": "5bc85f0caf70f1dd126680f4d5e1a7e9b2ef68237de83f15d5a895914e5c1fd2",
+                    "common.cuh": "8f53808619b116427904fbedf2719663a9b508addd86fc0b6cc31ff4bb12667b"},
     },
 }
 
