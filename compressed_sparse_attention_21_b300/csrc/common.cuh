@@ -277,14 +277,13 @@ __device__ __forceinline__ void find_digit_256(const uint32_t *hist, uint32_t re
     }
 }
 
-// Warp-aggregated shared-memory histogram increment: lanes that hit the same
-// bin add their count with one atomic.  All 32 lanes of the warp must call.
+// Shared-memory histogram increment.  A plain atomic: measured on B300 with
+// 512 threads, shared atomics retire 16-30 lanes per cycle per SM (lanes of a
+// warp on one address are merged), while aggregating the lanes first with
+// __match_any_sync managed 0.6.
 __device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t bin, bool valid)
 {
-    const unsigned act = __ballot_sync(0xffffffffu, valid);
-    if (!valid) return;
-    const unsigned peers = __match_any_sync(act, bin);
-    if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(hist + bin, (uint32_t)__popc(peers));
+    if (valid) atomicAdd(hist + bin, 1u);
 }
 
 // CTA-wide exclusive scan of one value per thread; returns the prefix and

@@ -294,7 +294,8 @@ index_block_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *
                                 if (sc_row) sc_row[i] = -INFINITY;
                             }
                         } else if (cnt >= k_eff && cnt <= (uint32_t)kBCap) {
-                            fall = warp_select_write(cand + qq * kBCap, (int)cnt, Q.n, top_k,
+                            const uint64_t *qc = cand + qq * kBCap;
+                            fall = warp_select_write<8>([&](int i) { return __ldcg(qc + i); }, (int)cnt, Q.n, top_k,
                                                      sm + C::off_buf + qq * C::warp_scratch, s_wdig[qq], idx_row,
                                                      sc_row) ? 0 : 1;   // 1: ties at the k-th key
                         } else {
@@ -353,7 +354,7 @@ index_block_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *
                     }
                     __syncthreads();
                     auto src = [&](int i, uint32_t &key, int32_t &ent) -> bool {
-                        const int e = tid * kBFallKeys + i;
+                        const int e = i * kBT + tid;   // a warp's loads are consecutive words
                         ent = e;
                         if (e >= n) return false;
                         key = __ldcg(fkeys + e);

@@ -26,27 +26,33 @@ struct BlockQ {           // per-query record of the current block
     int ok;               // layout consistent
 };
 
-// The k-th largest of a warp's keys (k >= 1; at least k keys exist): four
-// 8-bit radix levels over the keys that `get(i, key)` hands out for
-// i < count (lane-strided), with a warp-private 256-bin histogram `hist` and
-// two words `dig` of shared memory.  Stops at the first level whose bin is
-// taken whole.  Returns the prefix found (its lower bits zero when it stopped
-// early) in *kstar and the number of keys equal to it still to take in
-// *need_eq (0xffffffff when every key at or above *kstar is taken).  Every
-// lane of the warp calls it.
-template <typename Get>
+// The k-th largest of a warp's keys (k >= 1; at least k keys exist): 8-bit
+// radix levels over the keys that `get(i, key)` hands out for i < count
+// (lane-strided, U loads in flight per lane), with a warp-private 256-bin
+// histogram `hist` and two words `dig` of shared memory.  Every key lies in
+// [lo, hi], so the bits above the highest bit where lo and hi differ are
+// common to all of them and the levels start at the byte holding that bit.
+// Stops at the first level whose bin is taken whole.  Returns the prefix
+// found (its lower bits zero when it stopped early) in *kstar and the number
+// of keys equal to it still to take in *need_eq (0xffffffff when every key at
+// or above *kstar is taken).  Every lane of the warp calls it.
+template <int U = 8, typename Get>
 __device__ __forceinline__ void warp_radix_select(Get get, int count, uint32_t k, uint32_t *hist, uint32_t *dig,
-                                                  uint32_t *kstar, uint32_t *need_eq)
+                                                  uint32_t *kstar, uint32_t *need_eq, uint32_t lo = 0u,
+                                                  uint32_t hi = 0xffffffffu)
 {
     const int lane = threadIdx.x & 31;
-    uint32_t prefix = 0, pmask = 0, remaining = k;
+    const uint32_t diff = lo ^ hi;
+    const int top = diff ? 31 - __clz(diff) : 0;          // highest bit that can differ
+    const int sh0 = 8 * (top / 8);
+    const uint32_t low = sh0 >= 24 ? 0xffffffffu : (1u << (sh0 + 8)) - 1u;   // the bits the levels resolve
+    uint32_t prefix = lo & ~low, pmask = ~low, remaining = k;
     bool whole = false;
 #pragma unroll 1
-    for (int sh = 24; sh >= 0 && !whole; sh -= 8) {
+    for (int sh = sh0; sh >= 0 && !whole; sh -= 8) {
 #pragma unroll
         for (int i = 0; i < 8; i++) hist[lane * 8 + i] = 0;
         __syncwarp();
-        constexpr int U = 8;
 #pragma unroll 1
         for (int base = 0; base < count; base += 32 * U) {
             uint32_t kk[U];
@@ -77,13 +83,17 @@ __device__ __forceinline__ void warp_radix_select(Get get, int count, uint32_t k
 }
 
 // One query's top-k by one warp, from its `cnt` candidates (key << 32 | entry,
-// every entry at or above the query's threshold) in global memory: the exact
-// k-th key, then a bitmap of the taken entries, its word prefixes, and the
-// selection written in index order.  Returns false, writing nothing, when keys
-// equal to the k-th key would have to be split (the block-wide selection
-// resolves that case).
-__device__ __forceinline__ bool warp_select_write(const uint64_t *__restrict__ cand, int cnt, int n, int top_k,
-                                                  uint8_t *scratch, uint32_t *dig, int32_t *idx_row, float *sc_row)
+// every key in [lo, hi]; `cand(i)` loads candidate i from global memory): the exact k-th key, then a bitmap
+// of the taken entries, and the selection written in index order.  Without
+// scores the entries are emitted from the bitmap itself; with scores a second
+// pass over the candidates places each (entry, score) by the bitmap's word
+// prefixes.  Returns false, writing nothing, when keys equal to the k-th key
+// would have to be split (the block-wide selection resolves that case).
+// U candidates are in flight per lane.
+template <int U = 16, typename Cand>
+__device__ __forceinline__ bool warp_select_write(Cand cand, int cnt, int n, int top_k,
+                                                  uint8_t *scratch, uint32_t *dig, int32_t *idx_row, float *sc_row,
+                                                  uint32_t lo = 0u, uint32_t hi = 0xffffffffu)
 {
     const int lane = threadIdx.x & 31;
     uint32_t *hist = reinterpret_cast<uint32_t *>(scratch);
@@ -91,20 +101,19 @@ __device__ __forceinline__ bool warp_select_write(const uint64_t *__restrict__ c
     uint16_t *pre = reinterpret_cast<uint16_t *>(taken + kBWords);
     const uint32_t k_eff = (uint32_t)(n < top_k ? n : top_k);
     uint32_t kstar, need_eq;
-    warp_radix_select([&](int i, uint32_t &key) { key = (uint32_t)(__ldcg(cand + i) >> 32); }, cnt, k_eff, hist, dig,
-                      &kstar, &need_eq);
+    warp_radix_select<U>([&](int i, uint32_t &key) { key = (uint32_t)(cand(i) >> 32); }, cnt, k_eff, hist,
+                         dig, &kstar, &need_eq, lo, hi);
     if (need_eq != 0xffffffffu) return false;   // ties at the k-th key: the block-wide path
     const int words = (n + 31) >> 5;
     for (int w = lane; w < words; w += 32) taken[w] = 0;
     __syncwarp();
-    constexpr int U = 8;
 #pragma unroll 1
     for (int base = 0; base < cnt; base += 32 * U) {
         uint64_t v[U];
 #pragma unroll
         for (int u = 0; u < U; u++) {
             const int i = base + 32 * u + lane;
-            v[u] = i < cnt ? __ldcg(cand + i) : 0ull;
+            v[u] = i < cnt ? cand(i) : 0ull;
         }
 #pragma unroll
         for (int u = 0; u < U; u++) {
@@ -114,40 +123,65 @@ __device__ __forceinline__ bool warp_select_write(const uint64_t *__restrict__ c
         }
     }
     __syncwarp();
-    // word prefixes: lane takes a contiguous run of words
-    const int wpl = (words + 31) / 32;
-    const int w0 = lane * wpl, w1 = w0 + wpl < words ? w0 + wpl : words;
-    uint32_t mine = 0;
-    for (int w = w0; w < w1; w++) mine += (uint32_t)__popc(taken[w]);
-    uint32_t incl = mine;
+    if (!sc_row) {
+        // 32 words at a time: a scan of their counts gives each lane the place
+        // of its word's first entry, and the lane writes the word's entries
+        uint32_t at = 0;
+        for (int w0 = 0; w0 < words; w0 += 32) {
+            const int w = w0 + lane;
+            uint32_t bits = w < words ? taken[w] : 0u;
+            const uint32_t c = (uint32_t)__popc(bits);
+            uint32_t incl = c;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-    }
-    uint32_t run = incl - mine;
-    for (int w = w0; w < w1; w++) {
-        pre[w] = (uint16_t)run;
-        run += (uint32_t)__popc(taken[w]);
-    }
-    __syncwarp();
-#pragma unroll 1
-    for (int base = 0; base < cnt; base += 32 * U) {
-        uint64_t v[U];
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-            const int i = base + 32 * u + lane;
-            v[u] = i < cnt ? __ldcg(cand + i) : 0ull;
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            uint32_t pos = at + incl - c;
+            while (bits) {
+                const int j = __ffs(bits) - 1;
+                bits &= bits - 1u;
+                if (pos < (uint32_t)top_k) idx_row[pos] = (int32_t)((w << 5) + j);
+                pos++;
+            }
+            at += __shfl_sync(0xffffffffu, incl, 31);
         }
+    } else {
+        // word prefixes: lane takes a contiguous run of words
+        const int wpl = (words + 31) / 32;
+        const int w0 = lane * wpl, w1 = w0 + wpl < words ? w0 + wpl : words;
+        uint32_t mine = 0;
+        for (int w = w0; w < w1; w++) mine += (uint32_t)__popc(taken[w]);
+        uint32_t incl = mine;
 #pragma unroll
-        for (int u = 0; u < U; u++) {
-            const int i = base + 32 * u + lane;
-            const uint32_t key = (uint32_t)(v[u] >> 32), e = (uint32_t)v[u];
-            if (i < cnt && key >= kstar) {
-                const uint32_t pos = pre[e >> 5] + (uint32_t)__popc(taken[e >> 5] & ((1u << (e & 31)) - 1u));
-                if (pos < (uint32_t)top_k) {
-                    idx_row[pos] = (int32_t)e;
-                    if (sc_row) sc_row[pos] = key_score(key);
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        uint32_t run = incl - mine;
+        for (int w = w0; w < w1; w++) {
+            pre[w] = (uint16_t)run;
+            run += (uint32_t)__popc(taken[w]);
+        }
+        __syncwarp();
+#pragma unroll 1
+        for (int base = 0; base < cnt; base += 32 * U) {
+            uint64_t v[U];
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int i = base + 32 * u + lane;
+                v[u] = i < cnt ? cand(i) : 0ull;
+            }
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int i = base + 32 * u + lane;
+                const uint32_t key = (uint32_t)(v[u] >> 32), e = (uint32_t)v[u];
+                if (i < cnt && key >= kstar) {
+                    const uint32_t pos = pre[e >> 5] + (uint32_t)__popc(taken[e >> 5] & ((1u << (e & 31)) - 1u));
+                    if (pos < (uint32_t)top_k) {
+                        idx_row[pos] = (int32_t)e;
+                        sc_row[pos] = key_score(key);
+                    }
                 }
             }
         }

@@ -37,8 +37,15 @@
  *   - The library allocates no device memory.  Scratch space is the caller's
  *     workspace (ws, ws_bytes), sized by the *_workspace_size calls.  It must
  *     be zero-filled once before its first use (csa_workspace_init does
- *     that); every call that returns CSA_OK leaves it zero-filled again.
- *     After a call that failed, zero it again before reuse.
+ *     that).  It holds counters and histograms, which every call that
+ *     returns CSA_OK leaves at zero again (or which the call resets itself),
+ *     and scratch (candidate lists, partial outputs), which calls overwrite
+ *     and leave as they are.  Scratch of an indexer call with 1024 or more
+ *     queries lies where a call with fewer keeps its histograms: after such
+ *     a call (lightning_index_topk, or hybrid_attend), zero the workspace
+ *     again before a call with fewer queries uses it, and zero it again
+ *     after any call that failed.  Calls on the same side of that divide
+ *     (every decode step of a serving loop, say) reuse it as it is.
  *   - Every call is asynchronous on the given stream and does not
  *     synchronise.  Calls that share one workspace must not overlap in time.
  *   - Every call returns a csa_status_t.  Argument errors are detected on the

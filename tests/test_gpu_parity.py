@@ -205,6 +205,28 @@ def test_index_topk_all_ties_lowest_index_wins(queries, dI):
         assert list(idx[qi]) == want
 
 
+def test_index_topk_prefill_fallback_then_next_sequence():
+    # the 128-query block at 16384 holds the last 16 queries of a sequence whose
+    # keys all tie (rows of 4097-4100 entries overflow the candidate buffer, so
+    # the exact fallback runs and reuses the query tiles' space) and then the first
+    # 112 queries of a sequence with ordinary keys, scored after the fallback
+    lengths = [16400, 2000]
+    k = 8
+    p = problem(lengths, lengths, HI=2, dI=64, k=k, seed=16)
+    n0 = lengths[0] // 4
+    p["kI"][:n0] = 1.0
+    g = P.GpuProblem(p)
+    idx, score = csa.lightning_index_topk(g.layout, g.qI, g.kI, k)
+    torch.cuda.synchronize()
+    idx, score = idx.cpu().numpy(), score.cpu().numpy()
+    for qi in range(16300, lengths[0]):
+        n = (qi + 1) // 4
+        assert list(idx[qi]) == list(range(min(k, n))) + [-1] * (k - min(k, n)), qi
+    rows = np.arange(lengths[0], lengths[0] + 400)
+    kinds = _check_index_rows(p, idx, score, rows)
+    assert kinds["equal"] >= len(rows) - 2, kinds
+
+
 # ---------------------------------------------------------------------------
 # f2: FP8 indexer keys
 # ---------------------------------------------------------------------------
