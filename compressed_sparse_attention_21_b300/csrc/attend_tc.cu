@@ -656,10 +656,573 @@ attend_tc_merge_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64
     if (lse && c == 0) lse[qi * H + head] = (M + log2f(Ls)) * kTcLn2;
 }
 
+// ---------------------------------------------------------------------------
+// Persistent form, for calls with one split per query (prefill-sized): one
+// CTA per SM walks work items (64 heads of one query), taken longest first
+// from a counter in the workspace, so that an item's query tile, selection
+// and first key tiles load while the previous item's last tiles and
+// epilogue run.  The roles and products are those of attend_tc_kernel; key
+// tiles are numbered across items, so the stage, S and P barriers keep their
+// phases.  The TMA warp takes each item and publishes its record in a ring of
+// four slots; the gather warps, the MMA issuer and the softmax warps each
+// release a slot once they have read it.  Per item: the query tile is
+// reloaded once every S^T of the previous item has completed (QFREE), the
+// item's first P V overwrites O^T once the previous epilogue has read it
+// (OFREE), and the selection indices alternate between two buffers
+// (IDXFULL / IDXFREE).  The epilogue stores O / l from registers (two
+// neighbouring d of one head per thread), leaving the key stages to the next
+// item, and the last CTA to finish returns the counters to zero.
+constexpr int kTcpIdxCap = 1024;   // selection indices per buffer
+constexpr int kTcpRing = 4;
+constexpr uint32_t OFF_BARP = OFF_P + 2 * kReg;
+constexpr int PB_KFULL = 0, PB_KFREE = 2, PB_SFULL = 4, PB_SFREE = 6, PB_PFULL = 8, PB_OFULL = 10, PB_QFULL = 11,
+              PB_QFREE = 12, PB_OFREE = 13, PB_IDXFULL = 14, PB_IDXFREE = 16, PB_IFULL = 18, PB_IFREE = 22,
+              PB_FIN = 26, PB_COUNT = 27;
+constexpr uint32_t OFF_MISCP = OFF_BARP + 32 * 8;
+static_assert(PB_COUNT <= 32, "persistent barriers fit their area");
+
+struct alignas(16) TcItem {
+    int64_t qi;          // query
+    int64_t n_vis;       // visible entries
+    int64_t e0;          // first entry row of the query's sequence
+    int64_t tail_row0;   // first raw row of the query's open block
+    int hg;              // 64-head group
+    int T;               // key tiles; 0: skip the item (layout error), -1: no more items
+    int T_main;          // tiles of selected (or visible) entries
+    int n_main;          // selected (or visible) entries
+    int r_tail;          // raw tail rows
+};
+constexpr uint32_t OFF_RING = OFF_MISCP + MISC_END;
+constexpr uint32_t OFF_IDXP = (OFF_RING + kTcpRing * (uint32_t)sizeof(TcItem) + 15u) & ~15u;
+constexpr uint32_t kTcpSmem = OFF_IDXP + 2 * kTcpIdxCap * 4 + 1024;   // + alignment slack
+static_assert(kTcpSmem <= 232448, "shared memory per CTA");
+constexpr size_t kTcpHeader = 256;   // workspace: next item, CTAs done
+
+template <bool GATHER>
+__global__ void __launch_bounds__(kTcThreads, 1)
+attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_ent_rows,
+                  const __grid_constant__ CUtensorMap map_kv, int batch, const int64_t *__restrict__ cu_kv,
+                  const int64_t *__restrict__ cu_q, const int64_t *__restrict__ cu_ent,
+                  const uint16_t *__restrict__ entries, const int32_t *__restrict__ idx, int H, int ratio, int top_k,
+                  float scale_log2, int max_kv_len, int64_t n_items, unsigned *__restrict__ counters,
+                  uint16_t *__restrict__ out, float *__restrict__ lse, int *err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;          // swizzled tiles need 1024-byte alignment
+    uint8_t *sm = smem_raw + (sb - raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int HG = H / kTcHeads;
+    auto bar = [&](int i) { return sb + OFF_BARP + 8u * (uint32_t)i; };
+    uint8_t *misc = sm + OFF_MISCP;
+    float *s_m = reinterpret_cast<float *>(misc + MISC_M);
+    float *s_l = reinterpret_cast<float *>(misc + MISC_L);
+    float *s_al = reinterpret_cast<float *>(misc + MISC_AL);
+    float *s_rmax = reinterpret_cast<float *>(misc + MISC_RMAX);   // [4 warps][64 heads]
+    float *s_rsum = reinterpret_cast<float *>(misc + MISC_RSUM);
+    volatile int *s_flag = reinterpret_cast<volatile int *>(misc + MISC_FLAG);
+    TcItem *ring = reinterpret_cast<TcItem *>(sm + OFF_RING);
+    int32_t *s_idx0 = reinterpret_cast<int32_t *>(sm + OFF_IDXP);
+
+    if (tid == 0) {
+        mbar_init(bar(PB_QFULL), 1);
+        mbar_init(bar(PB_QFREE), 1);
+        for (int s = 0; s < 2; s++) {
+            mbar_init(bar(PB_KFULL + s), 1 + kGatherThreads);   // TMA issuer + cp.async gatherers
+            mbar_init(bar(PB_KFREE + s), 1);
+            mbar_init(bar(PB_SFULL + s), 1);
+            mbar_init(bar(PB_SFREE + s), 128);
+            mbar_init(bar(PB_PFULL + s), 128);
+            mbar_init(bar(PB_IDXFULL + s), kGatherThreads);
+            mbar_init(bar(PB_IDXFREE + s), 128);
+        }
+        mbar_init(bar(PB_OFULL), 1);
+        mbar_init(bar(PB_OFREE), 128);
+        for (int k = 0; k < kTcpRing; k++) {
+            mbar_init(bar(PB_IFULL + k), 1);
+            mbar_init(bar(PB_IFREE + k), 3);   // gather warps, MMA issuer, softmax warps
+        }
+        mbar_init(bar(PB_FIN), 1);
+        fence_mbar_init();
+    }
+    if (warp == 4) tc::tmem_alloc(sb + OFF_MISCP + MISC_TMEM, kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + MISC_TMEM);
+    // the selection and the entries come from earlier kernels
+    griddep_wait();
+    // record k of the ring, once published (every calling thread waits)
+    auto item_at = [&](uint32_t k, TcItem &it) -> bool {
+        if (!mbar_wait(bar(PB_IFULL + (int)(k % kTcpRing)), (k / kTcpRing) & 1u)) return false;
+        it = ring[k % kTcpRing];
+        return true;
+    };
+
+    if (warp == 5) {
+        // ------------------------------------------------------------ items, query tiles, TMA loads
+        bool ok = true;
+        uint32_t g = 0, ri = 0;   // key tiles and items with tiles so far
+        const uint64_t keep = policy_evict_last(), once = policy_evict_first();
+        for (uint32_t k = 0;; k++) {
+            const int slot = (int)(k % kTcpRing);
+            int okw = 1;
+            if (lane == 0 && k >= kTcpRing && !mbar_wait(bar(PB_IFREE + slot), ((k - kTcpRing) / kTcpRing) & 1u)) okw = 0;
+            if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                ok = false;
+                break;
+            }
+            // the next item, longest rows first
+            unsigned j = 0;
+            if (lane == 0) j = atomicAdd(counters, 1u);
+            j = __shfl_sync(0xffffffffu, j, 0);
+            TcItem it;
+            it.T = -1;
+            if ((int64_t)j < n_items) {
+                const int64_t jj = n_items - 1 - (int64_t)j;
+                it.qi = jj / HG;
+                it.hg = (int)(jj % HG);
+                const QueryPos p = query_pos(cu_kv, cu_q, cu_ent, batch, it.qi);
+                const bool bad = p.t < 0 || p.t >= p.L || p.L > max_kv_len || p.ne != p.L / ratio;
+                it.n_vis = (p.t + 1) / ratio;
+                it.r_tail = (int)((p.t + 1) % ratio);
+                it.e0 = p.e0;
+                it.tail_row0 = p.kv0 + p.t - it.r_tail + 1;
+                it.n_main = GATHER ? (int)(it.n_vis < top_k ? it.n_vis : top_k) : (int)it.n_vis;
+                it.T = bad ? 0 : tc_tiles<GATHER>(p, ratio, top_k, &it.T_main);
+                if (bad && lane == 0) set_error(err, CSA_ERR_DEVICE);
+            }
+            if (lane == 0) {
+                ring[slot] = it;
+                mbar_arrive(bar(PB_IFULL + slot));
+            }
+            __syncwarp();
+            if (it.T < 0) break;
+            if (it.T == 0) continue;
+            if (lane == 0) {
+                // the query tile: every S^T of the previous item is done with it
+                if (ri > 0 && !mbar_wait(bar(PB_QFREE), (ri - 1) & 1u)) okw = 0;
+                if (okw) {
+                    mbar_expect_tx(bar(PB_QFULL), kStage);
+                    const int qrow = (int)(it.qi * H + (int64_t)it.hg * kTcHeads);
+#pragma unroll
+                    for (int r = 0; r < kRegions; r++)
+                        tma_tile2d(sb + OFF_Q + r * kReg, &map_q, r * 64, qrow, bar(PB_QFULL), once);
+                }
+                // tile g of the CTA goes to stage g & 1 once P V of tile g - 2 has released it;
+                // selected entries are gathered by warps 6-11, this thread only arrives for them
+                for (int tt = 0; okw && tt < it.T; tt++) {
+                    const int s = (int)(g & 1u);
+                    if (g >= 2 && !mbar_wait(bar(PB_KFREE + s), ((g - 2) >> 1) & 1u)) {
+                        okw = 0;
+                        break;
+                    }
+                    const uint32_t stage = sb + OFF_K + s * kStage;
+                    const uint32_t fb = bar(PB_KFULL + s);
+                    mbar_expect_tx(fb, (GATHER && tt < it.T_main) ? 0u : kStage);
+                    if (tt < it.T_main) {
+                        if (!GATHER) {
+                            const int row = (int)(it.e0 + (int64_t)tt * kTcKeys);
+#pragma unroll
+                            for (int r = 0; r < kRegions; r++)
+                                tma_tile2d(stage + r * kReg, &map_ent_rows, r * 64, row, fb, keep);
+                        }
+                    } else {
+                        const int row = (int)(it.tail_row0 + (int64_t)(tt - it.T_main) * kTcKeys);
+#pragma unroll
+                        for (int r = 0; r < kRegions; r++) tma_tile2d(stage + r * kReg, &map_kv, r * 64, row, fb, once);
+                    }
+                    g++;
+                }
+            }
+            g = __shfl_sync(0xffffffffu, g, 0);
+            ri++;
+            if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                ok = false;
+                break;
+            }
+        }
+        if (lane == 0) {
+            if (!ok) set_error(err, CSA_ERR_TIMEOUT);
+            // no load may still be landing when the CTA ends: the last phase of
+            // each stage and of the query tile
+            for (int64_t u = (int64_t)g - 1; u >= 0 && u >= (int64_t)g - 2; u--)
+                if (!mbar_wait(bar(PB_KFULL + (int)(u & 1)), (uint32_t)((u >> 1) & 1))) set_error(err, CSA_ERR_TIMEOUT);
+            if (ri > 0 && !mbar_wait(bar(PB_QFULL), (ri - 1) & 1u)) set_error(err, CSA_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------ selection indices, cp.async gathers
+        // Thread pt copies 16-byte chunk pt % 8 of rows pt / 8, + 24, ... in
+        // every region of selected-entry tiles; every thread arrives on each
+        // tile's KFULL (after its own copies landed), whatever the tile.
+        const int pt = tid - kGatherBase;
+        const int pc = pt & 7, pk0 = pt >> 3;
+        constexpr int RSTEP = kGatherThreads / 8;                 // 24 rows per pass
+        constexpr int KPP = (kTcKeys + RSTEP - 1) / RSTEP;        // 3 rows per thread
+        const uint64_t keep = policy_evict_last();
+        bool fail = false;
+        uint32_t g = 0, ri = 0;
+        for (uint32_t k = 0;; k++) {
+            TcItem it;
+            if (!item_at(k, it)) fail = true;
+            if (tc::named_bar_or(2, kGatherThreads, fail)) break;   // every gatherer leaves together
+            if (pt == 0) mbar_arrive(bar(PB_IFREE + (int)(k % kTcpRing)));   // all have read the record
+            if (it.T < 0) break;
+            if (it.T == 0) continue;
+            const int buf = (int)(ri & 1u);
+            int32_t *s_idx = s_idx0 + buf * kTcpIdxCap;
+            if (GATHER) {
+                // this buffer was last read by the softmax of item ri - 2
+                if (ri >= 2 && !mbar_wait(bar(PB_IDXFREE + buf), ((ri - 2) >> 1) & 1u)) fail = true;
+                if (tc::named_bar_or(2, kGatherThreads, fail)) break;
+                for (int i = pt; i < it.n_main; i += kGatherThreads) s_idx[i] = __ldg(idx + it.qi * top_k + i);
+                tc::named_bar(2, kGatherThreads);
+                mbar_arrive(bar(PB_IDXFULL + buf));
+            }
+            for (int tt = 0; tt < it.T && !fail; tt++, g++) {
+                const int s = (int)(g & 1u);
+                if (g >= 2 && !mbar_wait(bar(PB_KFREE + s), ((g - 2) >> 1) & 1u)) {
+                    fail = true;
+                    break;
+                }
+                if (GATHER && tt < it.T_main) {
+                    const uint32_t stage = sb + OFF_K + s * kStage;
+#pragma unroll
+                    for (int i = 0; i < KPP; i++) {
+                        const int kr = pk0 + RSTEP * i;
+                        if (kr < kTcKeys) {
+                            const int slot = tt * kTcKeys + kr;
+                            const int e = slot < it.n_main ? s_idx[slot] : -1;
+                            const bool v = e >= 0 && (int64_t)e < it.n_vis;
+                            const uint16_t *src = entries + (it.e0 + (v ? e : 0)) * kTcD;
+#pragma unroll
+                            for (int r = 0; r < kRegions; r++)
+                                cp_async_16_hint(stage + r * kReg + kr * 128 + ((pc ^ (kr & 7)) << 4), src + r * 64 + pc * 8,
+                                                 v ? 16 : 0, keep);
+                        }
+                    }
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    tc::fence_proxy_async();
+                }
+                mbar_arrive(bar(PB_KFULL + s));
+            }
+            ri++;
+        }
+        cp_async_wait<0>();
+        if (fail && pt == 0) set_error(err, CSA_ERR_TIMEOUT);
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        // S(t) and PV(t) are each issued in tile order (numbered across items);
+        // the issuer polls both and issues whichever is ready first.  The first
+        // S of an item waits for its query tile, the first PV for the previous
+        // epilogue; the last S of an item frees the query tile, the last PV
+        // completes the item's O^T.
+        if (lane == 0) {
+            constexpr uint32_t id_qk = tc::idesc_bf16_f32(64, kTcHeads, false, false);
+            constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, kTcHeads, true, true);
+            const uint64_t qa0 = tc::sdesc_sw128(sb + OFF_K, 16, 1024);
+            const uint64_t qb0 = tc::sdesc_sw128(sb + OFF_Q, 16, 1024);
+            const uint64_t pa0 = tc::sdesc_sw128(sb + OFF_K, kReg, 1024);
+            const uint64_t pb0 = tc::sdesc_sw128(sb + OFF_P, kReg, 1024);
+            bool ok = true;
+            uint32_t kS = 0, kP = 0;        // next ring record of each side
+            uint32_t riS = 0, riP = 0;      // items with tiles begun by each side
+            uint32_t nq = 0, np = 0;        // next S tile, next PV tile
+            uint32_t startS = 0, endS = 0, startP = 0, endP = 0;   // tiles of the current item of each side
+            bool hS = false, hP = false, doneS = false, doneP = false;
+            uint64_t idle0 = global_ns();
+            while (ok) {
+                bool did = false;
+                while (!hS && !doneS && mbar_test(bar(PB_IFULL + (int)(kS % kTcpRing)), (kS / kTcpRing) & 1u)) {
+                    const int T = ring[kS % kTcpRing].T;
+                    kS++;
+                    if (T < 0) doneS = true;
+                    else if (T > 0) {
+                        hS = true;
+                        startS = nq;
+                        endS = nq + (uint32_t)T;
+                    }
+                }
+                while (!hP && !doneP && mbar_test(bar(PB_IFULL + (int)(kP % kTcpRing)), (kP / kTcpRing) & 1u)) {
+                    const int T = ring[kP % kTcpRing].T;
+                    mbar_arrive(bar(PB_IFREE + (int)(kP % kTcpRing)));   // this side reads the record last
+                    kP++;
+                    if (T < 0) doneP = true;
+                    else if (T > 0) {
+                        hP = true;
+                        startP = np;
+                        endP = np + (uint32_t)T;
+                    }
+                }
+                if (doneS && doneP) break;   // every product issued
+                if (hS && nq <= np + 1) {
+                    const int sidx = (int)(nq & 1u);
+                    bool ready = (nq < 2 || mbar_test(bar(PB_SFREE + sidx), ((nq - 2) >> 1) & 1u)) &&
+                                 mbar_test(bar(PB_KFULL + sidx), (nq >> 1) & 1u);
+                    if (ready && nq == startS) ready = mbar_test(bar(PB_QFULL), riS & 1u);   // the item's query tile
+                    if (ready) {
+                        tc::fence_after_sync();
+                        // descriptors advance by adding (byte offset >> 4) to the address field
+                        const uint64_t a0 = qa0 + (uint64_t)((sidx * kStage) >> 4);
+                        const uint32_t dS = tmem + TM_S + 64 * sidx;
+#pragma unroll
+                        for (int j = 0; j < kTcD / 16; j++) {
+                            const uint64_t off = (uint64_t)(((j >> 2) * kReg + (j & 3) * 32) >> 4);
+                            tc::mma_ss(dS, a0 + off, qb0 + off, id_qk, j != 0);
+                        }
+                        tc::mma_commit(bar(PB_SFULL + sidx));
+                        nq++;
+                        if (nq == endS) {   // the item's last S^T: the query tile is free once it completes
+                            tc::mma_commit(bar(PB_QFREE));
+                            riS++;
+                            hS = false;
+                        }
+                        did = true;
+                    }
+                }
+                if (hP && np < nq) {
+                    const int sidx = (int)(np & 1u);
+                    const bool first = np == startP;
+                    bool ready = mbar_test(bar(PB_PFULL + sidx), (np >> 1) & 1u);
+                    if (ready && first && riP > 0) ready = mbar_test(bar(PB_OFREE), (riP - 1) & 1u);
+                    if (ready) {
+                        tc::fence_after_sync();
+                        const uint64_t a0 = pa0 + (uint64_t)((sidx * kStage) >> 4);
+                        const uint64_t b0 = pb0 + (uint64_t)((sidx * kReg) >> 4);
+#pragma unroll
+                        for (int m = 0; m < 4; m++)
+#pragma unroll
+                            for (int k4 = 0; k4 < kTcKeys / 16; k4++)
+                                tc::mma_ss(tmem + TM_O + 64 * m, a0 + (uint64_t)((2 * m * kReg + k4 * 2048) >> 4),
+                                           b0 + (uint64_t)((k4 * 2048) >> 4), id_pv, !first || k4 > 0);
+                        tc::mma_commit(bar(PB_KFREE + sidx));
+                        np++;
+                        if (np == endP) {   // the item's last P V: its O^T is complete once it completes
+                            tc::mma_commit(bar(PB_OFULL));
+                            riP++;
+                            hP = false;
+                        }
+                        did = true;
+                    }
+                }
+                if (did) {
+                    idle0 = global_ns();
+                } else if (global_ns() - idle0 > kWaitLimitNs) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) set_error(err, CSA_ERR_TIMEOUT);
+            // every issued product completes before the CTA ends
+            tc::mma_commit(bar(PB_FIN));
+            if (!mbar_wait(bar(PB_FIN), 0)) set_error(err, CSA_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax (128 threads)
+        // As in attend_tc_kernel, per item: thread (w, l) takes key 16 w + l % 16
+        // of each tile for heads 32 hh .. 32 hh + 31, keeps the running maxima in
+        // registers and its partial sums, reduced once after the item's last tile.
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const int hh = lane >> 4;                 // head half: heads 32 hh .. 32 hh + 31
+        const int key = 16 * warp + (lane & 15);  // key of the tile this thread takes
+        bool fail = false;   // a wait of this thread gave up (acted on at the next barrier reduction)
+        uint32_t g = 0, ri = 0;
+        for (uint32_t k = 0;; k++) {
+            TcItem it;
+            if (!item_at(k, it)) fail = true;
+            if (tc::named_bar_or(1, 128, fail)) break;   // every softmax thread leaves together
+            if (tid == 0) mbar_arrive(bar(PB_IFREE + (int)(k % kTcpRing)));   // all have read the record
+            if (it.T < 0) break;
+            if (it.T == 0) continue;
+            const int buf = (int)(ri & 1u);
+            const int32_t *s_idx = s_idx0 + buf * kTcpIdxCap;
+            if (GATHER && !mbar_wait(bar(PB_IDXFULL + buf), (ri >> 1) & 1u)) fail = true;
+            float m_run[32], l_part[32];
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                m_run[j] = -INFINITY;
+                l_part[j] = 0.f;
+            }
+            if (tid < kTcHeads) s_m[tid] = -INFINITY;   // read by the others after a barrier
+            for (int t = 0; t < it.T; t++, g++) {
+                const int sidx = (int)(g & 1u);
+                if (!mbar_wait(bar(PB_SFULL + sidx), (g >> 1) & 1u)) fail = true;
+                tc::fence_after_sync();
+                float v[64];
+                tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sidx, v);
+                tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sidx + 32, v + 32);
+                tc::tmem_wait_ld();
+                tc::fence_before_sync();
+                mbar_arrive(bar(PB_SFREE + sidx));
+                // lanes 0-15 hold the tile's rows: hand heads 32-63 to lanes 16-31
+                float sc[32];
+#pragma unroll
+                for (int j = 0; j < 32; j++) {
+                    const float other = __shfl_xor_sync(0xffffffffu, v[32 + j], 16);
+                    sc[j] = hh ? other : v[j];
+                }
+                bool valid;
+                if (t < it.T_main) {
+                    const int slot = t * kTcKeys + key;
+                    valid = slot < it.n_main;
+                    if (GATHER && valid) {
+                        const int e = s_idx[slot];
+                        valid = e >= 0 && (int64_t)e < it.n_vis;
+                        if (e >= 0 && !valid) set_error(err, CSA_ERR_DEVICE);   // an index that is not visible
+                    }
+                } else {
+                    valid = (t - it.T_main) * kTcKeys + key < it.r_tail;
+                }
+                bool exceed = false;
+#pragma unroll
+                for (int j = 0; j < 32; j++) {
+                    sc[j] = valid ? sc[j] * scale_log2 : -INFINITY;
+                    exceed |= sc[j] > m_run[j] + kRescaleLog2;   // a finite score always exceeds -inf
+                }
+                bool rescale = false;
+                if (tc::named_bar_or(1, 128, exceed || fail)) {
+                    if (tc::named_bar_or(1, 128, fail)) break;   // a wait gave up: every thread leaves together
+                    float r0, r1;
+                    halfwarp_reduce32<true>(sc, r0, r1);
+                    const int h2 = 32 * hh + 2 * (lane & 15);
+                    s_rmax[warp * 64 + h2] = r0;
+                    s_rmax[warp * 64 + h2 + 1] = r1;
+                    if (tid == 0) s_flag[1] = 0;
+                    tc::named_bar(1, 128);
+                    if (tid < kTcHeads) {
+                        const float M = fmaxf(fmaxf(s_rmax[tid], s_rmax[64 + tid]), fmaxf(s_rmax[128 + tid], s_rmax[192 + tid]));
+                        const float m_old = s_m[tid];
+                        float m_new = m_old, alpha = 1.f;
+                        if (M > m_old + kRescaleLog2 || (m_old == -INFINITY && M != -INFINITY)) {
+                            m_new = M;
+                            alpha = fast_exp2(m_old - m_new);   // 0 when nothing was accumulated yet
+                            if (t > 0) s_flag[1] = 1;
+                        }
+                        s_m[tid] = m_new;
+                        s_al[tid] = alpha;
+                    }
+                    tc::named_bar(1, 128);
+                    rescale = s_flag[1] != 0;
+#pragma unroll
+                    for (int j = 0; j < 32; j++) {
+                        m_run[j] = s_m[32 * hh + j];
+                        l_part[j] *= s_al[32 * hh + j];
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 32; j++) {
+                    sc[j] = (m_run[j] == -INFINITY) ? 0.f : fast_exp2(sc[j] - m_run[j]);
+                    l_part[j] += sc[j];
+                }
+                // This P stage was last read by P V of tile g - 2, which must be done.
+                // A rescale of the O^T columns also needs P V of tile g - 1 (of this item) done.
+                if (rescale ? (t >= 1 && !mbar_wait(bar(PB_KFREE + (int)((g - 1) & 1u)), ((g - 1) >> 1) & 1u))
+                            : (g >= 2 && !mbar_wait(bar(PB_KFREE + sidx), ((g - 2) >> 1) & 1u)))
+                    fail = true;
+                {
+                    uint8_t *prow = sm + OFF_P + sidx * kReg + key * 128;
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        const int ch = 4 * hh + c;
+                        uint4 w;
+                        w.x = pack_bf16x2(sc[8 * c + 0], sc[8 * c + 1]);
+                        w.y = pack_bf16x2(sc[8 * c + 2], sc[8 * c + 3]);
+                        w.z = pack_bf16x2(sc[8 * c + 4], sc[8 * c + 5]);
+                        w.w = pack_bf16x2(sc[8 * c + 6], sc[8 * c + 7]);
+                        *reinterpret_cast<uint4 *>(prow + ((ch ^ (key & 7)) << 4)) = w;
+                    }
+                }
+                if (rescale) {
+                    tc::fence_after_sync();
+#pragma unroll 1
+                    for (int c = 0; c < 8; c++) {
+                        float o[32];
+                        const uint32_t ta = tmem + lane_base + TM_O + 32 * c;
+                        tc::tmem_ld32(ta, o);
+                        tc::tmem_wait_ld();
+                        const float *al = s_al + 32 * (c & 1);
+#pragma unroll
+                        for (int j = 0; j < 32; j++) o[j] *= al[j];
+                        tc::tmem_st32(ta, o);
+                    }
+                    tc::tmem_wait_st();
+                }
+                tc::fence_proxy_async();
+                tc::fence_before_sync();
+                mbar_arrive(bar(PB_PFULL + sidx));
+            }
+            if (GATHER) mbar_arrive(bar(PB_IDXFREE + buf));   // this thread reads the indices no more
+            // the weights' sums over keys, once: lanes (keys) within each warp, then the warps
+            if (tc::named_bar_or(1, 128, fail)) break;
+            {
+                float r0, r1;
+                halfwarp_reduce32<false>(l_part, r0, r1);
+                const int h2 = 32 * hh + 2 * (lane & 15);
+                s_rsum[warp * 64 + h2] = r0;
+                s_rsum[warp * 64 + h2 + 1] = r1;
+            }
+            tc::named_bar(1, 128);
+            if (tid < kTcHeads) {
+                const float l = s_rsum[tid] + s_rsum[64 + tid] + s_rsum[128 + tid] + s_rsum[192 + tid];
+                s_l[tid] = l;
+                s_al[tid] = l > 0.f ? 1.f / l : 0.f;
+            }
+            // epilogue: O^T / l -> out[head][d] (bf16), lse
+            if (!mbar_wait(bar(PB_OFULL), ri & 1u)) fail = true;
+            if (tc::named_bar_or(1, 128, fail)) break;   // also: s_l and s_al are complete
+            tc::fence_after_sync();
+            const int64_t row0 = it.qi * H + (int64_t)it.hg * kTcHeads;
+#pragma unroll 1
+            for (int c = 0; c < 8; c++) {
+                float o[32];
+                tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
+                tc::tmem_wait_ld();
+                if (c == 7) {   // O^T is read: the next item's first P V may overwrite it
+                    tc::fence_before_sync();
+                    mbar_arrive(bar(PB_OFREE));
+                }
+                const int d = 128 * (c >> 1) + tid;   // this thread's row of O^T (tensor-memory lane)
+                const int h0 = 32 * (c & 1);
+                // lanes 2i and 2i+1 hold d and d+1: the even lane stores (d, d+1) of
+                // head h0 + j, the odd lane those of head h0 + j + 1
+                const bool odd = lane & 1;
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const float a = o[j] * s_al[h0 + j], b = o[j + 1] * s_al[h0 + j + 1];
+                    const float got = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+                    const uint32_t pk = odd ? pack_bf16x2(got, b) : pack_bf16x2(a, got);
+                    const int h = h0 + j + (odd ? 1 : 0);
+                    *reinterpret_cast<uint32_t *>(out + (row0 + h) * kTcD + (d & ~1)) = pk;
+                }
+            }
+            if (lse && tid < kTcHeads) lse[row0 + tid] = (s_m[tid] + log2f(s_l[tid])) * kTcLn2;
+            ri++;
+        }
+        if (fail && tid == 0) set_error(err, CSA_ERR_TIMEOUT);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    griddep_launch();
+    tc::fence_after_sync();
+    if (warp == 4) tc::tmem_dealloc(tmem, kTmemCols);
+    // the last CTA to finish returns the counters to zero for the next call
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(counters + 1, 1u) == gridDim.x - 1) {
+            counters[0] = 0u;
+            counters[1] = 0u;
+        }
+    }
+}
+
 // Key splits.  With fewer 64-head units than `share` SMs, a unit's tiles are
 // spread over as many CTAs as keep the grid within one wave of `share` CTAs.
 struct TcPlan {
     int nsplit_max;   // splits of a query with at least that many key tiles
+    bool persist;     // one split per query: the persistent kernel, one CTA per SM
 };
 
 TcPlan tc_plan(const AttendArgs &a)
@@ -677,11 +1240,17 @@ TcPlan tc_plan(const AttendArgs &a)
     if (want < 1) want = 1;
     TcPlan pl;
     pl.nsplit_max = (int)want;
+    pl.persist = want == 1 && units >= share && (a.idx == nullptr || a.top_k <= kTcpIdxCap);
     return pl;
 }
 
 size_t tc_ws_bytes(const AttendArgs &a, const TcPlan &pl, float **part_o, float2 **part_ml)
 {
+    if (pl.persist) {   // the item counters
+        if (part_o) *part_o = nullptr;
+        if (part_ml) *part_ml = nullptr;
+        return kTcpHeader;
+    }
     if (pl.nsplit_max <= 1) {
         if (part_o) *part_o = nullptr;
         if (part_ml) *part_ml = nullptr;
@@ -723,6 +1292,20 @@ cudaError_t launch_tc(const AttendArgs &a, cudaStream_t st)
     if (e == cudaSuccess) e = rows_map(&m_ent_rows, ent, ent_rows, 64);
     if (e == cudaSuccess) e = rows_map(&m_kv, a.kv, a.n_kv_rows, 64);
     if (e != cudaSuccess) return e;
+    if (pl.persist) {
+        // the counters start at zero whatever an earlier call left; the last CTA zeroes them again
+        if (!a.ws || a.ws_bytes < kTcpHeader) return cudaErrorInvalidValue;
+        unsigned *counters = static_cast<unsigned *>(a.ws);
+        e = cudaMemsetAsync(counters, 0, 2 * sizeof(unsigned), st);
+        if (e != cudaSuccess) return e;
+        const int64_t n_items = a.total_q * HG;
+        const int sms = a.num_sms > 0 ? a.num_sms : 148;
+        const unsigned pgrid = (unsigned)(n_items < sms ? n_items : sms);
+        return launch_kernel(GATHER ? "sparse_attend" : "dense_attend", attend_tcp_kernel<GATHER>, dim3(pgrid),
+                             dim3(kTcThreads), kTcpSmem, st, a.pdl, m_q, m_ent_rows, m_kv, a.batch, a.cu_kv, a.cu_q,
+                             a.cu_ent, static_cast<const uint16_t *>(ent), a.idx, a.n_heads, a.ratio, a.top_k,
+                             scale_log2, a.max_kv_len, n_items, counters, a.out, a.lse, a.err);
+    }
     e = launch_kernel(GATHER ? "sparse_attend" : "dense_attend", attend_tc_kernel<GATHER>, grid, dim3(kTcThreads),
                       kTcSmem, st, a.pdl, m_q, m_ent_rows, m_kv, a.batch, a.cu_kv, a.cu_q, a.cu_ent,
                       static_cast<const uint16_t *>(ent), a.idx, a.n_heads, a.ratio, a.top_k, scale_log2, a.max_kv_len, pl.nsplit_max, a.out, a.lse,
