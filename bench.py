@@ -38,12 +38,12 @@ EXTRA_WORKLOADS = ("prefill_128k", "ragged_decode", "decode_1m")
 # keyed by (workload, call, indexer key format), with the sha256 of the sources at capture time;
 # a changed source makes the figure stale and it is reported as null.
 NCU_TRAFFIC = {
-    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,599,360 B read +
-    # index_select_kernel 1,352,064 B read, 0 B written (means of two captured calls)
+    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,599,744 B read +
+    # index_select_kernel 1,351,936 B read, 0 B written (means of two captured calls)
     ("decode_64k", "index_topk", "bf16"): {
-        "bytes_per_launch": 34951424,
+        "bytes_per_launch": 34951680,
         "sources": {"indexer.cu": "5bc85f0caf70f1dd126680f4d5e1a7e9b2ef68237de83f15d5a895914e5c1fd2",
-                    "common.cuh": "8f53808619b116427904fbedf2719663a9b508addd86fc0b6cc31ff4bb12667b"},
+                    "common.cuh": "b93a7dad1acde03c5b427f390c736715adf747f244ae8d972599ce95b5ac6ab8"},
     },
 }
 
