@@ -381,6 +381,32 @@ def test_attend_invisible_index_is_reported_and_skipped():
     assert csa.check_device_error() == 0    # reading clears it
 
 
+def test_attend_persistent_invisible_index_is_reported_and_skipped():
+    # a prefill-sized call (d = 512, 64 heads, more queries than SMs) runs the
+    # persistent kernel; one row names an entry its query cannot see: the call
+    # reports it, skips that key, and every other row still matches the oracle
+    lengths = [300, 200]
+    k = 16
+    p = problem(lengths, lengths, H=64, d=512, k=k, seed=23)
+    g = P.GpuProblem(p)
+    inp = wl.to_numpy(p)
+    csa_cache, _ = g.build_caches()
+    orc = oracle.hybrid_queries(inp)
+    idx_np = orc["idx"].copy()
+    bad_row = 299                                    # t = 299 of sequence 0 sees entries 0 .. 74
+    assert idx_np[bad_row, -1] >= 0
+    idx_np[bad_row, -1] = 80                         # not visible
+    idx = torch.from_numpy(idx_np).cuda()
+    oC, _ = csa.sparse_mqa_attend(g.layout, g.q, csa_cache, g.kv, idx, k, p["scale"])
+    torch.cuda.synchronize()
+    assert csa.check_device_error() == 6
+    assert csa.check_device_error() == 0
+    got = P.bf16_to_f64(oC)
+    keep = np.ones(got.shape[0], bool)
+    keep[bad_row] = False
+    P.assert_att(got[keep], orc["oC"][keep], "sparse, rows without the invisible index")
+
+
 # ---------------------------------------------------------------------------
 # a6: the hybrid step
 # ---------------------------------------------------------------------------
