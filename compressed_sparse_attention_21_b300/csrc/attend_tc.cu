@@ -33,10 +33,11 @@
 // running maximum of a head is raised only when a tile exceeds it by more
 // than 2^8 (the accumulated O^T column and sum are then rescaled); the
 // result is exact either way because the sum uses the same maximum.
-// A split of a query that has several writes its unnormalised O (fp32,
-// [head][d], staged in the idle key stages and stored with one bulk copy)
-// and each head's (max, sum); attend_tc_merge_kernel, launched behind it,
-// combines the splits: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// When queries are split (decode-sized calls), every split writes its
+// unnormalised O (fp32, [head][d], staged in the idle key stages and stored
+// with one bulk copy) and each head's (max, sum), an empty (-inf, 0) when it
+// has no tiles; attend_tc_merge_kernel, launched behind it, combines the
+// splits: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 // Every wait is bounded: one that runs out reports CSA_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -168,15 +169,22 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const int64_t n_vis = (p.t + 1) / ratio;
     const int r_tail = (int)((p.t + 1) % ratio);
     const bool bad = p.t < 0 || p.t >= p.L || p.L > max_kv_len || p.ne != p.L / ratio;
+    // with splits, every slot of (max, sum) is written, empty where a split has
+    // no keys, so the merge reads them all without locating the query
+    const int64_t ml_slot = ((qi * HG + hg) * nsplit_max + split) * kTcHeads;
     if (bad) {
         if (tid == 0) set_error(err, CSA_ERR_DEVICE);
+        if (nsplit_max > 1 && tid < kTcHeads) part_ml[ml_slot + tid] = make_float2(-INFINITY, 0.f);
         return;
     }
     const int n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
     int T_main = 0;
     const int T_all = tc_tiles<GATHER>(p, ratio, top_k, &T_main);
     const int nsplit = tc_nsplit(T_all, nsplit_max);
-    if (split >= nsplit) return;   // this query has fewer key tiles than splits
+    if (split >= nsplit) {   // this query has fewer key tiles than splits
+        if (tid < kTcHeads) part_ml[ml_slot + tid] = make_float2(-INFINITY, 0.f);
+        return;
+    }
     const int t0 = (int)((int64_t)split * T_all / nsplit), t1 = (int)((int64_t)(split + 1) * T_all / nsplit);
     const int T = t1 - t0;
     // main-key slots of this split (selection entries read here)
@@ -526,7 +534,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         // epilogue: O^T / l -> out[head][d] (bf16), lse
         bool done = ok && mbar_wait(bar(BAR_OFULL), 0);
         done = !tc::named_bar_or(1, 128, !done);   // also: s_l is complete
-        if (done && nsplit > 1) {
+        if (done && nsplit_max > 1) {   // the merge normalises, also a query's only split
             // partial result: unnormalised O^T -> [head][d] fp32 in the key
             // stages (every product is done with them), one bulk store
             tc::fence_after_sync();
@@ -615,15 +623,15 @@ attend_tc_merge_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64
     const int c = threadIdx.x;
     const int64_t qi = blockIdx.x;
     const int head = blockIdx.y;
-    const QueryPos p = query_pos(cu_kv, cu_q, cu_ent, batch, qi);
-    if (p.t < 0 || p.t >= p.L || p.ne != p.L / ratio) return;   // reported by the attention kernel
-    const int nsplit = tc_nsplit(tc_tiles<GATHER>(p, ratio, top_k, nullptr), nsplit_max);
-    if (nsplit <= 1) return;   // written by the attention kernel itself
+    // every split slot holds a (max, sum): empty (-inf, 0) where the query has
+    // fewer tiles than splits, or a layout error (its row then reads zeros)
+    const int nsplit = nsplit_max;
     griddep_wait();            // the partial results are complete
     const int64_t base = (qi * (H / kTcHeads) + head / kTcHeads) * nsplit_max * kTcHeads + head % kTcHeads;
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; s++) M = fmaxf(M, __ldcg(part_ml + base + (int64_t)s * kTcHeads).x);
-    float Ls = 0.f;
+    // up to kMergeBatch splits' (max, sum) and columns are loaded at once, one
+    // round trip; the maximum over the batches so far is carried, and what was
+    // accumulated is rescaled when it rises (never within a single batch)
+    float M = -INFINITY, Ls = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const float4 *po = reinterpret_cast<const float4 *>(part_o + base * kTcD) + c;
     for (int s0 = 0; s0 < nsplit; s0 += kMergeBatch) {
@@ -636,10 +644,23 @@ attend_tc_merge_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64
                 ml[u] = __ldcg(part_ml + base + (int64_t)(s0 + u) * kTcHeads);
             }
         }
+        float Mb = M;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; u++)
+            if (s0 + u < nsplit) Mb = fmaxf(Mb, ml[u].x);
+        if (Mb > M) {
+            const float r = M == -INFINITY ? 0.f : fast_exp2(M - Mb);   // nothing accumulated under -inf
+            Ls *= r;
+            acc.x *= r;
+            acc.y *= r;
+            acc.z *= r;
+            acc.w *= r;
+            M = Mb;
+        }
 #pragma unroll
         for (int u = 0; u < kMergeBatch; u++) {
-            if (s0 + u < nsplit) {
-                const float w = ml[u].x == -INFINITY ? 0.f : fast_exp2(ml[u].x - M);
+            if (s0 + u < nsplit && ml[u].x != -INFINITY) {   // an empty split's columns are not read
+                const float w = fast_exp2(ml[u].x - M);
                 Ls = fmaf(w, ml[u].y, Ls);
                 acc.x = fmaf(w, v[u].x, acc.x);
                 acc.y = fmaf(w, v[u].y, acc.y);
