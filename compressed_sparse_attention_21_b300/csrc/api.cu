@@ -328,6 +328,15 @@ void hybrid_shares(const csa_hybrid_params *p, int num_sms, int *sparse_share, i
     ks *= 2;
     const int n = num_sms > 0 ? num_sms : 148;
     int64_t d = ks + kd > 0 ? (int64_t)n * kd / (ks + kd) : n / 2;
+    // The dense branch starts while the top-k select runs.  For rows longer
+    // than 131072 entries (decode-sized batches) the select takes 16 CTAs of
+    // 1024 threads per query, each filling an SM's registers: the dense
+    // branch gets the SMs they leave.
+    const int64_t max_n = Lmax / p->ratio_csa;
+    if (L->total_q < 1024 && max_n > 131072 && max_n <= 262144) {
+        const int64_t free_sms = (int64_t)n - 16 * L->total_q;
+        if (d > free_sms) d = free_sms;
+    }
     if (d < n / 8) d = n / 8;
     if (d > n - n / 8) d = n - n / 8;
     *dense_share = (int)d;

@@ -44,7 +44,8 @@ constexpr int kScanChunk = 1024;      // entries per scan/filter CTA
 constexpr int kHistBits = 12;
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kFilterSmemCand = 3072;  // boundary candidates resolved in shared memory
-constexpr int kSelCluster = 8;        // CTAs per query in the select cluster
+constexpr int kSelCluster = 8;        // CTAs per query in the select cluster (rows up to 131072 entries)
+constexpr int kSelClusterMax = 16;    // ... and for longer rows (a non-portable cluster size)
 constexpr int kSelCandCta = 512;      // boundary-bin members one select CTA ranks directly
 constexpr int kSelCandTotal = 2048;   // ... and the whole cluster
 constexpr int kMetaWords = 8;         // per-query: ticket1, ticket2, n_sel, n_cand, bin, above
@@ -753,7 +754,7 @@ struct SelSmem {
     uint32_t tot[256];
     uint32_t cnt[2];              // this CTA's (greater, equal) counts (read by the peers)
     uint32_t off[2];
-    uint32_t coff[kSelCluster + 1];
+    uint32_t coff[kSelClusterMax + 1];
     uint32_t w[2 * (NT / 32) + 1];
     uint32_t digit, above, bin;
 };
@@ -764,12 +765,11 @@ struct SelSmem {
 // ss.ncand is zero and a __syncthreads() has passed; thread t of cluster rank
 // r holds the keys seg0 .. seg0 + m - 1 of the row in key[0 .. m).  A
 // non-null ghist (the global histogram) is returned to zero.
-template <int NT, int KPT>
+template <int NT, int KPT, int CL>
 __device__ __forceinline__ void select_core(SelSmem<NT> &ss, uint32_t *big, const uint32_t (&key)[KPT], int m, int64_t seg0,
                                             uint32_t rank, int64_t n, int top_k, bool bad, uint32_t *ghist,
                                             int32_t *idx_row, float *sc_row, int *err)
 {
-    constexpr int CL = kSelCluster;
     constexpr int BPT = kHistBins / NT;                 // top-level bins per thread
     static_assert(KPT % 4 == 0 && BPT % 4 == 0 && NT >= 256 && kHistBins % CL == 0, "select tiling");
     static_assert(kSelCandTotal <= kHistBins, "the candidate list reuses the histogram stage");
@@ -968,13 +968,12 @@ __device__ __forceinline__ void select_core(SelSmem<NT> &ss, uint32_t *big, cons
     cluster_wait();   // the peers have read this CTA's counts and candidates
 }
 
-template <int NT, int KPT>
+template <int NT, int KPT, int CL>
 __global__ void __launch_bounds__(NT, 1)
 index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
                     const int64_t *__restrict__ cu_csa, int64_t q_begin, int ratio, int top_k, WsD w,
                     int32_t *__restrict__ idx_out, float *__restrict__ score_out, int *err)
 {
-    constexpr int CL = kSelCluster;
     __shared__ __align__(16) SelSmem<NT> ss;
     __shared__ __align__(16) uint32_t s_big[kHistBins];
 
@@ -1009,7 +1008,7 @@ index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
     for (int i = tid; i < kHistBins / 4; i += NT)
         reinterpret_cast<uint4 *>(s_big)[i] = bad ? make_uint4(0, 0, 0, 0) : __ldcg(reinterpret_cast<const uint4 *>(ghist) + i);
     __syncthreads();
-    select_core<NT, KPT>(ss, s_big, key, m, seg0, rank, n, top_k, bad, ghist, idx_row, sc_row, err);
+    select_core<NT, KPT, CL>(ss, s_big, key, m, seg0, rank, n, top_k, bad, ghist, idx_row, sc_row, err);
 }
 
 constexpr int64_t kSelMaxN = (int64_t)kSelCluster * 1024 * 32;   // longest row the select cluster holds (entries)
@@ -1042,16 +1041,16 @@ int device_sms()
 // threads holding KPT keys each.
 cudaError_t launch_select(const IndexArgs &a, int64_t max_n, int64_t q0, int64_t nq, const WsD &w, cudaStream_t st)
 {
-    const dim3 grid((unsigned)kSelCluster, (unsigned)nq);
-    auto go = [&](auto kern, int nt) {
-        return launch_kernel_cluster("index_select", kern, grid, dim3(nt), 0, st, true, (unsigned)kSelCluster,
-                                     a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0, a.ratio, a.top_k, w, a.idx_out,
-                                     a.score_out, a.err);
+    auto go = [&](auto kern, int nt, int cl) {
+        return launch_kernel_cluster("index_select", kern, dim3((unsigned)cl, (unsigned)nq), dim3(nt), 0, st, true,
+                                     (unsigned)cl, a.batch, a.cu_kv, a.cu_q, a.cu_csa, q0, a.ratio, a.top_k, w,
+                                     a.idx_out, a.score_out, a.err);
     };
-    if (max_n <= kSelCluster * 256 * 8) return go(index_select_kernel<256, 8>, 256);
-    if (max_n <= kSelCluster * 256 * 16) return go(index_select_kernel<256, 16>, 256);
-    if (max_n <= kSelCluster * 512 * 32) return go(index_select_kernel<512, 32>, 512);
-    return go(index_select_kernel<1024, 32>, 1024);
+    if (max_n <= kSelCluster * 256 * 8) return go(index_select_kernel<256, 8, kSelCluster>, 256, kSelCluster);
+    if (max_n <= kSelCluster * 256 * 16) return go(index_select_kernel<256, 16, kSelCluster>, 256, kSelCluster);
+    if (max_n <= kSelCluster * 512 * 32) return go(index_select_kernel<512, 32, kSelCluster>, 512, kSelCluster);
+    // the longest rows: 16 CTAs per query, half the keys per thread
+    return go(index_select_kernel<1024, 16, kSelClusterMax>, 1024, kSelClusterMax);
 }
 
 template <int DI>

@@ -62,6 +62,10 @@ cudaError_t launch_kernel_cluster(const char *name, void (*kern)(KArgs...), dim3
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         na++;
     }
+    if (cluster_x > 8) {   // beyond the portable cluster size
+        e = cudaFuncSetAttribute(reinterpret_cast<const void *>(kern), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
     if (cluster_x > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = cluster_x;
