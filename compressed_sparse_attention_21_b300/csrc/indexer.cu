@@ -968,8 +968,11 @@ __device__ __forceinline__ void select_core(SelSmem<NT> &ss, uint32_t *big, cons
     cluster_wait();   // the peers have read this CTA's counts and candidates
 }
 
+// Rows of 16385-32768 entries (256 threads, 16 keys each) come in large
+// batches: four CTAs per SM (64 registers a thread) let a batch's clusters
+// share the GPU in fewer waves.
 template <int NT, int KPT, int CL>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NT, (NT == 256 && KPT == 16) ? 4 : 1)
 index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
                     const int64_t *__restrict__ cu_csa, int64_t q_begin, int ratio, int top_k, WsD w,
                     int32_t *__restrict__ idx_out, float *__restrict__ score_out, int *err)
