@@ -685,20 +685,26 @@ attend_tc_merge_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64
 // epilogue run.  The roles and products are those of attend_tc_kernel; key
 // tiles are numbered across items, so the stage, S and P barriers keep their
 // phases.  The TMA warp takes each item and publishes its record in a ring of
-// four slots; the gather warps, the MMA issuer and the softmax warps each
-// release a slot once they have read it.  Per item: the query tile is
-// reloaded once every S^T of the previous item has completed (QFREE), the
-// item's first P V overwrites O^T once the previous epilogue has read it
-// (OFREE), and the selection indices alternate between two buffers
-// (IDXFULL / IDXFREE).  The epilogue stores O / l from registers (two
-// neighbouring d of one head per thread), leaving the key stages to the next
-// item, and the last CTA to finish returns the counters to zero.
+// four slots; the gather warps, the MMA issuer, the softmax warps and the
+// epilogue warps each release a slot once they have read it.  Per item: the
+// query tile is reloaded once every S^T of the previous item has completed
+// (QFREE), the item's first P V overwrites O^T once the previous epilogue has
+// read it (OFREE), and the selection indices alternate between two buffers
+// (IDXFULL / IDXFREE).  The softmax warps hand each item's per-head maximum,
+// sum and 1 / sum to four epilogue warps through a two-slot buffer (LFULL /
+// LFREE) and go straight on to the next item; the epilogue warps (one per
+// tensor-memory lane quarter) store O / l from registers (two neighbouring d
+// of one head per thread) and the LSE, and the last CTA to finish returns the
+// counters to zero.
 constexpr int kTcpIdxCap = 1024;   // selection indices per buffer
 constexpr int kTcpRing = 4;
 constexpr uint32_t OFF_BARP = OFF_P + 2 * kReg;
 constexpr int PB_KFULL = 0, PB_KFREE = 2, PB_SFULL = 4, PB_SFREE = 6, PB_PFULL = 8, PB_OFULL = 10, PB_QFULL = 11,
               PB_QFREE = 12, PB_OFREE = 13, PB_IDXFULL = 14, PB_IDXFREE = 16, PB_IFULL = 18, PB_IFREE = 22,
-              PB_FIN = 26, PB_COUNT = 27;
+              PB_FIN = 26, PB_LFULL = 27, PB_LFREE = 29, PB_COUNT = 31;
+// warps 6-7 gather selected entries, warps 8-11 (one per tensor-memory lane quarter) write the epilogue
+constexpr int kTcpGatherThreads = 64;
+constexpr int kTcpEpiBase = 256;
 constexpr uint32_t OFF_MISCP = OFF_BARP + 32 * 8;
 static_assert(PB_COUNT <= 32, "persistent barriers fit their area");
 
@@ -715,7 +721,8 @@ struct alignas(16) TcItem {
 };
 constexpr uint32_t OFF_RING = OFF_MISCP + MISC_END;
 constexpr uint32_t OFF_IDXP = (OFF_RING + kTcpRing * (uint32_t)sizeof(TcItem) + 15u) & ~15u;
-constexpr uint32_t kTcpSmem = OFF_IDXP + 2 * kTcpIdxCap * 4 + 1024;   // + alignment slack
+constexpr uint32_t OFF_LBUF = OFF_IDXP + 2 * kTcpIdxCap * 4;   // [2][3][64]: per item buffer, max, sum, 1 / sum of each head
+constexpr uint32_t kTcpSmem = OFF_LBUF + 2 * 3 * kTcHeads * 4 + 1024;   // + alignment slack
 static_assert(kTcpSmem <= 232448, "shared memory per CTA");
 constexpr size_t kTcpHeader = 256;   // workspace: next item, CTAs done
 
@@ -737,7 +744,6 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     auto bar = [&](int i) { return sb + OFF_BARP + 8u * (uint32_t)i; };
     uint8_t *misc = sm + OFF_MISCP;
     float *s_m = reinterpret_cast<float *>(misc + MISC_M);
-    float *s_l = reinterpret_cast<float *>(misc + MISC_L);
     float *s_al = reinterpret_cast<float *>(misc + MISC_AL);
     float *s_rmax = reinterpret_cast<float *>(misc + MISC_RMAX);   // [4 warps][64 heads]
     float *s_rsum = reinterpret_cast<float *>(misc + MISC_RSUM);
@@ -749,19 +755,21 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         mbar_init(bar(PB_QFULL), 1);
         mbar_init(bar(PB_QFREE), 1);
         for (int s = 0; s < 2; s++) {
-            mbar_init(bar(PB_KFULL + s), 1 + kGatherThreads);   // TMA issuer + cp.async gatherers
+            mbar_init(bar(PB_KFULL + s), 1 + kTcpGatherThreads);   // TMA issuer + cp.async gatherers
             mbar_init(bar(PB_KFREE + s), 1);
             mbar_init(bar(PB_SFULL + s), 1);
             mbar_init(bar(PB_SFREE + s), 128);
             mbar_init(bar(PB_PFULL + s), 128);
-            mbar_init(bar(PB_IDXFULL + s), kGatherThreads);
+            mbar_init(bar(PB_IDXFULL + s), kTcpGatherThreads);
             mbar_init(bar(PB_IDXFREE + s), 128);
+            mbar_init(bar(PB_LFULL + s), 128);   // the softmax warps: the item's (max, sum) are written
+            mbar_init(bar(PB_LFREE + s), 128);   // the epilogue warps: read
         }
         mbar_init(bar(PB_OFULL), 1);
         mbar_init(bar(PB_OFREE), 128);
         for (int k = 0; k < kTcpRing; k++) {
             mbar_init(bar(PB_IFULL + k), 1);
-            mbar_init(bar(PB_IFREE + k), 3);   // gather warps, MMA issuer, softmax warps
+            mbar_init(bar(PB_IFREE + k), 4);   // gather warps, MMA issuer, softmax warps, epilogue warps
         }
         mbar_init(bar(PB_FIN), 1);
         fence_mbar_init();
@@ -872,22 +880,22 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (ri > 0 && !mbar_wait(bar(PB_QFULL), (ri - 1) & 1u)) set_error(err, CSA_ERR_TIMEOUT);
         }
         __syncwarp();
-    } else if (warp >= 6) {
+    } else if (warp == 6 || warp == 7) {
         // ------------------------------------------------------------ selection indices, cp.async gathers
-        // Thread pt copies 16-byte chunk pt % 8 of rows pt / 8, + 24, ... in
+        // Thread pt copies 16-byte chunk pt % 8 of rows pt / 8, + 8, ... in
         // every region of selected-entry tiles; every thread arrives on each
         // tile's KFULL (after its own copies landed), whatever the tile.
         const int pt = tid - kGatherBase;
         const int pc = pt & 7, pk0 = pt >> 3;
-        constexpr int RSTEP = kGatherThreads / 8;                 // 24 rows per pass
-        constexpr int KPP = (kTcKeys + RSTEP - 1) / RSTEP;        // 3 rows per thread
+        constexpr int RSTEP = kTcpGatherThreads / 8;              // 8 rows per pass
+        constexpr int KPP = (kTcKeys + RSTEP - 1) / RSTEP;        // 8 rows per thread
         const uint64_t keep = policy_evict_last();
         bool fail = false;
         uint32_t g = 0, ri = 0;
         for (uint32_t k = 0;; k++) {
             TcItem it;
             if (!item_at(k, it)) fail = true;
-            if (tc::named_bar_or(2, kGatherThreads, fail)) break;   // every gatherer leaves together
+            if (tc::named_bar_or(2, kTcpGatherThreads, fail)) break;   // every gatherer leaves together
             if (pt == 0) mbar_arrive(bar(PB_IFREE + (int)(k % kTcpRing)));   // all have read the record
             if (it.T < 0) break;
             if (it.T == 0) continue;
@@ -896,9 +904,9 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (GATHER) {
                 // this buffer was last read by the softmax of item ri - 2
                 if (ri >= 2 && !mbar_wait(bar(PB_IDXFREE + buf), ((ri - 2) >> 1) & 1u)) fail = true;
-                if (tc::named_bar_or(2, kGatherThreads, fail)) break;
-                for (int i = pt; i < it.n_main; i += kGatherThreads) s_idx[i] = __ldg(idx + it.qi * top_k + i);
-                tc::named_bar(2, kGatherThreads);
+                if (tc::named_bar_or(2, kTcpGatherThreads, fail)) break;
+                for (int i = pt; i < it.n_main; i += kTcpGatherThreads) s_idx[i] = __ldg(idx + it.qi * top_k + i);
+                tc::named_bar(2, kTcpGatherThreads);
                 mbar_arrive(bar(PB_IDXFULL + buf));
             }
             for (int tt = 0; tt < it.T && !fail; tt++, g++) {
@@ -1041,6 +1049,59 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (!mbar_wait(bar(PB_FIN), 0)) set_error(err, CSA_ERR_TIMEOUT);
         }
         __syncwarp();
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ epilogue (warps 8-11)
+        // Warp w reads lanes 32 (w % 4) .. + 31 of O^T (rows d = 128 m + 32 (w % 4) + lane)
+        // once the item's last P V is done and the softmax has handed over each
+        // head's (max, sum); O / l -> out[head][d] (bf16), two neighbouring d of
+        // one head per store, and the log-sum-exp.
+        const int et = tid - kTcpEpiBase;
+        const int quarter = warp & 3;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        bool fail = false;
+        uint32_t ri = 0;
+        for (uint32_t k = 0;; k++) {
+            TcItem it;
+            if (!item_at(k, it)) fail = true;
+            if (tc::named_bar_or(3, 128, fail)) break;   // every epilogue thread leaves together
+            if (et == 0) mbar_arrive(bar(PB_IFREE + (int)(k % kTcpRing)));   // all have read the record
+            if (it.T < 0) break;
+            if (it.T == 0) continue;
+            const int buf = (int)(ri & 1u);
+            const float *lb = reinterpret_cast<const float *>(sm + OFF_LBUF) + buf * 3 * kTcHeads;
+            if (!mbar_wait(bar(PB_OFULL), ri & 1u)) fail = true;
+            if (!mbar_wait(bar(PB_LFULL + buf), (ri >> 1) & 1u)) fail = true;
+            if (tc::named_bar_or(3, 128, fail)) break;
+            tc::fence_after_sync();
+            const int64_t row0 = it.qi * H + (int64_t)it.hg * kTcHeads;
+#pragma unroll 1
+            for (int c = 0; c < 8; c++) {
+                float o[32];
+                tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
+                tc::tmem_wait_ld();
+                if (c == 7) {   // O^T is read: the next item's first P V may overwrite it
+                    tc::fence_before_sync();
+                    mbar_arrive(bar(PB_OFREE));
+                }
+                const int d = 128 * (c >> 1) + 32 * quarter + lane;   // this thread's row of O^T
+                const int h0 = 32 * (c & 1);
+                // lanes 2i and 2i+1 hold d and d+1: the even lane stores (d, d+1) of
+                // head h0 + j, the odd lane those of head h0 + j + 1
+                const bool odd = lane & 1;
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const float a = o[j] * lb[2 * kTcHeads + h0 + j], b = o[j + 1] * lb[2 * kTcHeads + h0 + j + 1];
+                    const float got = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+                    const uint32_t pk = odd ? pack_bf16x2(got, b) : pack_bf16x2(a, got);
+                    const int h = h0 + j + (odd ? 1 : 0);
+                    *reinterpret_cast<uint32_t *>(out + (row0 + h) * kTcD + (d & ~1)) = pk;
+                }
+            }
+            if (lse && et < kTcHeads) lse[row0 + et] = (lb[et] + log2f(lb[kTcHeads + et])) * kTcLn2;
+            mbar_arrive(bar(PB_LFREE + buf));   // this thread reads the buffer no more
+            ri++;
+        }
+        if (fail && et == 0) set_error(err, CSA_ERR_TIMEOUT);
     } else {
         // ------------------------------------------------------------ softmax (128 threads)
         // As in attend_tc_kernel, per item: thread (w, l) takes key 16 w + l % 16
@@ -1186,40 +1247,17 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 s_rsum[warp * 64 + h2 + 1] = r1;
             }
             tc::named_bar(1, 128);
+            // hand the item's (max, sum) of each head to the epilogue warps; this
+            // buffer was last read by the epilogue of item ri - 2
+            float *lb = reinterpret_cast<float *>(sm + OFF_LBUF) + buf * 3 * kTcHeads;
+            if (ri >= 2 && !mbar_wait(bar(PB_LFREE + buf), ((ri - 2) >> 1) & 1u)) fail = true;
             if (tid < kTcHeads) {
                 const float l = s_rsum[tid] + s_rsum[64 + tid] + s_rsum[128 + tid] + s_rsum[192 + tid];
-                s_l[tid] = l;
-                s_al[tid] = l > 0.f ? 1.f / l : 0.f;
+                lb[tid] = s_m[tid];
+                lb[kTcHeads + tid] = l;
+                lb[2 * kTcHeads + tid] = l > 0.f ? 1.f / l : 0.f;
             }
-            // epilogue: O^T / l -> out[head][d] (bf16), lse
-            if (!mbar_wait(bar(PB_OFULL), ri & 1u)) fail = true;
-            if (tc::named_bar_or(1, 128, fail)) break;   // also: s_l and s_al are complete
-            tc::fence_after_sync();
-            const int64_t row0 = it.qi * H + (int64_t)it.hg * kTcHeads;
-#pragma unroll 1
-            for (int c = 0; c < 8; c++) {
-                float o[32];
-                tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
-                tc::tmem_wait_ld();
-                if (c == 7) {   // O^T is read: the next item's first P V may overwrite it
-                    tc::fence_before_sync();
-                    mbar_arrive(bar(PB_OFREE));
-                }
-                const int d = 128 * (c >> 1) + tid;   // this thread's row of O^T (tensor-memory lane)
-                const int h0 = 32 * (c & 1);
-                // lanes 2i and 2i+1 hold d and d+1: the even lane stores (d, d+1) of
-                // head h0 + j, the odd lane those of head h0 + j + 1
-                const bool odd = lane & 1;
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const float a = o[j] * s_al[h0 + j], b = o[j + 1] * s_al[h0 + j + 1];
-                    const float got = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
-                    const uint32_t pk = odd ? pack_bf16x2(got, b) : pack_bf16x2(a, got);
-                    const int h = h0 + j + (odd ? 1 : 0);
-                    *reinterpret_cast<uint32_t *>(out + (row0 + h) * kTcD + (d & ~1)) = pk;
-                }
-            }
-            if (lse && tid < kTcHeads) lse[row0 + tid] = (s_m[tid] + log2f(s_l[tid])) * kTcLn2;
+            mbar_arrive(bar(PB_LFULL + buf));
             ri++;
         }
         if (fail && tid == 0) set_error(err, CSA_ERR_TIMEOUT);
