@@ -89,6 +89,14 @@ constexpr uint32_t TM_S = 0;     // S^T buffer s: columns 64 s .. 64 s + 63 (M =
 constexpr uint32_t TM_O = 128;   // O^T block m: columns 128 + 64 m .. +63
 constexpr uint32_t kTmemCols = 512;
 
+// 2^x with subnormal results flushed to zero: a softmax weight below 2^-126
+// is negligible beside the running sum, which is at least 1.
+__device__ __forceinline__ float fast_exp2_ftz(float x)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
+    return r;
+}
 // Reduce 32 values per lane over the 16 lanes of a half-warp (xor 8, 4, 2, 1):
 // on return lane l holds the result for values 2 (l % 16) and 2 (l % 16) + 1.
 template <bool MAX>
@@ -375,9 +383,13 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 }
                 if (did) {
                     idle0 = global_ns();
-                } else if (global_ns() - idle0 > kWaitLimitNs) {
-                    ok = false;
-                    break;
+                } else {
+                    // back off briefly: this warp shares its scheduler with a softmax warp
+                    __nanosleep(20);
+                    if (global_ns() - idle0 > kWaitLimitNs) {
+                        ok = false;
+                        break;
+                    }
                 }
             }
             if (!ok) set_error(err, CSA_ERR_TIMEOUT);
@@ -478,7 +490,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             }
 #pragma unroll
             for (int j = 0; j < 32; j++) {
-                s[j] = (m_run[j] == -INFINITY) ? 0.f : fast_exp2(s[j] - m_run[j]);
+                s[j] = (m_run[j] == -INFINITY) ? 0.f : fast_exp2_ftz(s[j] - m_run[j]);
                 l_part[j] += s[j];
             }
             // This P stage was last read by P V of tile t - 2, which must be done.
@@ -1038,9 +1050,13 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 }
                 if (did) {
                     idle0 = global_ns();
-                } else if (global_ns() - idle0 > kWaitLimitNs) {
-                    ok = false;
-                    break;
+                } else {
+                    // back off briefly: this warp shares its scheduler with a softmax warp
+                    __nanosleep(20);
+                    if (global_ns() - idle0 > kWaitLimitNs) {
+                        ok = false;
+                        break;
+                    }
                 }
             }
             if (!ok) set_error(err, CSA_ERR_TIMEOUT);
@@ -1196,7 +1212,7 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 }
 #pragma unroll
                 for (int j = 0; j < 32; j++) {
-                    sc[j] = (m_run[j] == -INFINITY) ? 0.f : fast_exp2(sc[j] - m_run[j]);
+                    sc[j] = (m_run[j] == -INFINITY) ? 0.f : fast_exp2_ftz(sc[j] - m_run[j]);
                     l_part[j] += sc[j];
                 }
                 // This P stage was last read by P V of tile g - 2, which must be done.
