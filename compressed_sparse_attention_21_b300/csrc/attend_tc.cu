@@ -127,6 +127,11 @@ __device__ __forceinline__ void halfwarp_reduce32(const float *v, float &r0, flo
     r1 = a[1];
 }
 
+// 4-byte cp.async (both addresses 4-byte aligned).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
 // 16-byte cp.async (src_bytes < 16 zero-fills the rest) with an L2 policy.
 __device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, int src_bytes, uint64_t pol)
 {
@@ -697,28 +702,30 @@ attend_tc_merge_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64
 // epilogue run.  The roles and products are those of attend_tc_kernel; key
 // tiles are numbered across items, so the stage, S and P barriers keep their
 // phases.  The TMA warp takes each item and publishes its record in a ring of
-// four slots; the gather warps, the MMA issuer, the softmax warps and the
-// epilogue warps each release a slot once they have read it.  Per item: the
-// query tile is reloaded once every S^T of the previous item has completed
-// (QFREE), the item's first P V overwrites O^T once the previous epilogue has
-// read it (OFREE), and the selection indices alternate between two buffers
-// (IDXFULL / IDXFREE).  The softmax warps hand each item's per-head maximum,
+// four slots, one item ahead of the item whose loads it issues; the gather
+// warps, the MMA issuer, the softmax warps and the epilogue warps each release
+// a slot once they have read it.  Per item: the query tile is reloaded once
+// every S^T of the previous item has completed (QFREE), the item's first P V
+// overwrites O^T once the previous epilogue has read it (OFREE), and the
+// selection indices rotate through three buffers (IDXFULL / IDXFREE), the
+// gather warps copying the next item's while the current one runs.  The softmax warps hand each item's per-head maximum,
 // sum and 1 / sum to four epilogue warps through a two-slot buffer (LFULL /
 // LFREE) and go straight on to the next item; the epilogue warps (one per
 // tensor-memory lane quarter) store O / l from registers (two neighbouring d
 // of one head per thread) and the LSE, and the last CTA to finish returns the
 // counters to zero.
 constexpr int kTcpIdxCap = 1024;   // selection indices per buffer
+constexpr int kTcpIdxBufs = 3;
 constexpr int kTcpRing = 4;
 constexpr uint32_t OFF_BARP = OFF_P + 2 * kReg;
 constexpr int PB_KFULL = 0, PB_KFREE = 2, PB_SFULL = 4, PB_SFREE = 6, PB_PFULL = 8, PB_OFULL = 10, PB_QFULL = 11,
-              PB_QFREE = 12, PB_OFREE = 13, PB_IDXFULL = 14, PB_IDXFREE = 16, PB_IFULL = 18, PB_IFREE = 22,
-              PB_FIN = 26, PB_LFULL = 27, PB_LFREE = 29, PB_COUNT = 31;
+              PB_QFREE = 12, PB_OFREE = 13, PB_IDXFULL = 14, PB_IDXFREE = 17, PB_IFULL = 20, PB_IFREE = 24,
+              PB_FIN = 28, PB_LFULL = 29, PB_LFREE = 31, PB_COUNT = 33;
 // warps 6-7 gather selected entries, warps 8-11 (one per tensor-memory lane quarter) write the epilogue
 constexpr int kTcpGatherThreads = 64;
 constexpr int kTcpEpiBase = 256;
-constexpr uint32_t OFF_MISCP = OFF_BARP + 32 * 8;
-static_assert(PB_COUNT <= 32, "persistent barriers fit their area");
+constexpr uint32_t OFF_MISCP = OFF_BARP + 40 * 8;
+static_assert(PB_COUNT <= 40, "persistent barriers fit their area");
 
 struct alignas(16) TcItem {
     int64_t qi;          // query
@@ -733,7 +740,7 @@ struct alignas(16) TcItem {
 };
 constexpr uint32_t OFF_RING = OFF_MISCP + MISC_END;
 constexpr uint32_t OFF_IDXP = (OFF_RING + kTcpRing * (uint32_t)sizeof(TcItem) + 15u) & ~15u;
-constexpr uint32_t OFF_LBUF = OFF_IDXP + 2 * kTcpIdxCap * 4;   // [2][3][64]: per item buffer, max, sum, 1 / sum of each head
+constexpr uint32_t OFF_LBUF = OFF_IDXP + kTcpIdxBufs * kTcpIdxCap * 4;   // [2][3][64]: per item buffer, max, sum, 1 / sum of each head
 constexpr uint32_t kTcpSmem = OFF_LBUF + 2 * 3 * kTcHeads * 4 + 1024;   // + alignment slack
 static_assert(kTcpSmem <= 232448, "shared memory per CTA");
 constexpr size_t kTcpHeader = 256;   // workspace: next item, CTAs done
@@ -772,10 +779,12 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             mbar_init(bar(PB_SFULL + s), 1);
             mbar_init(bar(PB_SFREE + s), 128);
             mbar_init(bar(PB_PFULL + s), 128);
-            mbar_init(bar(PB_IDXFULL + s), kTcpGatherThreads);
-            mbar_init(bar(PB_IDXFREE + s), 128);
             mbar_init(bar(PB_LFULL + s), 128);   // the softmax warps: the item's (max, sum) are written
             mbar_init(bar(PB_LFREE + s), 128);   // the epilogue warps: read
+        }
+        for (int b = 0; b < kTcpIdxBufs; b++) {
+            mbar_init(bar(PB_IDXFULL + b), kTcpGatherThreads);
+            mbar_init(bar(PB_IDXFREE + b), 128);
         }
         mbar_init(bar(PB_OFULL), 1);
         mbar_init(bar(PB_OFREE), 128);
@@ -805,19 +814,15 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         bool ok = true;
         uint32_t g = 0, ri = 0;   // key tiles and items with tiles so far
         const uint64_t keep = policy_evict_last(), once = policy_evict_first();
-        for (uint32_t k = 0;; k++) {
+        // take item k, longest rows first, and publish its record
+        auto publish = [&](uint32_t k, TcItem &it) -> bool {
             const int slot = (int)(k % kTcpRing);
             int okw = 1;
             if (lane == 0 && k >= kTcpRing && !mbar_wait(bar(PB_IFREE + slot), ((k - kTcpRing) / kTcpRing) & 1u)) okw = 0;
-            if (!__shfl_sync(0xffffffffu, okw, 0)) {
-                ok = false;
-                break;
-            }
-            // the next item, longest rows first
+            if (!__shfl_sync(0xffffffffu, okw, 0)) return false;
             unsigned j = 0;
             if (lane == 0) j = atomicAdd(counters, 1u);
             j = __shfl_sync(0xffffffffu, j, 0);
-            TcItem it;
             it.T = -1;
             if ((int64_t)j < n_items) {
                 const int64_t jj = n_items - 1 - (int64_t)j;
@@ -838,8 +843,20 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 mbar_arrive(bar(PB_IFULL + slot));
             }
             __syncwarp();
-            if (it.T < 0) break;
+            return true;
+        };
+        TcItem nxt;
+        if (!publish(0, nxt)) ok = false;
+        for (uint32_t k = 0; ok && nxt.T >= 0; k++) {
+            const TcItem it = nxt;
+            // the next record goes out before this item's loads, so that the
+            // other roles can prepare the next item while this one runs
+            if (!publish(k + 1, nxt)) {
+                ok = false;
+                break;
+            }
             if (it.T == 0) continue;
+            int okw = 1;
             if (lane == 0) {
                 // the query tile: every S^T of the previous item is done with it
                 if (ri > 0 && !mbar_wait(bar(PB_QFREE), (ri - 1) & 1u)) okw = 0;
@@ -851,7 +868,7 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                         tma_tile2d(sb + OFF_Q + r * kReg, &map_q, r * 64, qrow, bar(PB_QFULL), once);
                 }
                 // tile g of the CTA goes to stage g & 1 once P V of tile g - 2 has released it;
-                // selected entries are gathered by warps 6-11, this thread only arrives for them
+                // selected entries are gathered by warps 6-7, this thread only arrives for them
                 for (int tt = 0; okw && tt < it.T; tt++) {
                     const int s = (int)(g & 1u);
                     if (g >= 2 && !mbar_wait(bar(PB_KFREE + s), ((g - 2) >> 1) & 1u)) {
@@ -903,6 +920,7 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         constexpr int KPP = (kTcKeys + RSTEP - 1) / RSTEP;        // 8 rows per thread
         const uint64_t keep = policy_evict_last();
         bool fail = false;
+        bool pre = false;   // the indices of item ri were copied during item ri - 1
         uint32_t g = 0, ri = 0;
         for (uint32_t k = 0;; k++) {
             TcItem it;
@@ -911,15 +929,43 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (pt == 0) mbar_arrive(bar(PB_IFREE + (int)(k % kTcpRing)));   // all have read the record
             if (it.T < 0) break;
             if (it.T == 0) continue;
-            const int buf = (int)(ri & 1u);
+            const int buf = (int)(ri % kTcpIdxBufs);
             int32_t *s_idx = s_idx0 + buf * kTcpIdxCap;
             if (GATHER) {
-                // this buffer was last read by the softmax of item ri - 2
-                if (ri >= 2 && !mbar_wait(bar(PB_IDXFREE + buf), ((ri - 2) >> 1) & 1u)) fail = true;
-                if (tc::named_bar_or(2, kTcpGatherThreads, fail)) break;
-                for (int i = pt; i < it.n_main; i += kTcpGatherThreads) s_idx[i] = __ldg(idx + it.qi * top_k + i);
+                if (pre) {
+                    cp_async_wait<0>();   // this thread's copies of the indices
+                } else {
+                    // this buffer was last read by the softmax of item ri - 3
+                    if (ri >= kTcpIdxBufs &&
+                        !mbar_wait(bar(PB_IDXFREE + buf), ((ri - kTcpIdxBufs) / kTcpIdxBufs) & 1u))
+                        fail = true;
+                    if (tc::named_bar_or(2, kTcpGatherThreads, fail)) break;
+                    for (int i = pt; i < it.n_main; i += kTcpGatherThreads) s_idx[i] = __ldg(idx + it.qi * top_k + i);
+                }
                 tc::named_bar(2, kTcpGatherThreads);
                 mbar_arrive(bar(PB_IDXFULL + buf));
+                // The next record, if it is out and has tiles, is item ri + 1: copy its
+                // indices into their buffer (last read by the softmax of item ri - 2)
+                // while this item's tiles are gathered.
+                pre = false;
+                const bool out = tc::named_bar_or(2, kTcpGatherThreads,
+                                                  mbar_test(bar(PB_IFULL + (int)((k + 1) % kTcpRing)), ((k + 1) / kTcpRing) & 1u));
+                if (out) {
+                    TcItem nx;
+                    if (!item_at(k + 1, nx)) fail = true;   // complete: returns at once
+                    const uint32_t rn = ri + 1;
+                    const int bn = (int)(rn % kTcpIdxBufs);
+                    if (!fail && nx.T > 0 && rn >= kTcpIdxBufs &&
+                        !mbar_wait(bar(PB_IDXFREE + bn), ((rn - kTcpIdxBufs) / kTcpIdxBufs) & 1u))
+                        fail = true;
+                    pre = !tc::named_bar_or(2, kTcpGatherThreads, fail) && nx.T > 0;
+                    if (pre) {
+                        int32_t *s_nx = s_idx0 + bn * kTcpIdxCap;
+                        for (int i = pt; i < nx.n_main; i += kTcpGatherThreads)
+                            cp_async_4(smem_u32(s_nx + i), idx + nx.qi * top_k + i);
+                        cp_async_commit();
+                    }
+                }
             }
             for (int tt = 0; tt < it.T && !fail; tt++, g++) {
                 const int s = (int)(g & 1u);
@@ -1135,9 +1181,9 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (tid == 0) mbar_arrive(bar(PB_IFREE + (int)(k % kTcpRing)));   // all have read the record
             if (it.T < 0) break;
             if (it.T == 0) continue;
-            const int buf = (int)(ri & 1u);
-            const int32_t *s_idx = s_idx0 + buf * kTcpIdxCap;
-            if (GATHER && !mbar_wait(bar(PB_IDXFULL + buf), (ri >> 1) & 1u)) fail = true;
+            const int ibuf = (int)(ri % kTcpIdxBufs);
+            const int32_t *s_idx = s_idx0 + ibuf * kTcpIdxCap;
+            if (GATHER && !mbar_wait(bar(PB_IDXFULL + ibuf), (ri / kTcpIdxBufs) & 1u)) fail = true;
             float m_run[32], l_part[32];
 #pragma unroll
             for (int j = 0; j < 32; j++) {
@@ -1252,7 +1298,7 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 tc::fence_before_sync();
                 mbar_arrive(bar(PB_PFULL + sidx));
             }
-            if (GATHER) mbar_arrive(bar(PB_IDXFREE + buf));   // this thread reads the indices no more
+            if (GATHER) mbar_arrive(bar(PB_IDXFREE + ibuf));   // this thread reads the indices no more
             // the weights' sums over keys, once: lanes (keys) within each warp, then the warps
             if (tc::named_bar_or(1, 128, fail)) break;
             {
@@ -1265,6 +1311,7 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             tc::named_bar(1, 128);
             // hand the item's (max, sum) of each head to the epilogue warps; this
             // buffer was last read by the epilogue of item ri - 2
+            const int buf = (int)(ri & 1u);
             float *lb = reinterpret_cast<float *>(sm + OFF_LBUF) + buf * 3 * kTcHeads;
             if (ri >= 2 && !mbar_wait(bar(PB_LFREE + buf), ((ri - 2) >> 1) & 1u)) fail = true;
             if (tid < kTcHeads) {
