@@ -140,6 +140,26 @@ __device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, 
                  : "memory");
 }
 
+// The eight 16-byte chunks of one row's chunk column across the eight 64-column
+// regions of a key stage: shared addresses dst + 8 KiB r, global src + 128 r
+// bytes (r = 0..7), all zero-filled when src_bytes is 0.  Immediate offsets
+// keep the issue to one instruction per chunk.
+__device__ __forceinline__ void cp_async_16_regions(uint32_t dst, const void *src, int src_bytes, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n"
+        "cp.async.cg.shared.global.L2::cache_hint [%0+8192], [%1+128], 16, %2, %3;\n"
+        "cp.async.cg.shared.global.L2::cache_hint [%0+16384], [%1+256], 16, %2, %3;\n"
+        "cp.async.cg.shared.global.L2::cache_hint [%0+24576], [%1+384], 16, %2, %3;\n"
+        "cp.async.cg.shared.global.L2::cache_hint [%0+32768], [%1+512], 16, %2, %3;\n"
+        "cp.async.cg.shared.global.L2::cache_hint [%0+40960], [%1+640], 16, %2, %3;\n"
+        "cp.async.cg.shared.global.L2::cache_hint [%0+49152], [%1+768], 16, %2, %3;\n"
+        "cp.async.cg.shared.global.L2::cache_hint [%0+57344], [%1+896], 16, %2, %3;\n" ::"r"(dst),
+        "l"(src), "r"(src_bytes), "l"(pol)
+        : "memory");
+}
+static_assert(kReg == 8192 && kRegions == 8, "the region offsets of cp_async_16_regions");
+
 // Key tiles of the query at `p`: the main keys (selected or visible entries)
 // fill ceil(n_main / 64) tiles, the raw tail its own ceil(r / 64) tiles.
 template <bool GATHER>
@@ -983,10 +1003,7 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                             const int e = slot < it.n_main ? s_idx[slot] : -1;
                             const bool v = e >= 0 && (int64_t)e < it.n_vis;
                             const uint16_t *src = entries + (it.e0 + (v ? e : 0)) * kTcD;
-#pragma unroll
-                            for (int r = 0; r < kRegions; r++)
-                                cp_async_16_hint(stage + r * kReg + kr * 128 + ((pc ^ (kr & 7)) << 4), src + r * 64 + pc * 8,
-                                                 v ? 16 : 0, keep);
+                            cp_async_16_regions(stage + kr * 128 + ((pc ^ (kr & 7)) << 4), src + pc * 8, v ? 16 : 0, keep);
                         }
                     }
                     cp_async_commit();
