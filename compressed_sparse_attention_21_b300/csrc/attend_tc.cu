@@ -132,14 +132,6 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
 }
-// 16-byte cp.async (src_bytes < 16 zero-fills the rest) with an L2 policy.
-__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, int src_bytes, uint64_t pol)
-{
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src),
-                 "r"(src_bytes), "l"(pol)
-                 : "memory");
-}
-
 // The eight 16-byte chunks of one row's chunk column across the eight 64-column
 // regions of a key stage: shared addresses dst + 8 KiB r, global src + 128 r
 // bytes (r = 0..7), all zero-filled when src_bytes is 0.  Immediate offsets
@@ -340,10 +332,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                         const int e = slot < slot1 ? s_idx[slot - slot0] : -1;
                         const bool v = e >= 0 && (int64_t)e < n_vis;
                         const uint16_t *src = entries + (p.e0 + (v ? e : 0)) * kTcD;
-#pragma unroll
-                        for (int r = 0; r < kRegions; r++)
-                            cp_async_16_hint(stage + r * kReg + k * 128 + ((pc ^ (k & 7)) << 4), src + r * 64 + pc * 8,
-                                             v ? 16 : 0, keep);
+                        cp_async_16_regions(stage + k * 128 + ((pc ^ (k & 7)) << 4), src + pc * 8, v ? 16 : 0, keep);
                     }
                 }
                 cp_async_commit();
@@ -865,17 +854,23 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             __syncwarp();
             return true;
         };
+        // With many items per CTA the next record goes out before this item's
+        // loads, so that the other roles can prepare the next item while this
+        // one runs; with few, a CTA holding an item it has not started would
+        // leave another CTA without work, so the next item is taken after them.
+        const bool ahead = n_items >= 8 * (int64_t)gridDim.x;
         TcItem nxt;
         if (!publish(0, nxt)) ok = false;
         for (uint32_t k = 0; ok && nxt.T >= 0; k++) {
             const TcItem it = nxt;
-            // the next record goes out before this item's loads, so that the
-            // other roles can prepare the next item while this one runs
-            if (!publish(k + 1, nxt)) {
+            if (ahead && !publish(k + 1, nxt)) {
                 ok = false;
                 break;
             }
-            if (it.T == 0) continue;
+            if (it.T == 0) {
+                if (!ahead && !publish(k + 1, nxt)) ok = false;
+                continue;
+            }
             int okw = 1;
             if (lane == 0) {
                 // the query tile: every S^T of the previous item is done with it
@@ -919,6 +914,7 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 ok = false;
                 break;
             }
+            if (!ahead && !publish(k + 1, nxt)) ok = false;
         }
         if (lane == 0) {
             if (!ok) set_error(err, CSA_ERR_TIMEOUT);
