@@ -63,9 +63,10 @@ def _load():
         lib.orc_e4m3_encode.restype = ctypes.c_uint8
         lib.orc_quantize_index_keys.argtypes = [P, I64, I, P, P]
         lib.orc_index_scores_fp8.argtypes = [P, P, P, I64, I, I, P]
+        lib.orc_swa_queries.argtypes = [I, P, P, P, P, I, I, I64, D, I64, P, P, P]
         for f in ("orc_compress", "orc_index_scores", "orc_topk", "orc_attend",
                   "orc_hybrid_queries", "orc_compress_packed", "orc_compress_selected",
-                  "orc_quantize_index_keys", "orc_index_scores_fp8"):
+                  "orc_quantize_index_keys", "orc_index_scores_fp8", "orc_swa_queries"):
             getattr(lib, f).restype = I
         _lib = lib
     return _lib
@@ -236,3 +237,26 @@ def hybrid_queries(inp, eval_q=None, given_idx=None, do_csa=True, do_hca=True,
                                 _ptr(out["lseH"]))
     _check(rc, "hybrid_queries")
     return out
+
+
+def swa_queries(cu_kv, cu_q, kv_bits, q_bits, window, scale, eval_q=None):
+    """Sliding-window attention of whole queries of a packed problem: each
+    query over its own raw token and the window - 1 tokens before it.
+    kv_bits [ΣL, d] and q_bits [ΣQ, H, d] are bf16 bit patterns.  Returns
+    (o [n, H, d] fp64, lse [n, H] fp64)."""
+    cu_kv = _c(cu_kv, np.int64)
+    cu_q = _c(cu_q, np.int64)
+    kv = _c(kv_bits, np.uint16)
+    q = _c(q_bits, np.uint16)
+    B = len(cu_kv) - 1
+    d = kv.shape[1]
+    H = q.shape[1]
+    if eval_q is None:
+        eval_q = np.arange(int(cu_q[-1]), dtype=np.int64)
+    eval_q = _c(eval_q, np.int64)
+    n = len(eval_q)
+    o = np.zeros((n, H, d))
+    lse = np.zeros((n, H))
+    _check(_load().orc_swa_queries(B, _ptr(cu_kv), _ptr(cu_q), _ptr(kv), _ptr(q), d, H, int(window), float(scale),
+                                   n, _ptr(eval_q), _ptr(o), _ptr(lse)), "swa_queries")
+    return o, lse

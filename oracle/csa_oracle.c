@@ -17,6 +17,9 @@
  *   [DEBT] "DeepSeek V4's architecture debt chain" (vendordeep.com),
  *          "Constraint 1 -> Innovation 1: CSA+HCA hybrid attention"
  *          (128x fusion of many tokens' KV into one compressed token).
+ *   [SWA]  the bjdmk.com.cn DeepSeek-V4 walkthrough, §3.2 "SWA
+ *          sliding-window attention": each token attends only to the
+ *          tokens of a fixed window before it (4096 in its example).
  *
  * Readings where the pages leave a step open (all listed in the design
  * notes):
@@ -32,6 +35,8 @@
  *       the block's weights are the softmax of its tokens' logits.
  *   A7  top-k order: higher score first, ties to the lower entry index;
  *       the selected indices are returned ascending, padded with -1.
+ *   W1  [SWA] the window of a token at position t holds positions
+ *       max(0, t - w + 1) .. t: the token itself and the w - 1 before it.
  *   R8  the low-precision indexer stores each key row as FP8 E4M3 codes
  *       scaled so the row's largest magnitude maps to 448, plus an fp32
  *       scale (see the FP8 section below).
@@ -448,6 +453,45 @@ int orc_compress_selected(int B, const int64_t *cu_kv, const int64_t *cu_out,
         if (j < 0 || (j + 1) * m > L) { err |= 4; continue; }
         compress_block(kv + cu_kv[bb] * (int64_t)d, gate + cu_kv[bb], d, m, j,
                        out + i * (int64_t)d);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------
+ * Sliding-window attention over the raw tokens ([SWA] §3.2, reading W1),
+ * with the shared-KV MQA of [V4] §2.2 step 3: query qi at position t of its
+ * sequence attends, with each of its H heads, over the raw token rows
+ * max(0, t - w + 1) .. t of its sequence, each row its own key and value.
+ * Per evaluated query: o [H, d], lse [H] (natural log).
+ * ---------------------------------------------------------------------- */
+int orc_swa_queries(int B, const int64_t *cu_kv, const int64_t *cu_q,
+                    const uint16_t *kv, const uint16_t *q, int d, int H,
+                    int64_t w, double scale, int64_t n_eval,
+                    const int64_t *eval_q, double *o, double *lse)
+{
+    if (B <= 0 || !cu_kv || !cu_q || !kv || !q || d <= 0 || H <= 0 || w <= 0 ||
+        n_eval < 0 || !eval_q || !o)
+        return 1;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t e = 0; e < n_eval; e++) {
+        const int64_t qi = eval_q[e];
+        const int64_t b = find_seq(B, cu_q, qi);
+        const int64_t L = cu_kv[b + 1] - cu_kv[b];
+        const int64_t nq = cu_q[b + 1] - cu_q[b];
+        const int64_t t = L - nq + (qi - cu_q[b]);
+        if (t < 0 || t >= L) { err |= 1; continue; }
+        const int64_t u0 = t - w + 1 > 0 ? t - w + 1 : 0;
+        const int64_t nk = t - u0 + 1;
+        double *keys = (double *)malloc(sizeof(double) * (size_t)nk * d);
+        if (!keys) { err |= 2; continue; }
+        for (int64_t r = 0; r < nk; r++) {
+            const uint16_t *row = kv + (cu_kv[b] + u0 + r) * (int64_t)d;
+            for (int x = 0; x < d; x++) keys[r * d + x] = bf16_to_double(row[x]);
+        }
+        err |= orc_attend(q + qi * (int64_t)H * d, H, d, keys, nk, scale,
+                          o + e * (int64_t)H * d, lse ? lse + e * (int64_t)H : NULL);
+        free(keys);
     }
     return err;
 }

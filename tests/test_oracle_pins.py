@@ -564,3 +564,77 @@ def test_compress_packed_and_selected_equal_the_single_sequence_compressor(orc):
         rows = rows[(rows >= 0) & (rows < cu[-1])]
         sel = orc.compress_selected(p["cu_kv"], cu, p["kv"], p["gate"], m, rows)
         assert np.array_equal(sel, packed[rows]), m
+
+
+# ----------------------------------------------------------------------------
+# sliding-window attention over the raw tokens (bjdmk.com.cn DeepSeek-V4
+# walkthrough, §3.2 SWA; window of a token at t: positions t - w + 1 .. t)
+# ----------------------------------------------------------------------------
+
+def sdpa_band(q_bits, kv_bits, scale, w):
+    """MQA over a causal band of width w through torch's library routine
+    (boolean mask: key j visible to query i iff i - w < j <= i), fp64 on the CPU."""
+    q = torch.from_numpy(f(q_bits)).permute(1, 0, 2)[None]          # [1, H, L, d]
+    L = q.shape[2]
+    kv = torch.from_numpy(f(kv_bits))[None, None].expand(1, q.shape[1], -1, -1)
+    i = torch.arange(L)[:, None]
+    j = torch.arange(L)[None, :]
+    mask = (j <= i) & (j > i - w)
+    o = torch.nn.functional.scaled_dot_product_attention(q, kv, kv, attn_mask=mask, scale=scale)
+    return o[0].permute(1, 0, 2).numpy()                             # [L, H, d]
+
+
+def test_swa_matches_library_attention_with_a_band_mask(orc):
+    # every window from one token to more than the sequence, on a prefill
+    p = packed_problem([47], [47], d=8, H=3, seed=60)
+    for w in (1, 2, 5, 16, 46, 47, 48, 1000):
+        o, lse = orc.swa_queries(p["cu_kv"], p["cu_q"], p["kv"], p["q"], w, p["scale"])
+        assert np.allclose(o, sdpa_band(p["q"], p["kv"], p["scale"], w), atol=1e-12), w
+
+
+def test_swa_window_one_returns_the_token_itself(orc):
+    # a single key: its weight is 1, the output is the token's row and the
+    # log-sum-exp is the one logit, scale * q_h . c_t
+    p = packed_problem([19, 5], [19, 5], d=8, H=2, seed=61)
+    o, lse = orc.swa_queries(p["cu_kv"], p["cu_q"], p["kv"], p["q"], 1, p["scale"])
+    kv, q = f(p["kv"]), f(p["q"])
+    assert np.array_equal(o, np.broadcast_to(kv[:, None, :], o.shape))
+    assert np.allclose(lse, p["scale"] * np.einsum("qhd,qd->qh", q, kv), atol=1e-12)
+
+
+def test_swa_reads_exactly_the_window(orc):
+    # changing a token outside t - w + 1 .. t leaves query t's result bit for
+    # bit; changing the window's first or last token changes it
+    L, w, t = 60, 9, 40
+    p = packed_problem([L], [L], d=8, H=2, seed=62)
+    base_o, base_l = orc.swa_queries(p["cu_kv"], p["cu_q"], p["kv"], p["q"], w, p["scale"], eval_q=[t])
+    for u, inside in ((t - w, False), (t + 1, False), (t - w + 1, True), (t, True), (0, False), (L - 1, False)):
+        kv = p["kv"].copy()
+        kv[u] = bf(f(kv[u]) * -2.0 + 0.25)
+        o, l = orc.swa_queries(p["cu_kv"], p["cu_q"], kv, p["q"], w, p["scale"], eval_q=[t])
+        assert np.array_equal(o, base_o) != inside, u
+        assert np.array_equal(l, base_l) != inside, u
+
+
+def test_swa_packed_batch_and_decode_layout(orc):
+    # A packed batch (prefill, decode and chunked sequences, one without
+    # queries) equals each sequence alone, and a decode / chunked query equals
+    # the same position of that sequence's prefill, bit for bit.
+    lengths, n_q, w = [70, 1, 45, 130, 9], [70, 1, 0, 12, 1], 13
+    p = packed_problem(lengths, n_q, seed=63)
+    o, lse = orc.swa_queries(p["cu_kv"], p["cu_q"], p["kv"], p["q"], w, p["scale"])
+    full = packed_problem(lengths, lengths, seed=63)
+    row = 0
+    for b, (L, nq) in enumerate(zip(lengths, n_q)):
+        if nq == 0:
+            continue
+        s = one_sequence(p, b)
+        oa, la = orc.swa_queries(s["cu_kv"], s["cu_q"], s["kv"], s["q"], w, p["scale"])
+        assert np.array_equal(o[row:row + nq], oa) and np.array_equal(lse[row:row + nq], la), b
+        # the same tokens as a prefill whose last nq query rows are these
+        fs = one_sequence(full, b)
+        q = np.concatenate([fs["q"][:L - nq], p["q"][row:row + nq]])
+        op, lp = orc.swa_queries(fs["cu_kv"], fs["cu_q"], fs["kv"], q, w, p["scale"])
+        assert np.array_equal(op[L - nq:], oa) and np.array_equal(lp[L - nq:], la), b
+        row += nq
+    assert row == o.shape[0]
