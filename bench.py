@@ -31,18 +31,22 @@ sys.path.insert(0, ROOT)
 
 METRIC = "CSA+HCA attention tokens/s at 64K–1M ctx; % of HBM / tensor-core roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-EXTRA_WORKLOADS = ("prefill_128k", "ragged_decode", "decode_1m")
+EXTRA_WORKLOADS = ("prefill_128k", "ragged_decode", "decode_1m", "swa_prefill_32k")
+# sliding-window attention over the raw tokens, measured as a call of its own
+# (not part of the hybrid step): one 32768-token prefill, the 128K prefill's
+# heads and width, and the 4096-token window of the SWA page's example
+SWA_PREFILL = {"name": "swa_prefill_32k", "length": 32768, "H": 64, "d": 512, "window": 4096, "seed": 7}
 
 # DRAM traffic per call of the dominant call from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum over the call's kernels),
 # keyed by (workload, call, indexer key format), with the sha256 of the sources at capture time;
 # a changed source makes the figure stale and it is reported as null.
 NCU_TRAFFIC = {
-    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,600,256 B read and
-    # 2,944 B written + index_select_kernel 1,351,936 B read (means of two captured calls)
+    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,599,616 B read and
+    # 0 B written + index_select_kernel 1,351,936 B read (means of two captured calls)
     ("decode_64k", "index_topk", "bf16"): {
-        "bytes_per_launch": 34955136,
-        "sources": {"indexer.cu": "6464f7353937b28938b3ecf0079d0c16d5b296cf9c0e6a768034be2affefa055",
+        "bytes_per_launch": 34951552,
+        "sources": {"indexer.cu": "78d0f44520c46ceca8ce0d5ba0f240682a5a1d74e7a5d8d7ad2dde165077d0db",
                     "common.cuh": "b93a7dad1acde03c5b427f390c736715adf747f244ae8d972599ce95b5ac6ab8"},
     },
 }
@@ -594,6 +598,78 @@ def measure(w, args, dev, peaks, peak_src, world, rank, local, headline):
     return out
 
 
+def swa_flops(lengths, n_q, H, d, window):
+    """Algorithmic flops of sliding-window attention: per query and head, the
+    scores and the weighted sum over min(t + 1, window) keys of width d."""
+    tot = 0
+    for L, nq in zip(lengths, n_q):
+        for t0, t1 in ((L - nq, min(L, window)), (max(L - nq, window), L)):
+            if t1 <= t0:
+                continue
+            if t1 <= window:   # t + 1 keys for t in [t0, t1)
+                tot += (t0 + 1 + t1) * (t1 - t0) // 2
+            else:              # window keys each
+                tot += window * (t1 - t0)
+    return 4 * H * d * tot
+
+
+def measure_swa(args, dev, peaks, peak_src, world, cfg=SWA_PREFILL):
+    """swa_attend alone on a prefill: CUDA graph of back-to-back calls, CUDA
+    events on the capturing stream, clocks sampled over the timed region."""
+    import torch
+    from compressed_sparse_attention_21_b300 import _lib as csa
+    from compressed_sparse_attention_21_b300 import workloads as wl
+
+    L, H, d, win = cfg["length"], cfg["H"], cfg["d"], cfg["window"]
+    q = wl.randn(cfg["seed"], 4, (L, H, d), std=1.0).to(dev)
+    kv = wl.randn(cfg["seed"], 0, (L, d), std=1.0).to(dev)
+    layout = csa.Layout([L], [L], 4, 128, device=dev)
+    scale = 1.0 / float(d) ** 0.5
+    out = torch.empty_like(q)
+    lse = torch.empty((L, H), dtype=torch.float32, device=dev)
+    ws = torch.zeros(max(1, csa.swa_workspace_size(layout, H, d, win)), dtype=torch.uint8, device=dev)
+    call = lambda: csa.swa_attend(layout, q, kv, win, scale, out=out, lse=lse, ws=ws)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(int(dev.index or 0))
+    sampler.start()
+    time.sleep(0.3)
+    reps = []
+    t_start = time.perf_counter()
+    while True:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(2):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        reps.append(max_over_ranks(e0.elapsed_time(e1), dev) / 2)
+        if time.perf_counter() - t_start >= min(args.min_seconds, 1.0) and len(reps) >= 3:
+            break
+    clocks = sampler.stop()
+    if csa.check_device_error() != 0:
+        raise RuntimeError("device error word set during the sliding-window measurement")
+    ms = statistics.median(reps)
+    fl = swa_flops([L], [L], H, d, win)
+    achieved = fl / (ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "kernel": "swa_attend", "achieved": achieved, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+            "peak_source": f"bf16_tflops burst ({peak_src}); call timed alone",
+            "alg_flops_per_launch": fl, "avg_us": ms * 1e3, "traffic": None}
+    conf = {"workload": cfg["name"], "batch": 1, "ctx": L, "lengths": "fixed", "queries_per_seq": "all positions",
+            "H": H, "d": d, "window": win, "seed": cfg["seed"], "l2": "inputs larger than L2"}
+    del q, kv, out, lse, ws, g
+    torch.cuda.empty_cache()
+    return {"value": job_value(L, world, ms), "ms_per_step": ms, "steps": 2 * len(reps), "roofline": roof,
+            "clocks": clocks, "unit": "tokens/s", "config": conf, "calls_us": {"swa_attend": ms * 1e3}}
+
+
 def measure_e2e(copies, p, args, world, dev, tokens_per_step, ncopies):
     """The same metric through the C ABI with host buffers: every step copies its
     queries in from pinned host memory and both outputs and LSEs out.
@@ -722,6 +798,9 @@ def main(argv=None):
     extra = {}
     if not args.no_extra and args.ctx == 0:
         for name in [x for x in args.extra.split(",") if x and x != w.name]:
+            if name == SWA_PREFILL["name"]:
+                extra[name] = measure_swa(args, dev, peaks, peak_src, world)
+                continue
             r = measure(wl.WORKLOADS[name], args, dev, peaks, peak_src, world, rank, local, headline=False)
             extra[name] = {k: r[k] for k in ("value", "ms_per_step", "steps", "roofline", "step_roofline", "clocks",
                                              "launches_per_step", "cache_build_ms")}

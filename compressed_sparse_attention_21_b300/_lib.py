@@ -53,7 +53,8 @@ EXPORTS = ("csa_compress", "hca_compress", "lightning_index_topk", "csa_index_wo
            "lightning_index_topk_static", "csa_quantize_index_keys", "csa_quantize_index_keys_closed",
            "lightning_index_topk_fp8",
            "csa_index_fp8_workspace_size",
-           "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size", "hybrid_attend",
+           "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size", "swa_attend",
+           "swa_workspace_size", "hybrid_attend",
            "csa_workspace_size", "csa_workspace_init", "csa_status_string", "csa_check_device_error",
            "csa_version", "csa_timing_enable", "csa_timing_read", "csa_timing_reset")
 
@@ -81,6 +82,8 @@ def load():
     lib.sparse_mqa_attend.argtypes = [LP, P, P, P, P, I, I, I, I, F, P, P, P, Z, P]
     lib.hca_dense_attend.argtypes = [LP, P, P, P, I, I, I, F, P, P, P, Z, P]
     lib.csa_attend_workspace_size.argtypes = [LP, I, I, I, I, ctypes.POINTER(Z)]
+    lib.swa_attend.argtypes = [LP, P, P, I, I, I, F, P, P, P, Z, P]
+    lib.swa_workspace_size.argtypes = [LP, I, I, I, ctypes.POINTER(Z)]
     lib.hybrid_attend.argtypes = [ctypes.POINTER(csa_hybrid_params), P]
     lib.csa_workspace_size.argtypes = [ctypes.POINTER(csa_hybrid_params), ctypes.POINTER(Z)]
     lib.csa_workspace_init.argtypes = [P, Z, P]
@@ -96,7 +99,7 @@ def load():
     for f in ("csa_compress", "hca_compress", "lightning_index_topk", "csa_index_workspace_size",
               "lightning_index_topk_static", "csa_quantize_index_keys", "csa_quantize_index_keys_closed",
               "lightning_index_topk_fp8", "csa_index_fp8_workspace_size", "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size",
-              "hybrid_attend",
+              "swa_attend", "swa_workspace_size", "hybrid_attend",
               "csa_workspace_size", "csa_workspace_init", "csa_check_device_error", "csa_timing_enable"):
         getattr(lib, f).restype = I
     _lib = lib
@@ -321,6 +324,27 @@ def hca_dense_attend(layout, q, hca_entries, kv, scale, out=None, lse=None, ws=N
     _check(load().hca_dense_attend(ctypes.byref(layout.c), _ptr(q), _ptr(hca_entries), _ptr(kv), H, d, ratio,
                                    float(scale), _ptr(out), _ptr(lse), _ptr(ws), nb, _stream(stream)),
            "hca_dense_attend")
+    return out, lse
+
+
+def swa_workspace_size(layout, n_heads, d, window):
+    n = ctypes.c_size_t(0)
+    _check(load().swa_workspace_size(ctypes.byref(layout.c), n_heads, d, window, ctypes.byref(n)),
+           "swa_workspace_size")
+    return n.value
+
+
+def swa_attend(layout, q, kv, window, scale, out=None, lse=None, ws=None, stream=None):
+    """Sliding-window attention of each query over its own raw token and the
+    window - 1 tokens before it (all heads share the tokens as keys and values)."""
+    H, d = q.shape[-2], q.shape[-1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((layout.total_q, H), dtype=torch.float32, device=q.device)
+    ws, nb = _ws(swa_workspace_size(layout, H, d, window), q.device, ws)
+    _check(load().swa_attend(ctypes.byref(layout.c), _ptr(q), _ptr(kv), H, d, int(window), float(scale), _ptr(out),
+                             _ptr(lse), _ptr(ws), nb, _stream(stream)), "swa_attend")
     return out, lse
 
 

@@ -273,6 +273,33 @@ csa_status_t check_attend(const csa_layout *L, bool sparse, const csa_bf16 *q, c
     return CSA_OK;
 }
 
+// Sliding-window attention over the raw tokens: the dense attention with
+// every raw token as its own entry (entries = kv, ratio 1, so no raw tail)
+// and only the most recent `window` entries visible.
+AttendArgs swa_args(const csa_layout *L, const csa_bf16 *q, const csa_bf16 *kv, int H, int d, int window,
+                           float scale, csa_bf16 *out, float *lse, void *ws, size_t ws_bytes, int *err, int num_sms)
+{
+    AttendArgs a = attend_args(L, false, q, kv, kv, nullptr, H, d, 1, window, scale, out, lse, ws, ws_bytes, err,
+                               num_sms, num_sms);
+    a.cu_ent = L->cu_kv;
+    a.n_ent_rows = L->total_kv;
+    return a;
+}
+
+csa_status_t check_swa(const csa_layout *L, const csa_bf16 *q, const csa_bf16 *kv, int H, int d, int window,
+                              const csa_bf16 *out, const float *lse)
+{
+    CSA_TRY(check_layout(L, false, false));
+    if (window <= 0) return CSA_ERR_INVALID_ARG;
+    if (!attend_supported(H, d)) return CSA_ERR_UNSUPPORTED;
+    const bool any_q = L->total_q > 0;
+    CSA_TRY(check_ptr(q, any_q));
+    CSA_TRY(check_ptr(out, any_q));
+    CSA_TRY(check_ptr(kv, any_q));
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return CSA_ERR_INVALID_ARG;
+    return CSA_OK;
+}
+
 csa_status_t compress_impl(const csa_layout *L, bool csa_side, const csa_bf16 *kv, const float *gate, int d,
                            int ratio, csa_bf16 *out, cudaStream_t st)
 {
@@ -567,6 +594,34 @@ csa_status_t hca_dense_attend(const csa_layout *layout, const csa_bf16 *q, const
     return from_cuda(launch_attend(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+csa_status_t swa_workspace_size(const csa_layout *layout, int n_heads, int d, int window, size_t *bytes)
+{
+    if (!bytes) return CSA_ERR_INVALID_ARG;
+    CSA_TRY(check_layout(layout, false, false));
+    if (window <= 0) return CSA_ERR_INVALID_ARG;
+    if (!attend_supported(n_heads, d)) return CSA_ERR_UNSUPPORTED;
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    const AttendArgs a = swa_args(layout, nullptr, nullptr, n_heads, d, window, 1.f, nullptr, nullptr, nullptr, 0,
+                                  nullptr, ds->num_sms);
+    *bytes = align_ws(attend_workspace_bytes(a));
+    return CSA_OK;
+}
+
+csa_status_t swa_attend(const csa_layout *layout, const csa_bf16 *q, const csa_bf16 *kv, int n_heads, int d,
+                        int window, float scale, csa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                        csa_stream_t stream)
+{
+    CSA_TRY(check_swa(layout, q, kv, n_heads, d, window, out, lse));
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    const AttendArgs a = swa_args(layout, q, kv, n_heads, d, window, scale, out, lse, ws, ws_bytes, ds->err,
+                                  ds->num_sms);
+    const size_t need = attend_workspace_bytes(a);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return CSA_ERR_WORKSPACE;
+    return from_cuda(launch_attend(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 csa_status_t csa_workspace_size(const csa_hybrid_params *p, size_t *bytes)
 {
     if (!p || !bytes) return CSA_ERR_INVALID_ARG;
@@ -746,7 +801,7 @@ csa_status_t csa_check_device_error(csa_stream_t stream, csa_status_t *device_st
     return CSA_OK;
 }
 
-int csa_version(void) { return 111; }   // 1.1: FP8 indexer keys; .1: the closed-rows quantiser
+int csa_version(void) { return 120; }   // 1.1: FP8 indexer keys (.1: the closed-rows quantiser); 1.2: swa_attend
 
 csa_status_t csa_timing_enable(int enable)
 {

@@ -151,11 +151,13 @@ attend_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t *__res
     }
     KeySet ks;
     ks.safe = kv;
-    ks.entries = entries + p.e0 * D;
+    // main keys: the selected entries (at most top_k), or all visible entries,
+    // or with top_k > 0 only the most recent top_k of them (a sliding window)
+    ks.n_main = (int)(top_k > 0 && n_vis > top_k ? top_k : n_vis);
+    ks.entries = entries + (p.e0 + (GATHER ? 0 : n_vis - ks.n_main)) * D;
     ks.tail = kv + (p.kv0 + p.t - r_tail + 1) * D;
     ks.idx = GATHER ? idx + qi * top_k : nullptr;
     ks.n_vis = n_vis;
-    ks.n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
     ks.n_keys = ks.n_main + r_tail;
     const int nsplit = (ks.n_keys + kps - 1) / kps;
     if (split >= nsplit) return;
@@ -500,7 +502,7 @@ Plan make_plan(const AttendArgs &a)
     pl.HT = (a.n_heads <= 16 || units64 < share) ? 16 : 64;
     pl.HG = (a.n_heads + pl.HT - 1) / pl.HT;
     const int64_t max_vis = a.max_kv_len / a.ratio;
-    int64_t mk = (a.idx ? (max_vis < a.top_k ? max_vis : a.top_k) : max_vis) + (a.ratio - 1);
+    int64_t mk = (a.top_k > 0 && max_vis > a.top_k ? a.top_k : max_vis) + (a.ratio - 1);
     if (mk > a.max_kv_len) mk = a.max_kv_len;   // tail never exceeds the sequence
     if (mk < 1) mk = 1;
     pl.max_keys = (int)mk;

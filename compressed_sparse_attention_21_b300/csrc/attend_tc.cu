@@ -152,13 +152,22 @@ __device__ __forceinline__ void cp_async_16_regions(uint32_t dst, const void *sr
 }
 static_assert(kReg == 8192 && kRegions == 8, "the region offsets of cp_async_16_regions");
 
-// Key tiles of the query at `p`: the main keys (selected or visible entries)
-// fill ceil(n_main / 64) tiles, the raw tail its own ceil(r / 64) tiles.
+// Main keys of a query with n_vis visible entries: the selected entries
+// (GATHER: at most top_k), or the visible entries themselves, all of them, or
+// with top_k > 0 only the most recent top_k (a sliding window; the first of
+// them is entry n_vis - n_main).
+__device__ __forceinline__ int tc_main_keys(int64_t n_vis, int top_k)
+{
+    return (int)(top_k > 0 && n_vis > top_k ? top_k : n_vis);
+}
+
+// Key tiles of the query at `p`: the main keys fill ceil(n_main / 64)
+// tiles, the raw tail its own ceil(r / 64) tiles.
 template <bool GATHER>
 __device__ __forceinline__ int tc_tiles(const QueryPos &p, int ratio, int top_k, int *t_main)
 {
     const int64_t n_vis = (p.t + 1) / ratio;
-    const int n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
+    const int n_main = tc_main_keys(n_vis, top_k);
     const int r_tail = (int)((p.t + 1) % ratio);
     const int tm = (n_main + kTcKeys - 1) / kTcKeys;
     if (t_main) *t_main = tm;
@@ -202,7 +211,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         if (nsplit_max > 1 && tid < kTcHeads) part_ml[ml_slot + tid] = make_float2(-INFINITY, 0.f);
         return;
     }
-    const int n_main = GATHER ? (int)(n_vis < top_k ? n_vis : top_k) : (int)n_vis;
+    const int n_main = tc_main_keys(n_vis, top_k);
+    const int64_t e_first = p.e0 + (GATHER ? 0 : n_vis - n_main);   // dense: the first main entry row
     int T_main = 0;
     const int T_all = tc_tiles<GATHER>(p, ratio, top_k, &T_main);
     const int nsplit = tc_nsplit(T_all, nsplit_max);
@@ -287,7 +297,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 mbar_expect_tx(fb, (GATHER && tile < T_main) ? 0u : kStage);   // selected entries: cp.async
                 if (tile < T_main) {
                     if (!GATHER) {
-                        const int row = (int)(p.e0 + (int64_t)tile * kTcKeys);
+                        const int row = (int)(e_first + (int64_t)tile * kTcKeys);
 #pragma unroll
                         for (int r = 0; r < kRegions; r++)
                             tma_tile2d(stage + r * kReg, &map_ent_rows, r * 64, row, fb, keep);
@@ -841,9 +851,11 @@ attend_tcp_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const bool bad = p.t < 0 || p.t >= p.L || p.L > max_kv_len || p.ne != p.L / ratio;
                 it.n_vis = (p.t + 1) / ratio;
                 it.r_tail = (int)((p.t + 1) % ratio);
-                it.e0 = p.e0;
+                it.n_main = tc_main_keys(it.n_vis, top_k);
+                // gathered rows are indexed from the sequence's first entry,
+                // dense tiles start at the first main entry
+                it.e0 = p.e0 + (GATHER ? 0 : it.n_vis - it.n_main);
                 it.tail_row0 = p.kv0 + p.t - it.r_tail + 1;
-                it.n_main = GATHER ? (int)(it.n_vis < top_k ? it.n_vis : top_k) : (int)it.n_vis;
                 it.T = bad ? 0 : tc_tiles<GATHER>(p, ratio, top_k, &it.T_main);
                 if (bad && lane == 0) set_error(err, CSA_ERR_DEVICE);
             }
@@ -1365,7 +1377,7 @@ TcPlan tc_plan(const AttendArgs &a)
     const int share = a.sm_share > 0 ? a.sm_share : (a.num_sms > 0 ? a.num_sms : 148);
     const int64_t units = a.total_q * (a.n_heads / kTcHeads);
     const int64_t max_vis = a.max_kv_len / a.ratio;
-    int64_t mk = (a.idx ? (max_vis < a.top_k ? max_vis : a.top_k) : max_vis) + (a.ratio - 1);
+    int64_t mk = (a.top_k > 0 && max_vis > a.top_k ? a.top_k : max_vis) + (a.ratio - 1);
     if (mk > a.max_kv_len) mk = a.max_kv_len;   // the tail never exceeds the sequence
     if (mk < 1) mk = 1;
     const int64_t tiles = (mk + kTcKeys - 1) / kTcKeys;

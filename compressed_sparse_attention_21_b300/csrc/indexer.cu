@@ -602,7 +602,6 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
     __shared__ uint32_t s_hist[kHistBins];
     __shared__ __align__(8) uint64_t s_bar[kScanStages];
 
-    griddep_launch();   // the select kernel may launch; it waits for this grid
     const int tid = threadIdx.x;
     const int64_t qg = blockIdx.y;
     const int64_t qi = q_begin + qg;
@@ -733,6 +732,10 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
             return;
         }
         if (tid == 0 && c + kScanStages < nchunks) issue(c + kScanStages);
+        // the select kernel may launch once every CTA has scored its first
+        // chunk (it waits for this grid); launched earlier, its waiting CTAs
+        // hold SMs that the branch started beside the select wants
+        if (c == 0) griddep_launch();
     }
     uint32_t *ghist = w.hist + qg * kHistBins;
     for (int i = tid; i < kHistBins; i += kScanThreads) {

@@ -298,6 +298,29 @@ csa_status_t csa_attend_workspace_size(const csa_layout *layout, int n_heads, in
                                        int top_k, size_t *bytes);
 
 /* ---------------------------------------------------------------------------
+ * Sliding-window shared-KV multi-query attention over the raw tokens (the
+ * bjdmk.com.cn DeepSeek-V4 walkthrough, §3.2 "SWA sliding-window attention":
+ * each token attends only to a fixed window of the tokens before it, 4096 in
+ * its example).  Reading: the window holds the
+ * query's own token and the window - 1 tokens before it.  Query row i at
+ * position t of sequence b attends over
+ *     { kv[cu_kv[b] + u] : max(0, t - window + 1) <= u <= t }
+ * with the output and lse of sparse_mqa_attend (each token serves as its own
+ * key and value; all heads share them).  Only cu_kv and cu_q of the layout
+ * are read (cu_csa / cu_hca may be NULL).
+ *   q      [total_q, n_heads, d] bf16;  kv [total_kv, d] bf16
+ *   out    [total_q, n_heads, d] bf16;  lse [total_q, n_heads] fp32 (nullable)
+ *   window >= 1 (CSA_ERR_INVALID_ARG otherwise); d and n_heads as for
+ *   sparse_mqa_attend.  The workspace (swa_workspace_size) holds split
+ *   partial results; the caller owns it, and it needs no clearing.
+ * ------------------------------------------------------------------------- */
+csa_status_t swa_attend(const csa_layout *layout, const csa_bf16 *q, const csa_bf16 *kv,
+                        int n_heads, int d, int window, float scale, csa_bf16 *out, float *lse,
+                        void *ws, size_t ws_bytes, csa_stream_t stream);
+csa_status_t swa_workspace_size(const csa_layout *layout, int n_heads, int d, int window,
+                                size_t *bytes);
+
+/* ---------------------------------------------------------------------------
  * Hybrid step (§2.3: CSA and HCA layers alternate): runs, on the same
  * inputs, compression into both caches (unless CSA_SKIP_COMPRESS), then the
  * CSA branch (indexer, top-k, sparse attention) and the HCA branch (dense

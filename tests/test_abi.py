@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.csa_version() == 111
+    assert lib.csa_version() == 120
     assert lib.csa_status_string(0) == b"ok"
     assert lib.csa_status_string(3) == b"workspace missing or too small"
 
@@ -156,3 +156,23 @@ def test_hybrid_flags_checked_on_host(lib):
         p.k_idx_scale = 256
         assert lib.hybrid_attend(ctypes.byref(p), None) == 4
         assert lib.csa_quantize_index_keys(ctypes.byref(layout()), 256, 64, 256, 256, None) == 4
+
+
+def test_swa_arguments_checked_on_host(lib):
+    # swa_attend reads only cu_kv and cu_q of the layout; a window below one,
+    # an unsupported head count or d, a missing or misaligned pointer and a
+    # bad layout are refused before anything runs
+    L = layout(cu_csa=None, cu_hca=None)
+    need = ctypes.c_size_t(0)
+    for bad_window in (0, -5):
+        assert lib.swa_attend(ctypes.byref(L), 256, 256, 8, 128, bad_window, 1.0, 256, None, None, 0, None) == 1
+        assert lib.swa_workspace_size(ctypes.byref(L), 8, 128, bad_window, ctypes.byref(need)) == 1
+    assert lib.swa_attend(ctypes.byref(L), 256, 256, 32, 128, 64, 1.0, 256, None, None, 0, None) == 2   # 32 heads
+    assert lib.swa_attend(ctypes.byref(L), 256, 256, 8, 256, 64, 1.0, 256, None, None, 0, None) == 2   # d = 256
+    assert lib.swa_attend(ctypes.byref(L), None, 256, 8, 128, 64, 1.0, 256, None, None, 0, None) == 1  # q
+    assert lib.swa_attend(ctypes.byref(L), 256, 264, 8, 128, 64, 1.0, 256, None, None, 0, None) == 1   # kv
+    assert lib.swa_attend(ctypes.byref(L), 256, 256, 8, 128, 64, 1.0, 256, 258, None, 0, None) == 1    # lse
+    assert lib.swa_workspace_size(ctypes.byref(L), 8, 128, 64, None) == 1
+    for bad in BAD_LAYOUTS:
+        B = layout(**bad)
+        assert lib.swa_attend(ctypes.byref(B), 256, 256, 8, 128, 64, 1.0, 256, None, None, 0, None) == 1, bad

@@ -61,3 +61,12 @@ def test_fast_count_equals_the_per_position_count():
 def test_job_value_counts_every_rank():
     b = _bench()
     assert b.job_value(16, 4, 0.5) == 16 * 4 / 0.5e-3
+
+
+def test_swa_flops_closed_form_equals_the_per_position_count():
+    # 4 H d flops per key per query (scores and weighted sum), min(t + 1, w)
+    # keys for the query at position t
+    for lengths, n_q, w in (([100], [100], 7), ([100], [3], 7), ([5, 300, 64], [5, 1, 30], 64),
+                            ([4097, 10], [4097, 1], 4096), ([50], [50], 1000), ([1], [1], 1)):
+        per_pos = sum(min(t + 1, w) for L, nq in zip(lengths, n_q) for t in range(L - nq, L))
+        assert _bench().swa_flops(lengths, n_q, 2, 3, w) == 4 * 2 * 3 * per_pos

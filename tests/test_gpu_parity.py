@@ -408,6 +408,80 @@ def test_attend_persistent_invisible_index_is_reported_and_skipped():
 
 
 # ---------------------------------------------------------------------------
+# f4: sliding-window attention over the raw tokens
+# ---------------------------------------------------------------------------
+def _swa_check(p, window, eval_q=None):
+    g = P.GpuProblem(p)
+    inp = wl.to_numpy(p)
+    o, lse = csa.swa_attend(g.layout, g.q, g.kv, window, p["scale"])
+    torch.cuda.synchronize()
+    assert csa.check_device_error() == 0
+    ref_o, ref_l = oracle.swa_queries(inp["cu_kv"], inp["cu_q"], inp["kv"], inp["q"], window, p["scale"],
+                                      eval_q=eval_q)
+    got_o, got_l = P.bf16_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    if eval_q is not None:
+        got_o, got_l = got_o[eval_q], got_l[eval_q]
+    P.assert_att(got_o, ref_o, f"swa w={window}")
+    assert np.abs(got_l - ref_l).max() <= 1e-2, window
+
+
+@pytest.mark.parametrize("H,d", [(8, 128), (8, 512), (64, 512), (128, 512), (64, 128)])
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+@pytest.mark.parametrize("window", [1, 64, 65, 300, 1 << 20])
+def test_swa_parity(H, d, mode, window):
+    # decode: one query per sequence, its window split over several CTAs;
+    # prefill: every position (d = 512 with 64 heads runs the persistent kernel);
+    # windows of one token, one tile, one tile and one key, several tiles, all
+    lengths = [1, 3, 4, 129, 1000, 5003] if mode == "decode" else [1, 130, 257, 70]
+    n_q = [1] * len(lengths) if mode == "decode" else lengths
+    _swa_check(problem(lengths, n_q, H=H, d=d, seed=H + d + window % 97), window)
+
+
+def test_swa_bench_config_sampled():
+    # the sliding-window call exactly as bench.py times it (32768-token prefill,
+    # 64 heads, d = 512, window 4096, its seeded inputs), checked on the window's
+    # boundary positions and a random sample
+    import bench
+    cfg = bench.SWA_PREFILL
+    L, H, d, win = cfg["length"], cfg["H"], cfg["d"], cfg["window"]
+    q = wl.randn(cfg["seed"], 4, (L, H, d), std=1.0)
+    kv = wl.randn(cfg["seed"], 0, (L, d), std=1.0)
+    layout = csa.Layout([L], [L], 4, 128, device="cuda")
+    scale = 1.0 / float(d) ** 0.5
+    o, lse = csa.swa_attend(layout, q.cuda(), kv.cuda(), win, scale)
+    torch.cuda.synchronize()
+    assert csa.check_device_error() == 0
+    rng = np.random.default_rng(3)
+    eval_q = np.unique(np.concatenate([[0, 1, 63, 64, 4094, 4095, 4096, 4097, 20000, L - 1],
+                                       rng.integers(0, L, 22)])).astype(np.int64)
+    ref_o, ref_l = oracle.swa_queries(np.array([0, L]), np.array([0, L]), wl.bits(kv), wl.bits(q), win, scale,
+                                      eval_q=eval_q)
+    P.assert_att(P.bf16_to_f64(o)[eval_q], ref_o, "swa bench config")
+    assert np.abs(lse.cpu().numpy()[eval_q] - ref_l).max() <= 1e-2
+
+
+@pytest.mark.parametrize("window", [4096, 700])
+def test_swa_prefill_many_queries_per_cta(window):
+    # 4096 + 1500 queries on at most 148 CTAs: the persistent kernel takes each
+    # next query ahead of its loads; checked on every 7th query
+    lengths = [4096, 1500]
+    p = problem(lengths, lengths, H=64, d=512, seed=window)
+    _swa_check(p, window, eval_q=np.arange(0, sum(lengths), 7))
+
+
+def test_swa_chunked_and_decode_layouts_without_queries():
+    # chunked and decode sequences beside one with no queries, and a call
+    # with no queries at all
+    p = problem([900, 64, 77, 3000], [17, 0, 1, 64], H=64, d=512, seed=5)
+    _swa_check(p, 128)
+    e = problem([5, 9], [0, 0], H=64, d=512, seed=6)
+    g = P.GpuProblem(e)
+    o, lse = csa.swa_attend(g.layout, g.q, g.kv, 8, e["scale"])
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and csa.check_device_error() == 0
+
+
+# ---------------------------------------------------------------------------
 # a6: the hybrid step
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("case", ["prefill_small", "decode_small", "chunked"])
