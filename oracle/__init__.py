@@ -64,9 +64,11 @@ def _load():
         lib.orc_quantize_index_keys.argtypes = [P, I64, I, P, P]
         lib.orc_index_scores_fp8.argtypes = [P, P, P, I64, I, I, P]
         lib.orc_swa_queries.argtypes = [I, P, P, P, P, I, I, I64, D, I64, P, P, P]
+        lib.orc_inverse_rope.argtypes = [I, P, P, I, I, I, D, P, P]
         for f in ("orc_compress", "orc_index_scores", "orc_topk", "orc_attend",
                   "orc_hybrid_queries", "orc_compress_packed", "orc_compress_selected",
-                  "orc_quantize_index_keys", "orc_index_scores_fp8", "orc_swa_queries"):
+                  "orc_quantize_index_keys", "orc_index_scores_fp8", "orc_swa_queries",
+                  "orc_inverse_rope"):
             getattr(lib, f).restype = I
         _lib = lib
     return _lib
@@ -260,3 +262,17 @@ def swa_queries(cu_kv, cu_q, kv_bits, q_bits, window, scale, eval_q=None):
     _check(_load().orc_swa_queries(B, _ptr(cu_kv), _ptr(cu_q), _ptr(kv), _ptr(q), d, H, int(window), float(scale),
                                    n, _ptr(eval_q), _ptr(o), _ptr(lse)), "swa_queries")
     return o, lse
+
+
+def inverse_rope(cu_kv, cu_q, o, d_rope, base):
+    """Inverse-RoPE correction of attention outputs o [ΣQ, H, d] (fp64): each
+    query's last d_rope dims of every head, pairs (2i, 2i+1), turned by
+    -t * base^(-2i/d_rope) for the query's position t.  Returns a new array."""
+    cu_kv = _c(cu_kv, np.int64)
+    cu_q = _c(cu_q, np.int64)
+    o = _c(o, np.float64)
+    out = np.empty_like(o)
+    H, d = o.shape[1], o.shape[2]
+    _check(_load().orc_inverse_rope(len(cu_kv) - 1, _ptr(cu_kv), _ptr(cu_q), H, d, int(d_rope), float(base),
+                                    _ptr(o), _ptr(out)), "inverse_rope")
+    return out

@@ -35,6 +35,11 @@
  *       the block's weights are the softmax of its tokens' logits.
  *   A7  top-k order: higher score first, ties to the lower entry index;
  *       the selected indices are returned ascending, padded with -1.
+ *   P1-P4 [DEBT]'s inverse-RoPE correction of the attention output (the
+ *       pages give no convention; readings): P1 the rotated dims are the
+ *       last d_rope of each head's d; P2 they pair as (2i, 2i+1) within that
+ *       slice; P3 pair i turns at theta_i = base^(-2i/d_rope); P4 the output
+ *       of the query at position t is turned by the angle -t * theta_i.
  *   W1  [SWA] the window of a token at position t holds positions
  *       max(0, t - w + 1) .. t: the token itself and the w - 1 before it.
  *   R8  the low-precision indexer stores each key row as FP8 E4M3 codes
@@ -492,6 +497,46 @@ int orc_swa_queries(int B, const int64_t *cu_kv, const int64_t *cu_q,
         err |= orc_attend(q + qi * (int64_t)H * d, H, d, keys, nk, scale,
                           o + e * (int64_t)H * d, lse ? lse + e * (int64_t)H : NULL);
         free(keys);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------
+ * Inverse-RoPE correction of attention outputs ([DEBT] "Constraint 1 ->
+ * Innovation 1": the attention output receives an inverse rotary
+ * correction; readings P1-P4).  For the query qi at position t of its
+ * sequence, each head h and pair i < d_rope / 2, with
+ *     phi = t * base^(-2i / d_rope),
+ *     (x, y) = (o[qi, h, d - d_rope + 2i], o[qi, h, d - d_rope + 2i + 1]),
+ * the pair becomes (x cos phi + y sin phi, -x sin phi + y cos phi), the
+ * rotation by -phi; every other dim is copied.  in, out: [nq_total, H, d].
+ * ---------------------------------------------------------------------- */
+int orc_inverse_rope(int B, const int64_t *cu_kv, const int64_t *cu_q, int H, int d,
+                     int d_rope, double base, const double *in, double *out)
+{
+    if (B <= 0 || !cu_kv || !cu_q || !in || !out || H <= 0 || d <= 0 ||
+        d_rope <= 0 || d_rope > d || (d_rope & 1) || !(base > 0.0))
+        return 1;
+    const int64_t nq_total = cu_q[B];
+    int err = 0;
+#pragma omp parallel for schedule(static) reduction(| : err)
+    for (int64_t qi = 0; qi < nq_total; qi++) {
+        const int64_t b = find_seq(B, cu_q, qi);
+        const int64_t L = cu_kv[b + 1] - cu_kv[b];
+        const int64_t t = L - (cu_q[b + 1] - cu_q[b]) + (qi - cu_q[b]);
+        if (t < 0 || t >= L) { err |= 1; continue; }
+        for (int h = 0; h < H; h++) {
+            const double *x = in + (qi * H + h) * (int64_t)d;
+            double *y = out + (qi * H + h) * (int64_t)d;
+            for (int c = 0; c < d; c++) y[c] = x[c];
+            for (int i = 0; i < d_rope / 2; i++) {
+                const double phi = (double)t * pow(base, -2.0 * i / d_rope);
+                const double c0 = cos(phi), s0 = sin(phi);
+                const int j = d - d_rope + 2 * i;
+                y[j] = x[j] * c0 + x[j + 1] * s0;
+                y[j + 1] = -x[j] * s0 + x[j + 1] * c0;
+            }
+        }
     }
     return err;
 }

@@ -638,3 +638,55 @@ def test_swa_packed_batch_and_decode_layout(orc):
         assert np.array_equal(op[L - nq:], oa) and np.array_equal(lp[L - nq:], la), b
         row += nq
     assert row == o.shape[0]
+
+
+# ----------------------------------------------------------------------------
+# inverse-RoPE correction of the attention output ("DeepSeek V4's architecture
+# debt chain", Constraint 1 -> Innovation 1; convention readings P1-P4, which
+# the pages do not fix: parity partly unpinned)
+# ----------------------------------------------------------------------------
+
+def _rope_problem(lengths, n_q, H=3, d=16, seed=70):
+    rng = np.random.default_rng(seed)
+    cu_kv = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    cu_q = np.concatenate([[0], np.cumsum(n_q)]).astype(np.int64)
+    o = rng.standard_normal((int(cu_q[-1]), H, d))
+    return cu_kv, cu_q, o
+
+
+def test_inverse_rope_position_zero_and_other_dims_unchanged(orc):
+    cu_kv, cu_q, o = _rope_problem([40, 7], [40, 7])
+    for d_rope in (2, 8, 16):
+        out = orc.inverse_rope(cu_kv, cu_q, o, d_rope, 10000.0)
+        assert np.array_equal(out[:, :, :16 - d_rope], o[:, :, :16 - d_rope])   # untouched dims
+        assert np.array_equal(out[0], o[0]) and np.array_equal(out[40], o[40])   # t = 0 of each sequence
+        pairs_in = o[:, :, 16 - d_rope:].reshape(len(o), 3, -1, 2)
+        pairs_out = out[:, :, 16 - d_rope:].reshape(len(o), 3, -1, 2)
+        assert np.allclose(np.hypot(*np.moveaxis(pairs_out, -1, 0)), np.hypot(*np.moveaxis(pairs_in, -1, 0)),
+                           rtol=1e-13)
+
+
+def test_inverse_rope_undoes_the_forward_rotary_embedding(orc):
+    # Rotary position embedding (RoFormer): the pair (x, y) of frequency theta_i
+    # at position t is the complex number x + iy times e^{i t theta_i}; numpy's
+    # complex exponential applies it, and the correction must give x + iy back
+    # (a correction that turned the other way, or paired other dims, fails)
+    cu_kv, cu_q, o = _rope_problem([300, 1], [300, 1], d=16)
+    d_rope, base = 8, 500.0
+    t = np.concatenate([np.arange(300), [0]]).astype(np.float64)
+    theta = base ** (-2.0 * np.arange(d_rope // 2) / d_rope)
+    z = o[:, :, 16 - d_rope::2] + 1j * o[:, :, 16 - d_rope + 1::2]
+    zr = z * np.exp(1j * t[:, None, None] * theta[None, None, :])
+    fwd = o.copy()
+    fwd[:, :, 16 - d_rope::2], fwd[:, :, 16 - d_rope + 1::2] = zr.real, zr.imag
+    assert np.allclose(orc.inverse_rope(cu_kv, cu_q, fwd, d_rope, base), o, atol=1e-12)
+
+
+def test_inverse_rope_composes_over_positions(orc):
+    # the correction for position a followed by that for b is the one for
+    # a + b: the angle is linear in the query position t = L - n_q + i
+    rng = np.random.default_rng(71)
+    o = rng.standard_normal((1, 2, 12))
+    one = lambda L, x: orc.inverse_rope(np.array([0, L]), np.array([0, 1]), x, 12, 10000.0)
+    for a, b in ((3, 5), (100, 1), (4095, 4096), (70000, 12345)):
+        assert np.allclose(one(b + 1, one(a + 1, o)), one(a + b + 1, o), atol=1e-9), (a, b)
