@@ -31,11 +31,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "CSA+HCA attention tokens/s at 64K–1M ctx; % of HBM / tensor-core roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-EXTRA_WORKLOADS = ("prefill_128k", "ragged_decode", "decode_1m", "swa_prefill_32k")
+EXTRA_WORKLOADS = ("prefill_128k", "ragged_decode", "decode_1m", "swa_prefill_32k", "inverse_rope_32k")
 # sliding-window attention over the raw tokens, measured as a call of its own
 # (not part of the hybrid step): one 32768-token prefill, the 128K prefill's
 # heads and width, and the 4096-token window of the SWA page's example
 SWA_PREFILL = {"name": "swa_prefill_32k", "length": 32768, "H": 64, "d": 512, "window": 4096, "seed": 7}
+# the inverse-RoPE correction of an attention output, as a call of its own:
+# the output of that 32768-token prefill, the last 64 of each head's 512 dims
+ROPE_CFG = {"name": "inverse_rope_32k", "length": 32768, "H": 64, "d": 512, "d_rope": 64, "base": 10000.0,
+            "seed": 8}
 
 # DRAM traffic per call of the dominant call from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum over the call's kernels),
@@ -670,6 +674,70 @@ def measure_swa(args, dev, peaks, peak_src, world, cfg=SWA_PREFILL):
             "clocks": clocks, "unit": "tokens/s", "config": conf, "calls_us": {"swa_attend": ms * 1e3}}
 
 
+def rope_bytes(total_q, H, d_rope):
+    """Algorithmic bytes of the in-place inverse-RoPE correction: each query's
+    rope slice of every head read and written once (bf16)."""
+    return 2 * total_q * H * d_rope * 2
+
+
+def measure_rope(args, dev, peaks, peak_src, world, cfg=ROPE_CFG):
+    """csa_inverse_rope alone on a prefill-sized output: CUDA graph of
+    back-to-back calls over rotating copies of the output (their slices exceed
+    L2), CUDA events on the capturing stream."""
+    import torch
+    from compressed_sparse_attention_21_b300 import _lib as csa
+    from compressed_sparse_attention_21_b300 import workloads as wl
+
+    L, H, d, dr = cfg["length"], cfg["H"], cfg["d"], cfg["d_rope"]
+    x = wl.randn(cfg["seed"], 0, (L, H, d), std=1.0).to(dev)
+    outs = [x] + [x.clone() for _ in range(2)]   # 3 x 268 MB of rope slices per rotation
+    layout = csa.Layout([L], [L], 4, 128, device=dev)
+    call = lambda o: csa.inverse_rope(layout, o, dr, cfg["base"])
+    for _ in range(max(args.warmup, 3)):
+        for o in outs:
+            call(o)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for o in outs:
+            call(o)
+    g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(int(dev.index or 0))
+    sampler.start()
+    time.sleep(0.3)
+    reps = []
+    t_start = time.perf_counter()
+    while True:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(10):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        reps.append(max_over_ranks(e0.elapsed_time(e1), dev) / (10 * len(outs)))
+        if time.perf_counter() - t_start >= min(args.min_seconds, 1.0) and len(reps) >= 3:
+            break
+    clocks = sampler.stop()
+    if csa.check_device_error() != 0:
+        raise RuntimeError("device error word set during the inverse-RoPE measurement")
+    ms = statistics.median(reps)
+    nb = rope_bytes(L, H, dr)
+    achieved = nb / (ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": "inverse_rope", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "peak_source": f"hbm_gbs ({peak_src})", "alg_bytes_per_launch": nb,
+            "avg_us": ms * 1e3, "traffic": None}
+    conf = {"workload": cfg["name"], "batch": 1, "ctx": L, "queries_per_seq": "all positions", "H": H, "d": d,
+            "d_rope": dr, "base": cfg["base"], "seed": cfg["seed"],
+            "l2": f"{len(outs)} rotating outputs, {len(outs) * nb / 2 / 2**20:.0f} MiB of rope slices vs 126 MB L2"}
+    n_outs = len(outs)
+    del x, outs, g
+    torch.cuda.empty_cache()
+    return {"value": job_value(L, world, ms), "ms_per_step": ms, "steps": 10 * n_outs * len(reps),
+            "roofline": roof, "clocks": clocks, "unit": "tokens/s", "config": conf,
+            "calls_us": {"inverse_rope": ms * 1e3}}
+
+
 def measure_e2e(copies, p, args, world, dev, tokens_per_step, ncopies):
     """The same metric through the C ABI with host buffers: every step copies its
     queries in from pinned host memory and both outputs and LSEs out.
@@ -800,6 +868,9 @@ def main(argv=None):
         for name in [x for x in args.extra.split(",") if x and x != w.name]:
             if name == SWA_PREFILL["name"]:
                 extra[name] = measure_swa(args, dev, peaks, peak_src, world)
+                continue
+            if name == ROPE_CFG["name"]:
+                extra[name] = measure_rope(args, dev, peaks, peak_src, world)
                 continue
             r = measure(wl.WORKLOADS[name], args, dev, peaks, peak_src, world, rank, local, headline=False)
             extra[name] = {k: r[k] for k in ("value", "ms_per_step", "steps", "roofline", "step_roofline", "clocks",

@@ -54,7 +54,7 @@ EXPORTS = ("csa_compress", "hca_compress", "lightning_index_topk", "csa_index_wo
            "lightning_index_topk_fp8",
            "csa_index_fp8_workspace_size",
            "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size", "swa_attend",
-           "swa_workspace_size", "hybrid_attend",
+           "swa_workspace_size", "csa_inverse_rope", "hybrid_attend",
            "csa_workspace_size", "csa_workspace_init", "csa_status_string", "csa_check_device_error",
            "csa_version", "csa_timing_enable", "csa_timing_read", "csa_timing_reset")
 
@@ -84,6 +84,7 @@ def load():
     lib.csa_attend_workspace_size.argtypes = [LP, I, I, I, I, ctypes.POINTER(Z)]
     lib.swa_attend.argtypes = [LP, P, P, I, I, I, F, P, P, P, Z, P]
     lib.swa_workspace_size.argtypes = [LP, I, I, I, ctypes.POINTER(Z)]
+    lib.csa_inverse_rope.argtypes = [LP, P, I, I, I, F, P]
     lib.hybrid_attend.argtypes = [ctypes.POINTER(csa_hybrid_params), P]
     lib.csa_workspace_size.argtypes = [ctypes.POINTER(csa_hybrid_params), ctypes.POINTER(Z)]
     lib.csa_workspace_init.argtypes = [P, Z, P]
@@ -99,7 +100,7 @@ def load():
     for f in ("csa_compress", "hca_compress", "lightning_index_topk", "csa_index_workspace_size",
               "lightning_index_topk_static", "csa_quantize_index_keys", "csa_quantize_index_keys_closed",
               "lightning_index_topk_fp8", "csa_index_fp8_workspace_size", "sparse_mqa_attend", "hca_dense_attend", "csa_attend_workspace_size",
-              "swa_attend", "swa_workspace_size", "hybrid_attend",
+              "swa_attend", "swa_workspace_size", "csa_inverse_rope", "hybrid_attend",
               "csa_workspace_size", "csa_workspace_init", "csa_check_device_error", "csa_timing_enable"):
         getattr(lib, f).restype = I
     _lib = lib
@@ -346,6 +347,16 @@ def swa_attend(layout, q, kv, window, scale, out=None, lse=None, ws=None, stream
     _check(load().swa_attend(ctypes.byref(layout.c), _ptr(q), _ptr(kv), H, d, int(window), float(scale), _ptr(out),
                              _ptr(lse), _ptr(ws), nb, _stream(stream)), "swa_attend")
     return out, lse
+
+
+def inverse_rope(layout, out, d_rope, base=10000.0, stream=None):
+    """Inverse-RoPE correction of an attention output [total_q, H, d] in place:
+    each query's last d_rope dims of every head, pairs (2i, 2i+1), turned by
+    -t * base^(-2i/d_rope) for the query's position t."""
+    H, d = out.shape[-2], out.shape[-1]
+    _check(load().csa_inverse_rope(ctypes.byref(layout.c), _ptr(out), H, d, int(d_rope), float(base),
+                                   _stream(stream)), "csa_inverse_rope")
+    return out
 
 
 class Hybrid:

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <memory>
@@ -622,6 +623,30 @@ csa_status_t swa_attend(const csa_layout *layout, const csa_bf16 *q, const csa_b
     return from_cuda(launch_attend(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+csa_status_t csa_inverse_rope(const csa_layout *layout, csa_bf16 *out, int n_heads, int d, int d_rope, float base,
+                              csa_stream_t stream)
+{
+    CSA_TRY(check_layout(layout, false, false));
+    if (n_heads <= 0 || !(base > 0.f) || !std::isfinite(base)) return CSA_ERR_INVALID_ARG;
+    if (!inverse_rope_supported(d, d_rope)) return CSA_ERR_UNSUPPORTED;
+    CSA_TRY(check_ptr(out, layout->total_q > 0));
+    DeviceState *ds = nullptr;
+    CSA_TRY(device_state(&ds));
+    RopeArgs a;
+    a.batch = layout->batch;
+    a.total_q = layout->total_q;
+    a.cu_kv = layout->cu_kv;
+    a.cu_q = layout->cu_q;
+    a.n_heads = n_heads;
+    a.d = d;
+    a.d_rope = d_rope;
+    a.base = (double)base;
+    a.out = reinterpret_cast<uint16_t *>(out);
+    a.err = ds->err;
+    a.num_sms = ds->num_sms;
+    return from_cuda(launch_inverse_rope(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 csa_status_t csa_workspace_size(const csa_hybrid_params *p, size_t *bytes)
 {
     if (!p || !bytes) return CSA_ERR_INVALID_ARG;
@@ -801,7 +826,7 @@ csa_status_t csa_check_device_error(csa_stream_t stream, csa_status_t *device_st
     return CSA_OK;
 }
 
-int csa_version(void) { return 120; }   // 1.1: FP8 indexer keys (.1: the closed-rows quantiser); 1.2: swa_attend
+int csa_version(void) { return 130; }   // 1.1: FP8 indexer keys (.1: the closed-rows quantiser); 1.2: swa_attend; 1.3: csa_inverse_rope
 
 csa_status_t csa_timing_enable(int enable)
 {

@@ -101,6 +101,20 @@ struct CompressArgs {
 bool compress_supported(int d, int ratio_small, int ratio_big);
 cudaError_t launch_compress(const CompressArgs &a, cudaStream_t st);
 
+// ---- inverse rotary correction of attention outputs ----
+struct RopeArgs {
+    int batch;
+    int64_t total_q;
+    const int64_t *cu_kv, *cu_q;
+    int n_heads, d, d_rope;
+    double base;
+    uint16_t *out;   // [total_q, n_heads, d], corrected in place
+    int *err;
+    int num_sms;
+};
+bool inverse_rope_supported(int d, int d_rope);
+cudaError_t launch_inverse_rope(const RopeArgs &a, cudaStream_t st);
+
 // ---- indexer + top-k ----
 struct IndexArgs {
     int batch;

@@ -321,6 +321,28 @@ csa_status_t swa_workspace_size(const csa_layout *layout, int n_heads, int d, in
                                 size_t *bytes);
 
 /* ---------------------------------------------------------------------------
+ * Inverse-RoPE correction of an attention output ("DeepSeek V4's
+ * architecture debt chain", Constraint 1 -> Innovation 1: the compressed
+ * entries carry no per-token position, so the attention output is corrected
+ * by an inverse rotary embedding).  The pages fix no convention; readings:
+ * the last d_rope dims of each head turn, paired as (2i, 2i+1) within that
+ * slice, pair i at theta_i = base^(-2i/d_rope), and the output row of the
+ * query at position t (of its sequence, from cu_kv / cu_q) turns by
+ * -t * theta_i:
+ *     (x, y) -> (x cos phi + y sin phi, -x sin phi + y cos phi),  phi = t theta_i
+ * in fp32 with the angle reduced modulo 2 pi in double precision, rounded to
+ * bf16 once; every other dim is left as it is.
+ *   out    [total_q, n_heads, d] bf16, corrected in place (any attention
+ *          output of this library, e.g. o_hca)
+ *   d % 8 == 0; d_rope % 8 == 0, 8 <= d_rope <= min(d, 512) (else
+ *   CSA_ERR_UNSUPPORTED); base > 0 and finite, n_heads >= 1 (else
+ *   CSA_ERR_INVALID_ARG).  No workspace.  Only cu_kv and cu_q of the layout
+ *   are read.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_inverse_rope(const csa_layout *layout, csa_bf16 *out, int n_heads, int d, int d_rope,
+                              float base, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Hybrid step (§2.3: CSA and HCA layers alternate): runs, on the same
  * inputs, compression into both caches (unless CSA_SKIP_COMPRESS), then the
  * CSA branch (indexer, top-k, sparse attention) and the HCA branch (dense

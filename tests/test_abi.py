@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.csa_version() == 120
+    assert lib.csa_version() == 130
     assert lib.csa_status_string(0) == b"ok"
     assert lib.csa_status_string(3) == b"workspace missing or too small"
 
@@ -176,3 +176,19 @@ def test_swa_arguments_checked_on_host(lib):
     for bad in BAD_LAYOUTS:
         B = layout(**bad)
         assert lib.swa_attend(ctypes.byref(B), 256, 256, 8, 128, 64, 1.0, 256, None, None, 0, None) == 1, bad
+
+
+def test_inverse_rope_arguments_checked_on_host(lib):
+    L = layout(cu_csa=None, cu_hca=None)
+    assert lib.csa_inverse_rope(ctypes.byref(L), 256, 8, 128, 12, 10000.0, None) == 2     # d_rope not a multiple of 8
+    assert lib.csa_inverse_rope(ctypes.byref(L), 256, 8, 128, 136, 10000.0, None) == 2    # d_rope > d
+    assert lib.csa_inverse_rope(ctypes.byref(L), 256, 8, 100, 64, 10000.0, None) == 2     # d not a multiple of 8
+    assert lib.csa_inverse_rope(ctypes.byref(L), 256, 8, 1024, 1024, 10000.0, None) == 2  # d_rope > 512
+    assert lib.csa_inverse_rope(ctypes.byref(L), 256, 0, 128, 64, 10000.0, None) == 1     # heads
+    assert lib.csa_inverse_rope(ctypes.byref(L), 256, 8, 128, 64, 0.0, None) == 1         # base
+    assert lib.csa_inverse_rope(ctypes.byref(L), 256, 8, 128, 64, float("inf"), None) == 1
+    assert lib.csa_inverse_rope(ctypes.byref(L), None, 8, 128, 64, 10000.0, None) == 1    # out
+    assert lib.csa_inverse_rope(ctypes.byref(L), 264, 8, 128, 64, 10000.0, None) == 1     # misaligned
+    for bad in BAD_LAYOUTS:
+        B = layout(**bad)
+        assert lib.csa_inverse_rope(ctypes.byref(B), 256, 8, 128, 64, 10000.0, None) == 1, bad

@@ -70,3 +70,7 @@ def test_swa_flops_closed_form_equals_the_per_position_count():
                             ([4097, 10], [4097, 1], 4096), ([50], [50], 1000), ([1], [1], 1)):
         per_pos = sum(min(t + 1, w) for L, nq in zip(lengths, n_q) for t in range(L - nq, L))
         assert _bench().swa_flops(lengths, n_q, 2, 3, w) == 4 * 2 * 3 * per_pos
+
+
+def test_rope_bytes_count_the_rope_slices_read_and_written():
+    assert _bench().rope_bytes(32768, 64, 64) == 2 * 32768 * 64 * 64 * 2

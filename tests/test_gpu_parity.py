@@ -482,6 +482,58 @@ def test_swa_chunked_and_decode_layouts_without_queries():
 
 
 # ---------------------------------------------------------------------------
+# f3: inverse-RoPE correction of the attention output
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("H,d,d_rope", [(1, 128, 8), (8, 128, 64), (8, 128, 128), (64, 512, 64), (128, 512, 512)])
+@pytest.mark.parametrize("base", [10000.0, 500.0])
+def test_inverse_rope_parity(H, d, d_rope, base):
+    # prefill, decode, chunked and query-free sequences, and one decode query
+    # at position 2^20 - 1 (angles up to 2^20 radians)
+    lengths, n_q = [300, 1 << 20, 50, 9, 4000], [300, 1, 0, 9, 17]
+    layout = csa.Layout(lengths, n_q, 4, 128, device="cuda")
+    rng = np.random.default_rng(H + d_rope)
+    x = torch.from_numpy(rng.standard_normal((layout.total_q, H, d)).astype(np.float32)).to(torch.bfloat16)
+    out = x.cuda()
+    csa.inverse_rope(layout, out, d_rope, base)
+    torch.cuda.synchronize()
+    assert csa.check_device_error() == 0
+    got = P.bf16_to_f64(out)
+    xin = P.bf16_to_f64(x)
+    ref = oracle.inverse_rope(np.array(layout.host["cu_kv"]), np.array(layout.host["cu_q"]), xin, d_rope, base)
+    assert np.array_equal(got[:, :, :d - d_rope], xin[:, :, :d - d_rope])   # untouched dims, bit for bit
+    pair = np.repeat(np.maximum(np.abs(xin[:, :, d - d_rope::2]), np.abs(xin[:, :, d - d_rope + 1::2])), 2, axis=-1)
+    err = np.abs(got[:, :, d - d_rope:] - ref[:, :, d - d_rope:])
+    # one bf16 rounding (half a bf16 spacing) of an fp32 rotation with fp32 sine and cosine
+    bound = P.half_ulp_bf16(ref[:, :, d - d_rope:]) * 1.001 + 2.0 ** -20 * pair
+    assert (err <= bound).all(), (err - bound).max()
+
+
+def test_inverse_rope_bench_config_sampled():
+    # the call exactly as bench.py times it (a 32768-token prefill's output, 64
+    # heads, d = 512, d_rope = 64, its seeded input), checked on sampled rows:
+    # each sampled query as a one-query sequence ending at its position
+    import bench
+    cfg = bench.ROPE_CFG
+    L, H, d, dr = cfg["length"], cfg["H"], cfg["d"], cfg["d_rope"]
+    x = wl.randn(cfg["seed"], 0, (L, H, d), std=1.0)
+    out = x.cuda()
+    csa.inverse_rope(csa.Layout([L], [L], 4, 128, device="cuda"), out, dr, cfg["base"])
+    torch.cuda.synchronize()
+    assert csa.check_device_error() == 0
+    rows = np.unique(np.concatenate([[0, 1, 2, 4095, L - 1], np.random.default_rng(4).integers(0, L, 40)]))
+    cu_kv = np.concatenate([[0], np.cumsum(rows + 1)]).astype(np.int64)
+    cu_q = np.arange(len(rows) + 1, dtype=np.int64)
+    xin = P.bf16_to_f64(x[torch.from_numpy(rows)])
+    ref = oracle.inverse_rope(cu_kv, cu_q, xin, dr, cfg["base"])
+    got = P.bf16_to_f64(out[torch.from_numpy(rows).cuda()])
+    pair = np.repeat(np.maximum(np.abs(xin[:, :, d - dr::2]), np.abs(xin[:, :, d - dr + 1::2])), 2, axis=-1)
+    assert np.array_equal(got[:, :, :d - dr], xin[:, :, :d - dr])
+    err = np.abs(got[:, :, d - dr:] - ref[:, :, d - dr:])
+    bound = P.half_ulp_bf16(ref[:, :, d - dr:]) * 1.001 + 2.0 ** -20 * pair
+    assert (err <= bound).all(), (err - bound).max()
+
+
+# ---------------------------------------------------------------------------
 # a6: the hybrid step
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("case", ["prefill_small", "decode_small", "chunked"])
