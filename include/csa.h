@@ -15,7 +15,10 @@
  *        across layers.
  * and "DeepSeek V4's architecture debt chain" (vendordeep.com),
  * "Constraint 1 -> Innovation 1" (many tokens' KV weighted into one
- * compressed token at up to 128x).
+ * compressed token at up to 128x; the "reverse RoPE" correction of the
+ * attention output: csa_inverse_rope).  Sliding-window attention over the
+ * raw tokens (swa_attend) follows §3.2 "SWA sliding-window attention" of the
+ * bjdmk.com.cn DeepSeek-V4 walkthrough.
  *
  * Where the pages leave a step open this library takes these readings:
  *   - one scalar gate logit per token; the weights of a block are the
