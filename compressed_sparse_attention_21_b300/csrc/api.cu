@@ -170,6 +170,7 @@ IndexArgs index_args(const csa_layout *L, const csa_bf16 *q_idx, const csa_bf16 
                      int top_k, int32_t *idx_out, float *score_out, void *ws, size_t ws_bytes, int *err)
 {
     IndexArgs a;
+    a.compress = nullptr;
     a.batch = L->batch;
     a.max_kv_len = L->max_kv_len;
     a.max_q_len = L->max_q_len;
@@ -709,40 +710,41 @@ csa_status_t hybrid_attend(const csa_hybrid_params *p, csa_stream_t stream_)
         if (cudaStreamWaitEvent(hp->aux, hp->fork, 0) != cudaSuccess) return CSA_ERR_CUDA;
     }
 
-    // a1: compression of the blocks closed by this call's query positions
+    // a1: compression of the blocks closed by this call's query positions.  The
+    // fused kernel runs inside the index call (after the key scan on the
+    // key-scan paths, ahead of the indexer otherwise); the fallback runs first.
     csa_status_t s_c = CSA_OK;
-    if (compress) {
-        CompressArgs a;
-        std::memset(&a, 0, sizeof a);
-        a.batch = L->batch;
-        a.max_kv_len = L->max_kv_len;
-        a.max_q_len = L->max_q_len;
-        a.cu_kv = L->cu_kv;
-        a.cu_q = L->cu_q;
-        a.d = p->d;
-        a.kv = p->kv;
-        a.gate = p->gate;
-        a.err = ds->err;
-        if (compress_supported(p->d, p->ratio_csa, p->ratio_hca)) {
-            a.ratio_small = p->ratio_csa;
-            a.cu_small = L->cu_csa;
-            a.out_small = p->csa_cache;
-            a.ratio_big = p->ratio_hca;
-            a.cu_big = L->cu_hca;
-            a.out_big = p->hca_cache;
-            s_c = from_cuda(launch_compress(a, st));
-        } else {
-            s_c = compress_impl(L, true, p->kv, p->gate, p->d, p->ratio_csa, p->csa_cache, st);
-            if (s_c == CSA_OK) s_c = compress_impl(L, false, p->kv, p->gate, p->d, p->ratio_hca, p->hca_cache, st);
-        }
+    CompressArgs ca;
+    std::memset(&ca, 0, sizeof ca);
+    const bool fused = compress && compress_supported(p->d, p->ratio_csa, p->ratio_hca);
+    if (fused) {
+        ca.batch = L->batch;
+        ca.max_kv_len = L->max_kv_len;
+        ca.max_q_len = L->max_q_len;
+        ca.cu_kv = L->cu_kv;
+        ca.cu_q = L->cu_q;
+        ca.d = p->d;
+        ca.kv = p->kv;
+        ca.gate = p->gate;
+        ca.err = ds->err;
+        ca.ratio_small = p->ratio_csa;
+        ca.cu_small = L->cu_csa;
+        ca.out_small = p->csa_cache;
+        ca.ratio_big = p->ratio_hca;
+        ca.cu_big = L->cu_hca;
+        ca.out_big = p->hca_cache;
+    } else if (compress) {
+        s_c = compress_impl(L, true, p->kv, p->gate, p->d, p->ratio_csa, p->csa_cache, st);
+        if (s_c == CSA_OK) s_c = compress_impl(L, false, p->kv, p->gate, p->d, p->ratio_hca, p->hca_cache, st);
     }
 
-    // a2 + a3 (records sdone once every key is scored)
+    // a2 + a3 (records sdone once every key is scored and the compression is done)
     if (s_c == CSA_OK) {
         IndexArgs ia = index_args(L, p->q_idx, p->k_idx, p->n_heads_idx, p->d_idx, p->ratio_csa, p->top_k,
                                   p->idx_out, p->score_out, w_idx ? ws : nullptr, w_idx, ds->err);
         ia.scan_done = hp ? hp->sdone : nullptr;
-        ia.pdl = compress;
+        ia.pdl = compress && !fused;   // behind the fallback compression
+        ia.compress = fused ? &ca : nullptr;
         if (fp8) {
             ia.fp8 = true;
             ia.k_fp8 = p->k_idx_fp8;

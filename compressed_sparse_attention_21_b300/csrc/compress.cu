@@ -24,11 +24,11 @@ constexpr int kSpan = 128;
 constexpr int kSliceCols = 128;   // columns per CTA (a d = 512 row is split over 4 CTAs)
 
 template <int D, int MS, int MB>
-__global__ void __launch_bounds__(kCompressThreads)
-compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
-                const int64_t *__restrict__ cu_s, const int64_t *__restrict__ cu_b, int batch,
-                const uint16_t *__restrict__ kv, const float *__restrict__ gate,
-                uint16_t *__restrict__ out_s, uint16_t *__restrict__ out_b, int *err)
+__device__ __forceinline__ void compress_body(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                                              const int64_t *__restrict__ cu_s, const int64_t *__restrict__ cu_b,
+                                              int batch, const uint16_t *__restrict__ kv,
+                                              const float *__restrict__ gate, uint16_t *__restrict__ out_s,
+                                              uint16_t *__restrict__ out_b, int *err)
 {
     constexpr int CS = D < kSliceCols ? D : kSliceCols;   // columns of this CTA's slice
     constexpr int G = CS / 8;                      // 16-byte column groups per slice row
@@ -208,6 +208,21 @@ compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ c
     }
 }
 
+// Launched behind another kernel of the same call (CompressArgs::pdl), this
+// grid reads nothing that kernel writes, but every CTA waits for it before
+// exiting, whatever path it took: whatever waits for this grid may rely on the
+// earlier one too.
+template <int D, int MS, int MB>
+__global__ void __launch_bounds__(kCompressThreads)
+compress_kernel(const int64_t *__restrict__ cu_kv, const int64_t *__restrict__ cu_q,
+                const int64_t *__restrict__ cu_s, const int64_t *__restrict__ cu_b, int batch,
+                const uint16_t *__restrict__ kv, const float *__restrict__ gate,
+                uint16_t *__restrict__ out_s, uint16_t *__restrict__ out_b, int *err)
+{
+    compress_body<D, MS, MB>(cu_kv, cu_q, cu_s, cu_b, batch, kv, gate, out_s, out_b, err);
+    griddep_wait();
+}
+
 template <int D, int MS, int MB>
 cudaError_t launch_compress_t(const CompressArgs &a, cudaStream_t st)
 {
@@ -219,7 +234,7 @@ cudaError_t launch_compress_t(const CompressArgs &a, cudaStream_t st)
     constexpr int slices = D / (D < kSliceCols ? D : kSliceCols);
     dim3 grid((unsigned)a.batch, (unsigned)spans, (unsigned)slices);
     return launch_kernel("compress", compress_kernel<D, MS, MB>, grid, dim3(kCompressThreads), 0,
-                         st, false, a.cu_kv, a.cu_q, a.cu_small, a.cu_big, a.batch, a.kv, a.gate,
+                         st, a.pdl, a.cu_kv, a.cu_q, a.cu_small, a.cu_big, a.batch, a.kv, a.gate,
                          a.out_small, a.out_big, a.err);
 }
 

@@ -1018,6 +1018,7 @@ index_select_kernel(int batch, const int64_t *__restrict__ cu_kv, const int64_t 
 }
 
 constexpr int64_t kSelMaxN = (int64_t)kSelCluster * 1024 * 32;   // longest row the select cluster holds (entries)
+constexpr int64_t kCompressBehindScan = 4096;   // scanned keys per SM that hide a fused compression
 
 bool use_cta_path(const IndexArgs &a)
 {
@@ -1060,15 +1061,34 @@ cudaError_t launch_select(const IndexArgs &a, int64_t max_n, int64_t q0, int64_t
 }
 
 template <int DI>
-cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
+cudaError_t launch_index_t(const IndexArgs &a_in, cudaStream_t st)
 {
+    IndexArgs a = a_in;
     if (a.total_q <= 0) return cudaSuccess;
     const int64_t max_n = a.max_kv_len / a.ratio;
     // scan_done: after the last key scan of the multi-kernel paths; the
     // single-kernel paths mark it up front (their kernel holds the GPU to the end)
     auto mark = [&]() -> cudaError_t { return a.scan_done ? cudaEventRecord(a.scan_done, st) : cudaSuccess; };
     const bool fp8 = a.fp8;   // FP8 keys: the chunk scan and the select only
-    if (!fp8 && (index_tc_applicable(a) || index_block_applicable(a) || use_cta_path(a))) {
+    const bool single = !fp8 && (index_tc_applicable(a) || index_block_applicable(a) || use_cta_path(a));
+    // A compression of the same call runs ahead of the indexer, except behind a
+    // chunk scan long enough to hide it (at least kCompressBehindScan keys per
+    // SM: measured, ragged decode 98.3 -> 94.7 us and 1M decode 69.0 -> 66.2 us,
+    // while a 64K decode's 11 us scan cannot hide it: 34.8 -> 36.9 us); there it
+    // starts after the first key scan, whose CTAs then hold every SM from the start.
+    const CompressArgs *comp = a.compress;
+    a.compress = nullptr;
+    const bool behind_scan = !single && max_n <= kSelMaxN &&
+                             a.total_q * max_n >= kCompressBehindScan * (int64_t)device_sms();
+    if (comp && !behind_scan) {
+        CompressArgs c = *comp;
+        c.pdl = false;
+        cudaError_t e = launch_compress(c, st);
+        if (e != cudaSuccess) return e;
+        a.pdl = true;
+        comp = nullptr;
+    }
+    if (single) {
         cudaError_t e = mark();
         if (e != cudaSuccess) return e;
     }
@@ -1110,6 +1130,14 @@ cudaError_t launch_index_t(const IndexArgs &a, cudaStream_t st)
                                         dim3(kScanThreads), (size_t)kScanStages * kChunkBytes, st, a.pdl, a.batch,
                                         a.cu_kv, a.cu_q, a.cu_csa, q0, a.q_idx, (const void *)a.k_idx, a.k_scale,
                                         a.n_heads_idx, a.ratio, (int)cpc, w, a.err);
+            if (e == cudaSuccess && comp) {
+                // the compression overlaps the key scan (it starts once every scan CTA
+                // has scored its first chunk) and completes only after it
+                CompressArgs c = *comp;
+                c.pdl = true;
+                e = launch_compress(c, st);
+                comp = nullptr;
+            }
             if (e == cudaSuccess && q0 + nq >= a.total_q) e = mark();
             if (e != cudaSuccess) return e;
             e = launch_select(a, max_n, q0, nq, w, st);

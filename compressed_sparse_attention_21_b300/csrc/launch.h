@@ -97,6 +97,7 @@ struct CompressArgs {
     const float *gate;
     uint16_t *out_small, *out_big;
     int *err;
+    bool pdl;   // may overlap the stream's previous kernel (and completes only after it)
 };
 bool compress_supported(int d, int ratio_small, int ratio_big);
 cudaError_t launch_compress(const CompressArgs &a, cudaStream_t st);
@@ -134,6 +135,12 @@ struct IndexArgs {
     void *ws;
     size_t ws_bytes;
     int *err;
+    // if set, the call also runs this compression (hybrid step): ahead of the
+    // indexer on the single-kernel paths; on the key-scan paths after the
+    // first key scan, overlapping it, and before the select (the scan reads no
+    // compressed entry; everything after the select needs them).  scan_done
+    // is then recorded after it too.
+    const CompressArgs *compress;
 };
 bool index_supported(int n_heads_idx, int d_idx, int top_k);
 // prefill-sized batches (index_block.cu): tensor-core score tiles, sampled
