@@ -40,6 +40,9 @@
  *       last d_rope of each head's d; P2 they pair as (2i, 2i+1) within that
  *       slice; P3 pair i turns at theta_i = base^(-2i/d_rope); P4 the output
  *       of the query at position t is turned by the angle -t * theta_i.
+ *       Parity partly unpinned: the pins fix the direction, the pairing
+ *       against the forward rotary embedding and the linearity in t, not
+ *       the readings P1-P3 themselves.
  *   W1  [SWA] the window of a token at position t holds positions
  *       max(0, t - w + 1) .. t: the token itself and the w - 1 before it.
  *   R8  the low-precision indexer stores each key row as FP8 E4M3 codes
