@@ -46,11 +46,11 @@ ROPE_CFG = {"name": "inverse_rope_32k", "length": 32768, "H": 64, "d": 512, "d_r
 # keyed by (workload, call, indexer key format), with the sha256 of the sources at capture time;
 # a changed source makes the figure stale and it is reported as null.
 NCU_TRAFFIC = {
-    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,599,104 B read and
-    # 0 B written + index_select_kernel 1,351,936 B read (means of two captured calls)
+    # ncu capture of the decode_64k indexer call: index_chunk_scan_kernel 33,600,256 B read and
+    # 0 B written + index_select_kernel 1,354,752 B read (means of two captured calls)
     ("decode_64k", "index_topk", "bf16"): {
-        "bytes_per_launch": 34951040,
-        "sources": {"indexer.cu": "a668ea15c26642081abc029685eea158803591854f74b7e03eda308977ae3a23",
+        "bytes_per_launch": 34955008,
+        "sources": {"indexer.cu": "f828009532c54521f3d1dd94c713f2f6257ef836e3719296be83a8f0835cb362",
                     "common.cuh": "b93a7dad1acde03c5b427f390c736715adf747f244ae8d972599ce95b5ac6ab8"},
     },
 }

@@ -599,7 +599,11 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
     constexpr int NWARP = kScanThreads / 32;
     extern __shared__ __align__(128) uint8_t s_rows[];  // kScanStages chunks
     __shared__ float s_q[DI];
-    __shared__ uint32_t s_hist[kHistBins];
+    // the CTA's histogram of the keys' top 12 bits, two 16-bit counts per word
+    // (bins 2i, 2i + 1): at most cpc x ROWS <= 65535 keys per CTA (the launcher
+    // bounds cpc), and half the shared memory lets a CTA of the step's
+    // compression stay on the SM beside two scan CTAs
+    __shared__ uint32_t s_hist[kHistBins / 2];
     __shared__ __align__(8) uint64_t s_bar[kScanStages];
 
     const int tid = threadIdx.x;
@@ -628,7 +632,7 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
         fence_mbar_init();
         for (int c = 0; c < nchunks && c < kScanStages; c++) issue(c);
     }
-    for (int i = tid; i < kHistBins; i += kScanThreads) s_hist[i] = 0;
+    for (int i = tid; i < kHistBins / 2; i += kScanThreads) s_hist[i] = 0;
     load_qsum<DI>(qI, qi, HI, s_q);
     __syncthreads();
     const int lane = tid & 31, warp = tid >> 5;
@@ -716,7 +720,8 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
             const uint32_t key = score_key(FP8 ? a[j] * sc_cur[j] : a[j]);
             if (emits && row < rows) {
                 kc[row] = key;
-                atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);
+                const uint32_t bin = key >> (32 - kHistBits);
+                atomicAdd(&s_hist[bin >> 1], (bin & 1u) ? 0x10000u : 1u);
             }
         }
         if constexpr (FP8) {
@@ -738,9 +743,10 @@ index_chunk_scan_kernel(int batch, const int64_t *__restrict__ cu_kv, const int6
         if (c == 0) griddep_launch();
     }
     uint32_t *ghist = w.hist + qg * kHistBins;
-    for (int i = tid; i < kHistBins; i += kScanThreads) {
-        const uint32_t cnt = s_hist[i];
-        if (cnt) atomicAdd(ghist + i, cnt);
+    for (int i = tid; i < kHistBins / 2; i += kScanThreads) {
+        const uint32_t pair = s_hist[i];
+        if (pair & 0xffffu) atomicAdd(ghist + 2 * i, pair & 0xffffu);
+        if (pair >> 16) atomicAdd(ghist + 2 * i + 1, pair >> 16);
     }
     // Launched behind another kernel (IndexArgs::pdl), this grid reads nothing
     // that kernel writes, but completes only after it: whatever waits for this
@@ -1118,6 +1124,7 @@ cudaError_t launch_index_t(const IndexArgs &a_in, cudaStream_t st)
         for (int64_t q0 = 0; q0 < a.total_q; q0 += gq) {
             const int64_t nq = a.total_q - q0 < gq ? a.total_q - q0 : gq;
             int64_t cpc = (nq * nch + slots - 1) / slots;
+            if (cpc > 65535 / ROWS) cpc = 65535 / ROWS;   // the scan's 16-bit per-CTA bin counts
             if (cpc < 1) cpc = 1;
             if (cpc > nch) cpc = nch;
             const int64_t gx = (nch + cpc - 1) / cpc;
